@@ -1,0 +1,141 @@
+/*
+ * gbattn.h -- C ABI of the GB300 streaming-attention library (libgbattn.so).
+ *
+ * The library computes the fused streaming attention forward
+ *     O = softmax(scale * Q K^T + mask) V
+ * without materialising the score or probability matrix: Q is tiled, K/V tiles stream
+ * through on-chip memory and an online-softmax running state (m, l) rescales the output
+ * accumulator.
+ *   Definition: "AttentionRegion Transformation - Deriving FlashAttention via
+ *   Memory-Centric Compilation in AICF", section 3 (MatMul(Q, K^T) -> Mask -> Softmax ->
+ *   MatMul(P, V)), section 6 (streaming region, online update of m and l), section 8
+ *   (kernel lowering: Q-tile outer loop, KV-tile inner loop, score never materialised).
+ *   Per-tile operation sequence, GQA stacking, split-KV decode and the log-sum-exp merge:
+ *   "ADR-0060: AHBM GQA Fused Attention Kernel (Llama3-70B)", sections 3, 4, 5.2, 5.4.
+ *   I/O contract (post-RoPE Q and K/V cache in, O out, no S or P out, KV cache read only):
+ *   the same ADR, section 0.5.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers named q, k, v, kcache, vcache, o, lse, kv_lens, workspace are DEVICE
+ *    pointers (CUDA global memory of the current device).  The caller allocates and owns
+ *    every buffer; the library allocates no device memory per call.
+ *  - Layouts are contiguous row-major "BHSD": Q and O [B, Hq, Sq, d], K and V
+ *    [B, Hkv, Skv, d], LSE [B, Hq, Sq].  Grouped-query attention: query head h reads
+ *    KV head h / (Hq / Hkv).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream).  Errors that the host can detect are returned before anything is launched.
+ *  - LSE is the natural log of sum_j exp(scale * q . k_j) over the visible keys, fp32.
+ *  - A row that sees no key (a decode sequence of length 0) gets O = 0, LSE = -inf.
+ *  - Causal masking is bottom-right aligned: query i sits at key position i + Skv - Sq and
+ *    sees keys j <= i + Skv - Sq.
+ *  - Numerics: bf16 inputs, fp32 scores / running state / accumulators, P rounded to
+ *    bf16 for the P.V product, O stored in the input dtype.
+ */
+#ifndef GBATTN_H
+#define GBATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of Q, K, V and O. */
+typedef enum {
+    GBATTN_BF16 = 0, /* bf16 storage; tcgen05 tensor-core path (d = 64 or 128) */
+    GBATTN_FP32 = 1  /* fp32 storage; exact fp32 CUDA-core path (d = 64 or 128) */
+} gbattn_dtype_t;
+
+/* Status codes (0 = success, negative = error). */
+enum {
+    GBATTN_OK = 0,
+    GBATTN_ERR_INVALID_ARG = -1,    /* null pointer, non-positive size, Hq % Hkv != 0, ... */
+    GBATTN_ERR_UNSUPPORTED = -2,    /* d not in {64,128}, dtype/path combination, causal with Sq > Skv */
+    GBATTN_ERR_MISALIGNED = -3,     /* a pointer is not 16-byte aligned */
+    GBATTN_ERR_CUDA = -4,           /* a CUDA runtime/driver call or launch failed */
+    GBATTN_ERR_TIMEOUT = -5,        /* a device-side bounded wait expired (see attn_last_device_error) */
+    GBATTN_ERR_WORKSPACE = -6,      /* workspace null or smaller than attn_decode_workspace_size() */
+    GBATTN_ERR_TOO_LARGE = -7       /* a size exceeds what the kernels index (e.g. > 2^31 rows) */
+};
+
+/*
+ * attn_fwd -- prefill / general attention forward.
+ *
+ *   q   [B, Hq, Sq, d]  device, dtype        post-RoPE queries
+ *   k   [B, Hkv, Skv, d] device, dtype       post-RoPE keys
+ *   v   [B, Hkv, Skv, d] device, dtype       values
+ *   o   [B, Hq, Sq, d]  device, dtype        output (written)
+ *   lse [B, Hq, Sq]     device, fp32         log-sum-exp per row (written); may be NULL
+ *   scale                                    softmax scale (typically 1/sqrt(d))
+ *   causal                                   0 = full attention, 1 = bottom-right causal
+ *   dtype                                    GBATTN_BF16 or GBATTN_FP32
+ *   stream                                   cudaStream_t
+ *
+ * Requirements: B, Hq, Hkv, Sq, Skv >= 1; Hq % Hkv == 0; d in {64, 128};
+ * causal requires Sq <= Skv; all pointers 16-byte aligned.
+ * Tile classes follow "ADR-0060" section 5.4: KV tiles entirely in a query tile's future
+ * are skipped, tiles crossing the diagonal are masked, the rest run unmasked.
+ * Returns GBATTN_OK or a negative status; nothing is launched on error.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int Sq, int Skv, int d, float scale, int causal, int dtype,
+             void* stream);
+
+/*
+ * attn_decode_workspace_size -- bytes of device workspace attn_decode_splitkv needs.
+ * Holds the per-split partial results (lse_s and O_s / l_s, fp32) and a work counter.
+ * num_splits > 0: fixed split count; 0: automatic (one split per 4096 keys).
+ * Returns 0 for invalid arguments.
+ */
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int num_splits);
+
+/*
+ * attn_decode_splitkv -- single-token (T_q = 1) decode against a KV cache, split-KV with a
+ * log-sum-exp merge ("ADR-0060" section 4 merge and section 5.2/5.3 decode).
+ *
+ *   q       [B, Hq, 1, d]       device, bf16    the step's post-RoPE queries
+ *   kcache  [B, Hkv, Lmax, d]   device, bf16    key cache (read only; rows >= kv_lens[b] never read)
+ *   vcache  [B, Hkv, Lmax, d]   device, bf16    value cache (read only)
+ *   kv_lens [B]                 device, int32   valid keys per sequence, 0 <= kv_lens[b] <= Lmax
+ *   o       [B, Hq, 1, d]       device, bf16    output (written)
+ *   lse     [B, Hq]             device, fp32    log-sum-exp (written); may be NULL
+ *   num_splits                                  > 0 fixed splits per sequence (<= 256),
+ *                                               0 = automatic per sequence length
+ *   workspace, ws_bytes                         device scratch of at least
+ *                                               attn_decode_workspace_size(...) bytes,
+ *                                               owned by the caller; calls that share a
+ *                                               workspace must be ordered on one stream
+ *
+ * Sequence b's keys [0, kv_lens[b]) are cut into contiguous splits of C keys,
+ * C = ceil(len / n) rounded up to 64 ("ADR-0060" section 2.1: contiguous blocks); each
+ * split streams its chunk once for all G = Hq / Hkv query heads of a KV head (the heads
+ * are stacked into one MMA operand, "ADR-0060" section 5.2), and a combine kernel merges
+ * the partial (lse_s, O_s) of the splits.  kv_lens values are read on the device; values
+ * outside [0, Lmax] are clamped into it.
+ * Requirements: d = 128 or 64, G <= 8 per launch group (larger G runs several groups),
+ * all pointers 16-byte aligned.  Returns GBATTN_OK or a negative status.
+ */
+int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
+                        const int* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Lmax, int d, float scale, int num_splits, void* workspace,
+                        size_t ws_bytes, void* stream);
+
+/*
+ * attn_last_device_error -- synchronise `stream`, then read and clear the device error
+ * word that bounded waits inside the kernels set when they give up (they never trap).
+ * Returns GBATTN_OK, GBATTN_ERR_TIMEOUT (the word was set) or GBATTN_ERR_CUDA.
+ * If detail != NULL it receives the raw word (which wait gave up).
+ */
+int attn_last_device_error(void* stream, int* detail);
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char* attn_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBATTN_H */

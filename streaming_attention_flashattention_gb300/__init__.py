@@ -1,0 +1,187 @@
+"""Python binding of libgbattn.so (GB300 streaming attention), argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module checks
+tensor properties, passes raw device pointers and the current CUDA stream through ctypes,
+and turns status codes into exceptions.  There is no fallback: if the library is missing
+or was not built for this machine, loading raises.
+
+Entry points (same names as the C ABI in include/gbattn.h):
+  attn_fwd(q, k, v, causal, scale=None, out=None, lse=None)
+  attn_decode_splitkv(q, kcache, vcache, kv_lens, num_splits=0, scale=None, ...)
+  attn_decode_workspace_size(B, Hq, Hkv, Lmax, d, num_splits)
+  attn_last_device_error(stream=None)
+  attn_status_string(status)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIBRARY_PATH = os.path.join(_PKG, "libgbattn.so")
+
+GBATTN_BF16 = 0
+GBATTN_FP32 = 1
+GBATTN_OK = 0
+GBATTN_ERR_TIMEOUT = -5
+
+_lock = threading.Lock()
+_lib = None
+
+# (name, restype, argtypes) of every exported symbol
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+EXPORTS = {
+    "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "attn_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "attn_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "attn_last_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_int)]),
+    "attn_status_string": (ctypes.c_char_p, [_I]),
+    "attn_version": (_I, []),
+}
+
+
+class GbAttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {attn_status_string(status)} (status {status})")
+        self.status = status
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libgbattn.so (built by build.build()); raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIBRARY_PATH
+        if not os.path.exists(p):
+            raise ImportError(
+                f"{p} is missing: build it with streaming_attention_flashattention_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in EXPORTS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != GBATTN_OK:
+        raise GbAttnError(fn, status)
+
+
+def _dev_tensor(name: str, t: torch.Tensor, dtypes):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def attn_version() -> int:
+    return int(load_library().attn_version())
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool,
+             scale: float | None = None, out: torch.Tensor | None = None,
+             lse: torch.Tensor | None = None, stream=None):
+    """O = softmax(scale * Q K^T + mask) V for BHSD tensors; returns (out, lse).
+
+    q [B, Hq, Sq, d], k/v [B, Hkv, Skv, d], bf16 (tensor-core path) or fp32 (exact fp32
+    path), contiguous CUDA tensors.  lse is fp32 [B, Hq, Sq].
+    """
+    lib = load_library()
+    dts = (torch.bfloat16, torch.float32)
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _dev_tensor(n, t, dts)
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share a dtype")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("expected q [B,Hq,Sq,d] and k, v [B,Hkv,Skv,d]")
+    B, Hq, Sq, d = q.shape
+    _, Hkv, Skv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _dev_tensor("out", out, (q.dtype,))
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    else:
+        _dev_tensor("lse", lse, (torch.float32,))
+    dtype = GBATTN_BF16 if q.dtype == torch.bfloat16 else GBATTN_FP32
+    st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                      B, Hq, Hkv, Sq, Skv, d, float(scale), 1 if causal else 0, dtype,
+                      _stream_ptr(stream))
+    _check("attn_fwd", st)
+    return out, lse
+
+
+def attn_decode_workspace_size(B: int, Hq: int, Hkv: int, Lmax: int, d: int,
+                               num_splits: int = 0) -> int:
+    return int(load_library().attn_decode_workspace_size(B, Hq, Hkv, Lmax, d, num_splits))
+
+
+def attn_decode_splitkv(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
+                        kv_lens: torch.Tensor, num_splits: int = 0, scale: float | None = None,
+                        out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None, stream=None):
+    """Single-token decode: q [B,Hq,1,d], caches [B,Hkv,Lmax,d] bf16, kv_lens int32 [B].
+
+    Returns (out [B,Hq,1,d] bf16, lse [B,Hq] fp32).  `workspace` (uint8, on the device) is
+    allocated here when not given; pass one to keep allocations out of a hot loop.
+    """
+    lib = load_library()
+    for n, t in (("q", q), ("kcache", kcache), ("vcache", vcache)):
+        _dev_tensor(n, t, (torch.bfloat16,))
+    _dev_tensor("kv_lens", kv_lens, (torch.int32,))
+    B, Hq, one, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes one query token per sequence")
+    _, Hkv, Lmax, _ = kcache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = attn_decode_workspace_size(B, Hq, Hkv, Lmax, d, num_splits)
+    if need == 0:
+        _check("attn_decode_workspace_size", -1)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = lib.attn_decode_splitkv(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
+                                 kv_lens.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                 B, Hq, Hkv, Lmax, d, float(scale), int(num_splits),
+                                 workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                 _stream_ptr(stream))
+    _check("attn_decode_splitkv", st)
+    return out, lse
+
+
+def attn_last_device_error(stream=None) -> tuple[int, int]:
+    """Synchronise the stream and read+clear the bounded-wait error word: (status, word)."""
+    lib = load_library()
+    detail = ctypes.c_int(0)
+    st = lib.attn_last_device_error(_stream_ptr(stream), ctypes.byref(detail))
+    return int(st), int(detail.value)

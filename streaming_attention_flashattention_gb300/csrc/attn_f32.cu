@@ -1,0 +1,137 @@
+// attn_f32.cu -- exact-fp32 streaming attention forward on CUDA cores.
+//
+// Serves GBATTN_FP32 inputs (fp32 Q/K/V/O), where a bf16 or tf32 tensor-core product
+// would miss a 1e-4 tolerance.  Same algorithm as the tensor-core path: a resident Q
+// tile, K/V tiles streamed through shared memory, and the online softmax update of
+// "AttentionRegion Transformation" section 6 / "ADR-0060" section 3 (running max m,
+// running sum l, O rescaled by exp(m_old - m_new)), normalised once at the end.
+//
+// Mapping: a CTA owns 16 query rows of one (b, h); each warp owns 4 rows.  Per 32-key
+// tile, lane j computes the score of key j for the warp's row, the warp reduces max and
+// sum with shuffles, and each lane accumulates its own d/32 output columns.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gbattn {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kRowsPerWarp = 4;
+constexpr int kRowsPerCta = kWarps * kRowsPerWarp;
+constexpr int kKeysPerTile = 32;
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32)
+attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
+                    const float* __restrict__ v, float* __restrict__ o, float* __restrict__ lse,
+                    int Hq, int Hkv, int Sq, int Skv, float scale_log2, int causal) {
+    constexpr int P = D + 1;  // padded row: lane j reading row j is conflict free
+    constexpr int C = D / 32; // output columns per lane
+    __shared__ float sq[kRowsPerCta][D];
+    __shared__ float sk[kKeysPerTile][P];
+    __shared__ float sv[kKeysPerTile][P];
+
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int row0 = blockIdx.x * kRowsPerCta;
+    const int kvh = h / (Hq / Hkv);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long q_base = ((long long)b * Hq + h) * Sq;
+    const long long kv_base = ((long long)b * Hkv + kvh) * (long long)Skv * D;
+    const int off = Skv - Sq;  // bottom-right causal offset
+
+    for (int idx = threadIdx.x; idx < kRowsPerCta * D; idx += blockDim.x) {
+        const int r = idx / D, c = idx % D;
+        const int i = row0 + r;
+        sq[r][c] = (i < Sq) ? q[(q_base + i) * D + c] : 0.f;
+    }
+
+    float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][C];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        m[r] = -INFINITY;
+        l[r] = 0.f;
+#pragma unroll
+        for (int c = 0; c < C; ++c) acc[r][c] = 0.f;
+    }
+
+    // keys needed by this CTA: all of them, or up to the last row's causal limit
+    int kv_end = Skv;
+    if (causal) {
+        const int last = min(row0 + kRowsPerCta, Sq) - 1;
+        kv_end = min(Skv, last + off + 1);
+    }
+
+    for (int t0 = 0; t0 < kv_end; t0 += kKeysPerTile) {
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < kKeysPerTile * D; idx += blockDim.x) {
+            const int j = idx / D, c = idx % D;
+            const bool ok = (t0 + j) < Skv;
+            sk[j][c] = ok ? k[kv_base + (long long)(t0 + j) * D + c] : 0.f;
+            sv[j][c] = ok ? v[kv_base + (long long)(t0 + j) * D + c] : 0.f;
+        }
+        __syncthreads();
+
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            const int lr = warp * kRowsPerWarp + r;
+            const int i = row0 + lr;
+            const int key = t0 + lane;
+            float dot = 0.f;
+#pragma unroll 16
+            for (int c = 0; c < D; ++c) dot = fmaf(sq[lr][c], sk[lane][c], dot);
+            bool visible = key < Skv;
+            if (causal) visible = visible && (key <= i + off);
+            const float s = visible ? dot * scale_log2 : -INFINITY;
+            float mt = s;
+#pragma unroll
+            for (int w = 16; w > 0; w >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, w));
+            const float m_new = fmaxf(m[r], mt);
+            if (m_new == -INFINITY) continue;  // nothing visible yet for this row
+            const float corr = exp2f(m[r] - m_new);
+            const float p = exp2f(s - m_new);
+            float ps = p;
+#pragma unroll
+            for (int w = 16; w > 0; w >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, w);
+            l[r] = l[r] * corr + ps;
+            m[r] = m_new;
+#pragma unroll
+            for (int c = 0; c < C; ++c) acc[r][c] *= corr;
+            for (int j = 0; j < kKeysPerTile; ++j) {
+                const float pj = __shfl_sync(0xffffffffu, p, j);
+#pragma unroll
+                for (int c = 0; c < C; ++c) acc[r][c] = fmaf(pj, sv[j][lane + 32 * c], acc[r][c]);
+            }
+        }
+    }
+
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        const int i = row0 + warp * kRowsPerWarp + r;
+        if (i >= Sq) continue;
+        const float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
+#pragma unroll
+        for (int c = 0; c < C; ++c) o[(q_base + i) * D + lane + 32 * c] = acc[r][c] * inv;
+        if (lse != nullptr && lane == 0)
+            lse[q_base + i] = l[r] > 0.f ? (m[r] + log2f(l[r])) * 0.69314718055994531f : -INFINITY;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd_f32(const float* q, const float* k, const float* v, float* o,
+                                float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                                float scale, int causal, cudaStream_t stream) {
+    const float scale_log2 = scale * 1.4426950408889634f;
+    dim3 grid((Sq + kRowsPerCta - 1) / kRowsPerCta, Hq, B);
+    dim3 block(kWarps * 32);
+    if (d == 64)
+        attn_fwd_f32_kernel<64><<<grid, block, 0, stream>>>(q, k, v, o, lse, Hq, Hkv, Sq, Skv,
+                                                            scale_log2, causal);
+    else
+        attn_fwd_f32_kernel<128><<<grid, block, 0, stream>>>(q, k, v, o, lse, Hq, Hkv, Sq, Skv,
+                                                             scale_log2, causal);
+    return cudaGetLastError();
+}
+
+}  // namespace gbattn

@@ -1,0 +1,518 @@
+// decode_splitkv.cu -- single-token GQA decode over a bf16 KV cache: split-KV partial
+// attention streamed at HBM rate, then a log-sum-exp combine.
+//
+// "ADR-0060: AHBM GQA Fused Attention Kernel (Llama3-70B)":
+//   section 5.2 -- decode has T_q = 1 and sees every past key, so only a ragged last tile
+//                  is masked; the G query heads of one KV head are stacked into one GEMM
+//                  operand so that every K/V tile is read once for all G heads;
+//   section 3   -- per tile: S = scale * Q K^T, row max, exp, corr = exp(m - m_new),
+//                  l = l * corr + sum P, O = O * corr + P V;
+//   section 4   -- partial (m, l, O) of independent KV ranges merge associatively with
+//                  m = max(m_a, m_b), weights exp(m_a - m), exp(m_b - m); normalise once;
+//   section 2.1 -- each range is one contiguous block of the cache.
+//
+// GB300 mapping.
+//   split kernel: persistent CTAs (one per SM) pull work items (sequence b, KV head,
+//   head chunk, split s) from a device counter.  One producer warp streams the split's
+//   K and V through a 5-stage shared-memory ring with 3-D TMA copies (64 keys x d,
+//   128-byte swizzle) and mbarrier handoff.  Four consumer warps take 16 keys each per
+//   stage and run S^T = K Q^T and O^T += V^T P^T on mma.sync m16n8k16 with the G <= 8
+//   query heads in the N = 8 dimension (the MMA's M dimension is filled by keys, so no
+//   lane is wasted on padding heads).  The S^T accumulator fragment is turned into the
+//   P^T operand fragment in registers with movmatrix.  Each warp keeps its own running
+//   (m, l, O); at the end of a split the four states merge through shared memory and the
+//   normalised partial (lse_s, O_s / l_s) goes to the workspace.
+//   combine kernel: one warp per (b, query head) merges the partials of its splits.
+//   Decode is HBM bound (8 flop per byte of KV), so these contractions stay on the
+//   warp-level tensor path; the streaming design is what sets the speed.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gbattn {
+
+namespace {
+
+constexpr int kKeysPerStage = 64;
+constexpr int kConsumerWarps = 4;          // 16 keys each per stage
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 5;
+constexpr int kHeads = 8;                  // query heads per work item (MMA N)
+
+struct StageInfo {
+    int b, kvh, hc, s;
+    int tile, ntok, last, done;
+};
+
+template <int D>
+struct Layout {
+    static constexpr int kBoxes = D / 64;                       // 64-element swizzle boxes
+    static constexpr int kKBytes = kKeysPerStage * D * 2;       // K tile
+    static constexpr int kVBytes = kKeysPerStage * D * 2;
+    static constexpr int kQBytes = kHeads * D * 2;              // 8 query rows
+    static constexpr int kStageBytes = kKBytes + kVBytes + kQBytes;   // multiple of 1024
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kInfoOff = kRingBytes;
+    static constexpr int kBarOff = kInfoOff + kStages * (int)sizeof(StageInfo);
+    static constexpr int kNumBars = 2 * kStages + 2;
+    static constexpr int kRedMOff = kBarOff + kNumBars * 8;
+    static constexpr int kRedLOff = kRedMOff + kConsumerWarps * kHeads * 4;
+    static constexpr int kRedOOff = kRedLOff + kConsumerWarps * kHeads * 4;
+    static constexpr int kBytes = kRedOOff + kConsumerWarps * kHeads * D * 4;
+    static constexpr int kAlloc = kBytes + 1024;                // slack for 1024-B alignment
+    static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
+};
+
+// 16-byte chunk `chunk` of row `row` inside a 128-byte-swizzled box.
+__device__ __forceinline__ uint32_t sw128(uint32_t box, int row, int chunk) {
+    return box + (uint32_t)row * 128u + ((uint32_t)(chunk ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(addr));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// bf16 element e of x (low 16 bits) and of y (high 16 bits) packed into one register.
+__device__ __forceinline__ uint32_t pair_elem(const uint4& x, const uint4& y, int e) {
+    return __byte_perm(word(x, e >> 1), word(y, e >> 1), (e & 1) ? 0x7632 : 0x5410);
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// Split bounds of the reading "contiguous blocks": n splits of C keys,
+// C = ceil(len / n) rounded up to kSplitAlign.
+__device__ __forceinline__ void split_range(int len, int n, int s, int& t0, int& t1) {
+    int c = (len + n - 1) / n;
+    c = ((c + kSplitAlign - 1) / kSplitAlign) * kSplitAlign;
+    if (c == 0) c = kSplitAlign;
+    const long long a = (long long)s * c;
+    t0 = (int)min((long long)len, a);
+    t1 = (int)min((long long)len, a + c);
+}
+
+__device__ __forceinline__ int splits_for(int len, int fixed_splits) {
+    if (fixed_splits > 0) return fixed_splits;
+    int n = (len + kAutoChunk - 1) / kAutoChunk;
+    return max(1, min(kMaxSplits, n));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_split_kernel(const __grid_constant__ DecodeParams p) {
+    using L = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    StageInfo* info = reinterpret_cast<StageInfo*>(smem + L::kInfoOff);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+    uint64_t* full = bars;                   // [kStages] producer -> consumers (TMA bytes)
+    uint64_t* empty = bars + kStages;        // [kStages] consumers -> producer (4 arrivals)
+    uint64_t* sync_a = bars + 2 * kStages;   // consumer-warp rendezvous at a split's end
+    uint64_t* sync_b = sync_a + 1;
+    float* red_m = reinterpret_cast<float*>(smem + L::kRedMOff);
+    float* red_l = reinterpret_cast<float*>(smem + L::kRedLOff);
+    float* red_o = reinterpret_cast<float*>(smem + L::kRedOOff);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        mbar_init(sync_a, kConsumerWarps);
+        mbar_init(sync_b, kConsumerWarps);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ============================== producer warp ==============================
+        if (lane == 0) {
+            prefetch_tensormap(&p.tmap_k);
+            prefetch_tensormap(&p.tmap_v);
+            prefetch_tensormap(&p.tmap_q);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t filled = 0, fill_parity = 0;   // per-stage bits for the exit drain
+            bool ok = true;
+            while (ok) {
+                const int item = atomicAdd(p.counter, 1);
+                if (item >= p.n_items) break;
+                int rem = item;
+                const int hc = rem % p.n_hc; rem /= p.n_hc;
+                const int kvh = rem % p.Hkv; rem /= p.Hkv;
+                const int b = rem % p.B; rem /= p.B;
+                const int s = rem;
+                int len = __ldg(&p.kv_lens[b]);
+                len = max(0, min(len, p.Lmax));
+                const int nb = splits_for(len, p.fixed_splits);
+                if (s >= nb) continue;
+                int t0, t1;
+                split_range(len, nb, s, t0, t1);
+                const int h0 = kvh * p.G + hc * kHeads;
+                const int gcnt = min(kHeads, p.G - hc * kHeads);
+                if (t1 <= t0) {      // empty split: its partial carries no weight
+                    for (int g = 0; g < gcnt; ++g)
+                        p.ws_lse[((long long)b * p.Hq + h0 + g) * p.n_slots + s] = -INFINITY;
+                    continue;
+                }
+                const int ntiles = (t1 - t0 + kKeysPerStage - 1) / kKeysPerStage;
+                const int zkv = b * p.Hkv + kvh;
+                for (int tile = 0; tile < ntiles; ++tile) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, kErrWaitProducer, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const int y = t0 + tile * kKeysPerStage;
+                    StageInfo& si = info[stage];
+                    si.b = b; si.kvh = kvh; si.hc = hc; si.s = s;
+                    si.tile = tile;
+                    si.ntok = min(kKeysPerStage, t1 - y);
+                    si.last = (tile == ntiles - 1);
+                    si.done = 0;
+                    uint8_t* st = smem + stage * L::kStageBytes;
+                    const uint32_t bytes = L::kKBytes + L::kVBytes + (tile == 0 ? L::kQBytes : 0);
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+                    #pragma unroll
+                    for (int bx = 0; bx < L::kBoxes; ++bx) {
+                        tma_load_3d(st + bx * (kKeysPerStage * 128), &p.tmap_k, bx * 64, y, zkv,
+                                    &full[stage]);
+                        tma_load_3d(st + L::kKBytes + bx * (kKeysPerStage * 128), &p.tmap_v,
+                                    bx * 64, y, zkv, &full[stage]);
+                    }
+                    if (tile == 0) {
+                        const int yq = b * p.Hq + h0;
+                        #pragma unroll
+                        for (int bx = 0; bx < L::kBoxes; ++bx)
+                            tma_load_3d(st + L::kKBytes + L::kVBytes + bx * (kHeads * 128),
+                                        &p.tmap_q, bx * 64, yq, 0, &full[stage]);
+                    }
+                    filled |= 1u << stage;
+                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (ok) {
+                // end-of-work marker for the consumers
+                if (mbar_wait(&empty[stage], phase ^ 1u, kErrWaitProducer, p.err)) {
+                    info[stage].done = 1;
+                    mbar_arrive(&full[stage]);
+                }
+            }
+            // drain: never leave the CTA with a TMA copy still writing its shared memory
+            for (int i = 0; i < kStages; ++i)
+                if (filled & (1u << i)) mbar_wait(&full[i], (fill_parity >> i) & 1u, kErrWaitDrain, p.err);
+        }
+    } else {
+        // ============================== consumer warps =============================
+        const int g = lane >> 2, c = lane & 3;
+        const uint32_t ring = smem_u32(smem);
+        const float scale_log2 = p.scale_log2;
+        uint4 qf[D / 32];
+        float acc[D / 16][4];
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        int stage = 0;
+        uint32_t phase = 0, sync_phase = 0;
+        const int R0 = warp * 16;   // this warp's 16 keys within a stage
+        while (true) {
+            if (!mbar_wait(&full[stage], phase, kErrWaitConsumer, p.err)) break;
+            const StageInfo si = info[stage];
+            if (si.done) break;
+            const uint32_t kbox = ring + stage * L::kStageBytes;
+            const uint32_t vbox = kbox + L::kKBytes;
+            const uint32_t qbox = vbox + L::kVBytes;
+            const int gcnt = min(kHeads, p.G - si.hc * kHeads);
+            if (si.tile == 0) {
+                #pragma unroll
+                for (int s = 0; s < D / 32; ++s) {
+                    uint4 z = make_uint4(0, 0, 0, 0);
+                    if (g < gcnt) z = lds128(sw128(qbox + (s >> 1) * (kHeads * 128), g, 2 * c + (s & 1)));
+                    qf[s] = z;
+                }
+                m0 = m1 = -INFINITY;
+                l0 = l1 = 0.f;
+                #pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt)
+                    acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+            }
+            const int nvalid = min(16, si.ntok - R0);
+            if (nvalid > 0) {
+                // ---- S^T[16 keys x 8 heads] = K Q^T ----
+                float sc[4] = {0.f, 0.f, 0.f, 0.f};
+                #pragma unroll
+                for (int s = 0; s < D / 32; ++s) {
+                    const uint32_t kb = kbox + (s >> 1) * (kKeysPerStage * 128);
+                    const int ch = 2 * c + (s & 1);
+                    const uint4 k0 = lds128(sw128(kb, R0 + g, ch));
+                    const uint4 k1 = lds128(sw128(kb, R0 + g + 8, ch));
+                    mma16816(sc, k0.x, k1.x, k0.y, k1.y, qf[s].x, qf[s].y);
+                    mma16816(sc, k0.z, k1.z, k0.w, k1.w, qf[s].z, qf[s].w);
+                }
+                // ---- online softmax over the keys (columns = heads 2c, 2c+1) ----
+                const bool v_lo = g < nvalid, v_hi = g + 8 < nvalid;
+                sc[0] = v_lo ? sc[0] * scale_log2 : -INFINITY;
+                sc[1] = v_lo ? sc[1] * scale_log2 : -INFINITY;
+                sc[2] = v_hi ? sc[2] * scale_log2 : -INFINITY;
+                sc[3] = v_hi ? sc[3] * scale_log2 : -INFINITY;
+                float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+                #pragma unroll
+                for (int w = 4; w < 32; w <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, w));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, w));
+                }
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+                const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+                const float corr0 = ex2_approx(m0 - base0), corr1 = ex2_approx(m1 - base1);
+                const float p00 = ex2_approx(sc[0] - base0), p01 = ex2_approx(sc[1] - base1);
+                const float p10 = ex2_approx(sc[2] - base0), p11 = ex2_approx(sc[3] - base1);
+                l0 = l0 * corr0 + p00 + p10;
+                l1 = l1 * corr1 + p01 + p11;
+                m0 = mn0;
+                m1 = mn1;
+                #pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    acc[mt][0] *= corr0; acc[mt][1] *= corr1;
+                    acc[mt][2] *= corr0; acc[mt][3] *= corr1;
+                }
+                // ---- P^T operand: transpose the (key x head) 8x8 blocks in registers ----
+                const uint32_t b0 = movmatrix_trans(pack_bf16(p00, p01));
+                const uint32_t b1 = movmatrix_trans(pack_bf16(p10, p11));
+                // ---- O^T[d x 8 heads] += V^T P^T ----
+                const int tk[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+                if constexpr (D == 128) {
+                    uint4 vv[4][2];
+                    #pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        #pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint4 z = make_uint4(0, 0, 0, 0);
+                            if (tk[i] < nvalid) z = lds128(sw128(vbox + h * (kKeysPerStage * 128), R0 + tk[i], g));
+                            vv[i][h] = z;
+                        }
+                    #pragma unroll
+                    for (int mt = 0; mt < 8; ++mt)
+                        mma16816(acc[mt], pair_elem(vv[0][0], vv[1][0], mt),
+                                 pair_elem(vv[0][1], vv[1][1], mt),
+                                 pair_elem(vv[2][0], vv[3][0], mt),
+                                 pair_elem(vv[2][1], vv[3][1], mt), b0, b1);
+                } else {
+                    uint4 vv[4];
+                    #pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 z = make_uint4(0, 0, 0, 0);
+                        if (tk[i] < nvalid) z = lds128(sw128(vbox, R0 + tk[i], g));
+                        vv[i] = z;
+                    }
+                    #pragma unroll
+                    for (int mt = 0; mt < 4; ++mt)
+                        mma16816(acc[mt], pair_elem(vv[0], vv[1], mt),
+                                 pair_elem(vv[0], vv[1], mt + 4),
+                                 pair_elem(vv[2], vv[3], mt),
+                                 pair_elem(vv[2], vv[3], mt + 4), b0, b1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+
+            if (si.last) {
+                // ---- merge the four warps' states; write the split's partial ----
+                float lr0 = l0, lr1 = l1;
+                #pragma unroll
+                for (int w = 4; w < 32; w <<= 1) {
+                    lr0 += __shfl_xor_sync(0xffffffffu, lr0, w);
+                    lr1 += __shfl_xor_sync(0xffffffffu, lr1, w);
+                }
+                if (g == 0) {
+                    red_m[warp * kHeads + 2 * c] = m0;
+                    red_m[warp * kHeads + 2 * c + 1] = m1;
+                    red_l[warp * kHeads + 2 * c] = lr0;
+                    red_l[warp * kHeads + 2 * c + 1] = lr1;
+                }
+                float* ro = red_o + warp * kHeads * D;
+                #pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    const int d_lo = (D == 128) ? 8 * g + mt : 8 * g + mt;
+                    const int d_hi = (D == 128) ? 64 + 8 * g + mt : 8 * g + 4 + mt;
+                    ro[(2 * c) * D + d_lo] = acc[mt][0];
+                    ro[(2 * c + 1) * D + d_lo] = acc[mt][1];
+                    ro[(2 * c) * D + d_hi] = acc[mt][2];
+                    ro[(2 * c + 1) * D + d_hi] = acc[mt][3];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sync_a);
+                if (!mbar_wait(sync_a, sync_phase, kErrWaitConsumer, p.err)) break;
+                {
+                    const int t = threadIdx.x;          // 0..127
+                    const int head = t >> 4;
+                    constexpr int per = D / 16;
+                    const int d0 = (t & 15) * per;
+                    if (head < gcnt) {
+                        float M = -INFINITY;
+                        #pragma unroll
+                        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * kHeads + head]);
+                        float wt[kConsumerWarps], Ltot = 0.f;
+                        #pragma unroll
+                        for (int w = 0; w < kConsumerWarps; ++w) {
+                            const float mw = red_m[w * kHeads + head];
+                            wt[w] = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
+                            Ltot += wt[w] * red_l[w * kHeads + head];
+                        }
+                        const float inv = 1.f / Ltot;
+                        const int hq = si.kvh * p.G + si.hc * kHeads + head;
+                        const long long slot = ((long long)si.b * p.Hq + hq) * p.n_slots + si.s;
+                        float* dst = p.ws_o + slot * D + d0;
+                        #pragma unroll
+                        for (int e = 0; e < per; e += 4) {
+                            float4 r;
+                            float* rr = &r.x;
+                            #pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                float sum = 0.f;
+                                #pragma unroll
+                                for (int w = 0; w < kConsumerWarps; ++w)
+                                    sum += wt[w] * red_o[(w * kHeads + head) * D + d0 + e + u];
+                                rr[u] = sum * inv;
+                            }
+                            *reinterpret_cast<float4*>(dst + e) = r;
+                        }
+                        if ((t & 15) == 0) p.ws_lse[slot] = M + __log2f(Ltot);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sync_b);
+                if (!mbar_wait(sync_b, sync_phase, kErrWaitConsumer, p.err)) break;
+                sync_phase ^= 1u;
+            }
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+    }
+    __syncthreads();
+}
+
+// One warp per (b, query head): O = sum_s w_s O_s / sum_s w_s, w_s = 2^(lse_s - max lse).
+template <int D>
+__global__ void __launch_bounds__(256)
+decode_combine_kernel(const __grid_constant__ DecodeParams p) {
+    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= p.B * p.Hq) return;
+    const int b = gw / p.Hq;
+    int len = __ldg(&p.kv_lens[b]);
+    len = max(0, min(len, p.Lmax));
+    const int nb = splits_for(len, p.fixed_splits);
+    const float* lse_s = p.ws_lse + (long long)gw * p.n_slots;
+    const float* o_s = p.ws_o + (long long)gw * p.n_slots * D;
+    float M = -INFINITY;
+    for (int s = lane; s < nb; s += 32) M = fmaxf(M, lse_s[s]);
+    #pragma unroll
+    for (int w = 16; w > 0; w >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, w));
+    constexpr int per = D / 32;
+    float acc[per];
+    #pragma unroll
+    for (int e = 0; e < per; ++e) acc[e] = 0.f;
+    float Ltot = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < nb; ++s) {
+            const float ls = lse_s[s];
+            if (ls == -INFINITY) continue;
+            const float w = ex2_approx(ls - M);
+            Ltot += w;
+            const float* src = o_s + (long long)s * D + lane * per;
+            if constexpr (per == 4) {
+                const float4 x = *reinterpret_cast<const float4*>(src);
+                acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+            } else {
+                const float2 x = *reinterpret_cast<const float2*>(src);
+                acc[0] += w * x.x; acc[1] += w * x.y;
+            }
+        }
+    }
+    const float inv = Ltot > 0.f ? 1.f / Ltot : 0.f;
+    __nv_bfloat16* dst = p.o + (long long)gw * D + lane * per;
+    if constexpr (per == 4) {
+        uint2 packed;
+        packed.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+        packed.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(dst) = packed;
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
+    }
+    if (p.lse != nullptr && lane == 0)
+        p.lse[gw] = (Ltot > 0.f) ? (M + __log2f(Ltot)) * 0.69314718055994531f : -INFINITY;
+}
+
+}  // namespace
+
+int decode_slots(int Lmax, int num_splits) {
+    if (num_splits > 0) return num_splits;
+    int n = (Lmax + kAutoChunk - 1) / kAutoChunk;
+    return n < 1 ? 1 : (n > kMaxSplits ? kMaxSplits : n);
+}
+
+size_t decode_workspace_bytes(int B, int Hq, int d, int n_slots) {
+    const size_t rows = (size_t)B * Hq * n_slots;
+    size_t bytes = 256;                                  // work counter
+    bytes += ((rows * 4 + 255) / 256) * 256;             // lse partials
+    bytes += rows * (size_t)d * 4;                       // O partials
+    return bytes;
+}
+
+cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
+                                  cudaStream_t stream) {
+    cudaError_t err = cudaMemsetAsync(p.counter, 0, sizeof(int), stream);
+    if (err != cudaSuccess) return err;
+    const int grid = p.n_items < num_sms ? p.n_items : num_sms;
+    if (d == 128) {
+        constexpr int smem = Layout<128>::kAlloc;
+        static bool attr = false;
+        if (!attr) {
+            err = cudaFuncSetAttribute(decode_split_kernel<128>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (err != cudaSuccess) return err;
+            attr = true;
+        }
+        if (grid > 0) decode_split_kernel<128><<<grid, kThreads, smem, stream>>>(p);
+        err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+        const int cblocks = (p.B * p.Hq + 7) / 8;
+        decode_combine_kernel<128><<<cblocks, 256, 0, stream>>>(p);
+    } else {
+        constexpr int smem = Layout<64>::kAlloc;
+        static bool attr = false;
+        if (!attr) {
+            err = cudaFuncSetAttribute(decode_split_kernel<64>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (err != cudaSuccess) return err;
+            attr = true;
+        }
+        if (grid > 0) decode_split_kernel<64><<<grid, kThreads, smem, stream>>>(p);
+        err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+        const int cblocks = (p.B * p.Hq + 7) / 8;
+        decode_combine_kernel<64><<<cblocks, 256, 0, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gbattn

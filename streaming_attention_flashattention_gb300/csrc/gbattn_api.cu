@@ -1,0 +1,230 @@
+// gbattn_api.cu -- the C ABI: argument validation ("AI Compiler pipeline stages",
+// Legality Checking: shape, dtype, layout and memory conditions decide whether the fused
+// kernel may run; here they turn into status codes), launch planning (TMA descriptors,
+// work counts, workspace carving) and the launches themselves.  No device memory is
+// allocated per call; the only device state is the error word of bounded waits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gbattn {
+
+namespace {
+__device__ int g_device_error = 0;
+}  // namespace
+
+int* device_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    static int* cached[64] = {nullptr};
+    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return nullptr;
+    if (dev >= 0 && dev < 64) cached[dev] = static_cast<int*>(ptr);
+    return static_cast<int*>(ptr);
+}
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 3-D bf16 tensor map with a 128-byte swizzle: dims innermost first, box (64, rows, 1).
+bool make_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
+                      uint64_t d2, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    const cuuint32_t box[3] = {64, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    static int cached[64] = {0};
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr long long kIntMax = 2147483647LL;
+
+}  // namespace
+}  // namespace gbattn
+
+using namespace gbattn;
+
+extern "C" {
+
+int attn_version(void) { return 100; }
+
+const char* attn_status_string(int status) {
+    switch (status) {
+        case GBATTN_OK: return "ok";
+        case GBATTN_ERR_INVALID_ARG: return "invalid argument";
+        case GBATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+        case GBATTN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case GBATTN_ERR_CUDA: return "CUDA error";
+        case GBATTN_ERR_TIMEOUT: return "device bounded wait expired";
+        case GBATTN_ERR_WORKSPACE: return "workspace missing or too small";
+        case GBATTN_ERR_TOO_LARGE: return "size exceeds kernel indexing range";
+        default: return "unknown status";
+    }
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int Sq, int Skv, int d, float scale, int causal, int dtype,
+             void* stream) {
+    if (!q || !k || !v || !o) return GBATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || d <= 0)
+        return GBATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return GBATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || scale != scale) return GBATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return GBATTN_ERR_INVALID_ARG;
+    if (dtype != GBATTN_BF16 && dtype != GBATTN_FP32) return GBATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return GBATTN_ERR_UNSUPPORTED;
+    if (causal && Sq > Skv) return GBATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (lse && !aligned16(lse)))
+        return GBATTN_ERR_MISALIGNED;
+    if ((long long)B * Hq > 65535LL * 65535LL || (long long)B * Hq * Sq > kIntMax ||
+        (long long)B * Hkv * Skv > kIntMax)
+        return GBATTN_ERR_TOO_LARGE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (dtype == GBATTN_FP32) {
+        if (B > 65535 || Hq > 65535) return GBATTN_ERR_TOO_LARGE;
+        cudaError_t e = launch_attn_fwd_f32(static_cast<const float*>(q),
+                                            static_cast<const float*>(k),
+                                            static_cast<const float*>(v), static_cast<float*>(o),
+                                            lse, B, Hq, Hkv, Sq, Skv, d, scale, causal, st);
+        return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+    }
+
+    PrefillParams p{};
+    if (!make_map_bf16_3d(&p.tmap_q, q, d, Sq, (uint64_t)B * Hq, 128) ||
+        !make_map_bf16_3d(&p.tmap_k, k, d, Skv, (uint64_t)B * Hkv, 128) ||
+        !make_map_bf16_3d(&p.tmap_v, v, d, Skv, (uint64_t)B * Hkv, 128))
+        return GBATTN_ERR_CUDA;
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv;
+    p.G = Hq / Hkv;
+    p.n_qblk = (Sq + 127) / 128;
+    const long long per_group = ((long long)p.n_qblk * p.G + 1) / 2;
+    const long long n_pairs = per_group * B * Hkv;
+    if (n_pairs > kIntMax) return GBATTN_ERR_TOO_LARGE;
+    p.n_pairs = (int)n_pairs;
+    p.causal = causal;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = device_error_word();
+    if (!p.err) return GBATTN_ERR_CUDA;
+    cudaError_t e = launch_attn_fwd_bf16(p, d, st);
+    return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int num_splits) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lmax <= 0 || (d != 64 && d != 128)) return 0;
+    if (num_splits < 0 || num_splits > kMaxSplits) return 0;
+    return decode_workspace_bytes(B, Hq, d, decode_slots(Lmax, num_splits));
+}
+
+int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
+                        const int* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Lmax, int d, float scale, int num_splits, void* workspace,
+                        size_t ws_bytes, void* stream) {
+    if (!q || !kcache || !vcache || !kv_lens || !o) return GBATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lmax <= 0 || d <= 0) return GBATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return GBATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || scale != scale) return GBATTN_ERR_INVALID_ARG;
+    if (num_splits < 0 || num_splits > kMaxSplits) return GBATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return GBATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
+        (lse && !aligned16(lse)) || (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
+        return GBATTN_ERR_MISALIGNED;
+    const int n_slots = decode_slots(Lmax, num_splits);
+    const size_t need = decode_workspace_bytes(B, Hq, d, n_slots);
+    if (!workspace || ws_bytes < need) return GBATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return GBATTN_ERR_MISALIGNED;
+    const int G = Hq / Hkv;
+    const int n_hc = (G + 7) / 8;
+    const long long n_items = (long long)n_slots * B * Hkv * n_hc;
+    if (n_items > kIntMax || (long long)B * Hkv * Lmax > kIntMax ||
+        (long long)B * Hq > kIntMax / 8)
+        return GBATTN_ERR_TOO_LARGE;
+    const int nsm = sm_count();
+    if (nsm <= 0) return GBATTN_ERR_CUDA;
+
+    DecodeParams p{};
+    if (!make_map_bf16_3d(&p.tmap_k, kcache, d, Lmax, (uint64_t)B * Hkv, 64) ||
+        !make_map_bf16_3d(&p.tmap_v, vcache, d, Lmax, (uint64_t)B * Hkv, 64) ||
+        !make_map_bf16_3d(&p.tmap_q, q, d, (uint64_t)B * Hq, 1, 8))
+        return GBATTN_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t rows = (size_t)B * Hq * n_slots;
+    p.counter = reinterpret_cast<int*>(ws);
+    p.ws_lse = reinterpret_cast<float*>(ws + 256);
+    p.ws_o = reinterpret_cast<float*>(ws + 256 + ((rows * 4 + 255) / 256) * 256);
+    p.kv_lens = kv_lens;
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Lmax = Lmax; p.G = G;
+    p.n_hc = n_hc;
+    p.n_slots = n_slots;
+    p.fixed_splits = num_splits;
+    p.n_items = (int)n_items;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = device_error_word();
+    if (!p.err) return GBATTN_ERR_CUDA;
+    cudaError_t e = launch_decode_splitkv(p, d, nsm, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+int attn_last_device_error(void* stream, int* detail) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GBATTN_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_device_error, sizeof(int)) != cudaSuccess)
+        return GBATTN_ERR_CUDA;
+    if (detail) *detail = word;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess)
+            return GBATTN_ERR_CUDA;
+        return GBATTN_ERR_TIMEOUT;
+    }
+    return GBATTN_OK;
+}
+
+}  // extern "C"

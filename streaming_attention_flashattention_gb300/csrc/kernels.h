@@ -1,0 +1,66 @@
+// kernels.h -- internal launch interface between the C ABI (gbattn_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gbattn {
+
+// Address of this device's error word (the word itself lives in gbattn_api.cu).
+int* device_error_word();
+
+// ---- fp32 CUDA-core path (attn_f32.cu) ------------------------------------------------
+cudaError_t launch_attn_fwd_f32(const float* q, const float* k, const float* v, float* o,
+                                float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                                float scale, int causal, cudaStream_t stream);
+
+// ---- bf16 tcgen05 prefill path (prefill_tcgen05.cu) ------------------------------------
+struct PrefillParams {
+    CUtensorMap tmap_q;   // 3-D (d, Sq, B*Hq), box (64, 128, 1), 128B swizzle
+    CUtensorMap tmap_k;   // 3-D (d, Skv, B*Hkv), box (64, 128, 1), 128B swizzle
+    CUtensorMap tmap_v;   // same as K
+    __nv_bfloat16* o;     // [B, Hq, Sq, d]
+    float* lse;           // [B, Hq, Sq] or null
+    int B, Hq, Hkv, Sq, Skv;
+    int G;                // Hq / Hkv
+    int n_qblk;           // ceil(Sq / 128)
+    int n_pairs;          // work units (pairs of Q tiles)
+    int causal;
+    float scale_log2;     // scale * log2(e)
+    int* err;             // device error word of bounded waits
+};
+cudaError_t launch_attn_fwd_bf16(const PrefillParams& p, int d, cudaStream_t stream);
+
+// ---- bf16 split-KV decode path (decode_splitkv.cu) --------------------------------------
+struct DecodeParams {
+    CUtensorMap tmap_k;   // 3-D (d, Lmax, B*Hkv), box (64, 64, 1), 128B swizzle
+    CUtensorMap tmap_v;
+    CUtensorMap tmap_q;   // 2-D (d, B*Hq), box (64, 8), 128B swizzle
+    const int* kv_lens;   // [B] device
+    __nv_bfloat16* o;     // [B, Hq, d]
+    float* lse;           // [B, Hq] or null
+    int* counter;         // work counter (zeroed before the split kernel)
+    float* ws_lse;        // [B, Hq, n_slots] log2-domain partial lse
+    float* ws_o;          // [B, Hq, n_slots, d] normalised partial outputs
+    int B, Hq, Hkv, Lmax, G;
+    int n_hc;             // head chunks of <= 8 heads per KV head: ceil(G / 8)
+    int n_slots;          // split slots per sequence
+    int fixed_splits;     // > 0 fixed count, 0 automatic
+    int n_items;          // n_slots * B * Hkv * n_hc
+    float scale_log2;
+    int* err;             // device error word of bounded waits
+};
+// Split-count rule of the automatic mode: one split per kAutoChunk keys.
+constexpr int kAutoChunk = 4096;
+constexpr int kMaxSplits = 256;
+constexpr int kSplitAlign = 64;
+
+size_t decode_workspace_bytes(int B, int Hq, int d, int n_slots);
+int decode_slots(int Lmax, int num_splits);
+cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
+                                  cudaStream_t stream);
+
+}  // namespace gbattn

@@ -1,0 +1,113 @@
+"""The C-ABI library: it loads, exports every symbol include/gbattn.h declares, and its
+host-side validation returns the documented status codes (no GPU needed: every case here
+is rejected before anything touches the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import streaming_attention_flashattention_gb300 as gb
+from streaming_attention_flashattention_gb300 import build as gbbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbbuild.build()
+    return gb.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_]\w*\s*\*?\s*(attn_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["attn_fwd", "attn_decode_splitkv", "attn_decode_workspace_size",
+              "attn_last_device_error", "attn_status_string", "attn_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"libgbattn.so does not export {n}"
+        assert n in gb.EXPORTS, f"binding does not describe {n}"
+
+
+def test_version_and_status_strings(lib):
+    assert gb.attn_version() >= 100
+    assert gb.attn_status_string(0) == "ok"
+    for code in range(-7, 0):
+        s = gb.attn_status_string(code)
+        assert s and s != "unknown status"
+    assert gb.attn_status_string(-99) == "unknown status"
+
+
+A = 0x10000      # fake, 16-byte-aligned addresses: every call below is rejected first
+B_ = 0x20000
+MIS = 0x10008    # 8-byte aligned only
+
+
+def fwd(lib, q=A, k=A, v=A, o=B_, lse=None, B=1, Hq=2, Hkv=1, Sq=128, Skv=128, d=128,
+        scale=0.1, causal=0, dtype=0):
+    return lib.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, scale, causal, dtype, None)
+
+
+def test_fwd_argument_validation(lib):
+    assert fwd(lib, q=None) == -1
+    assert fwd(lib, o=None) == -1
+    assert fwd(lib, B=0) == -1
+    assert fwd(lib, Sq=0) == -1
+    assert fwd(lib, Skv=-3) == -1
+    assert fwd(lib, Hq=3, Hkv=2) == -1
+    assert fwd(lib, scale=0.0) == -1
+    assert fwd(lib, scale=float("nan")) == -1
+    assert fwd(lib, causal=2) == -1
+    assert fwd(lib, dtype=5) == -1
+    assert fwd(lib, d=96) == -2
+    assert fwd(lib, d=256) == -2
+    assert fwd(lib, causal=1, Sq=200, Skv=100) == -2
+    assert fwd(lib, q=MIS) == -3
+    assert fwd(lib, lse=MIS) == -3
+    assert fwd(lib, B=70000, Hq=70000, Hkv=70000) == -7
+
+
+def dec(lib, q=A, kc=A, vc=A, lens=A, o=B_, lse=None, B=4, Hq=64, Hkv=8, Lmax=32768, d=128,
+        scale=0.1, ns=16, ws=A, wsb=None):
+    if wsb is None:
+        wsb = lib.attn_decode_workspace_size(B, Hq, Hkv, Lmax, d, ns)
+    return lib.attn_decode_splitkv(q, kc, vc, lens, o, lse, B, Hq, Hkv, Lmax, d, scale, ns, ws,
+                                   wsb, None)
+
+
+def test_decode_argument_validation(lib):
+    assert dec(lib, kc=None) == -1
+    assert dec(lib, lens=None) == -1
+    assert dec(lib, B=0) == -1
+    assert dec(lib, Hq=63) == -1
+    assert dec(lib, ns=-1) == -1
+    assert dec(lib, ns=257) == -1
+    assert dec(lib, d=80) == -2
+    assert dec(lib, q=MIS) == -3
+    assert dec(lib, lens=0x10002) == -3
+    assert dec(lib, ws=None) == -6
+    assert dec(lib, wsb=16) == -6
+
+
+def test_workspace_size(lib):
+    ws = gb.attn_decode_workspace_size
+    # fixed splits: counter (256) + lse partials (rounded to 256) + O partials
+    rows = 4 * 64 * 16
+    assert ws(4, 64, 8, 32768, 128, 16) == 256 + ((rows * 4 + 255) // 256) * 256 + rows * 128 * 4
+    # automatic: one slot per 4096 keys of capacity
+    rows = 16 * 64 * 32
+    assert ws(16, 64, 8, 131072, 128, 0) == 256 + ((rows * 4 + 255) // 256) * 256 + rows * 128 * 4
+    assert ws(1, 1, 1, 1, 128, 0) > 0
+    assert ws(0, 64, 8, 10, 128, 0) == 0
+    assert ws(1, 64, 8, 10, 96, 0) == 0
+    assert ws(1, 64, 8, 10, 128, 300) == 0

@@ -1,0 +1,146 @@
+"""GPU parity of attn_fwd (bf16 tcgen05 path and fp32 path) against the fp64 oracle.
+
+All calls go through the C ABI (libgbattn.so) via the Python binding.  Inputs come from
+attn_workloads (seeded, CPU-generated); the oracle sees exactly the stored bytes.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attn_workloads as wl
+import oracle
+import streaming_attention_flashattention_gb300 as gb
+from _parity import compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from streaming_attention_flashattention_gb300 import build
+    build.build()
+    gb.load_library()
+    yield
+    st, word = gb.attn_last_device_error()
+    assert st == 0 and word == 0, f"device error word set: {word}"
+
+
+def run_gpu(q, k, v, causal, scale):
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = gb.attn_fwd(qd, kd, vd, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def check(w: wl.Workload, rows=None):
+    q, k, v = wl.prefill_inputs(w)
+    o, lse = run_gpu(q, k, v, w.causal, w.scale)
+    if rows is None:
+        o_ref, lse_ref = oracle.attention(wl.to_oracle(q), wl.to_oracle(k), wl.to_oracle(v),
+                                          w.scale, w.causal)
+        return compare(o, lse, o_ref, lse_ref, w.dtype, w.name)
+    o_ref, lse_ref = oracle.attention(wl.to_oracle(q), wl.to_oracle(k), wl.to_oracle(v),
+                                      w.scale, w.causal, rows=rows)
+    return compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, w.dtype,
+                   w.name)
+
+
+def small(B, Hq, Hkv, Sq, Skv, d, causal, dtype="bf16", seed=7, q_scale=1.0):
+    return wl.Workload(f"b{B}-h{Hq}/{Hkv}-s{Sq}x{Skv}-d{d}-{'c' if causal else 'nc'}-{dtype}",
+                       "prefill", B=B, Hq=Hq, Hkv=Hkv, d=d, dtype=dtype, Sq=Sq, Skv=Skv,
+                       causal=causal, seed=seed, q_scale=q_scale)
+
+
+# ---------------------------------------------------------------------------------------
+# fp32 path
+# ---------------------------------------------------------------------------------------
+
+def test_workload1_tiny_fp32():
+    check(wl.WORKLOADS[1])
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Skv,d,causal", [
+    (1, 2, 1, 128, 128, 64, True),
+    (2, 4, 2, 77, 200, 128, False),
+    (2, 4, 2, 77, 200, 128, True),
+    (1, 8, 1, 1, 33, 64, True),
+    (1, 1, 1, 300, 300, 128, True),
+])
+def test_fp32_shapes(B, Hq, Hkv, Sq, Skv, d, causal):
+    check(small(B, Hq, Hkv, Sq, Skv, d, causal, dtype="fp32"))
+
+
+# ---------------------------------------------------------------------------------------
+# bf16 tcgen05 path
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Skv,d,causal", [
+    (1, 2, 1, 128, 128, 128, False),   # one pair of Q tiles, one KV tile
+    (1, 2, 1, 128, 128, 128, True),
+    (1, 2, 2, 256, 256, 128, True),    # G = 1: pairs are consecutive q blocks
+    (1, 8, 2, 384, 384, 128, True),    # GQA G = 4
+    (2, 8, 1, 200, 200, 128, True),    # ragged tail, G = 8
+    (1, 4, 4, 129, 129, 128, False),   # one row past a tile
+    (1, 3, 1, 127, 255, 128, False),   # odd G, Sq != Skv
+    (1, 4, 2, 100, 300, 128, True),    # bottom-right causal with Sq < Skv
+    (1, 2, 1, 1, 1, 128, False),       # single query, single key
+    (1, 2, 1, 1, 517, 128, True),      # one query row at the end of a long context
+    (2, 4, 2, 256, 256, 64, True),     # d = 64
+    (1, 6, 3, 130, 1000, 64, False),
+])
+def test_bf16_shapes(B, Hq, Hkv, Sq, Skv, d, causal):
+    check(small(B, Hq, Hkv, Sq, Skv, d, causal))
+
+
+def test_bf16_sharp_softmax_rescale_path():
+    # Q scaled up so that the running max moves by more than 2^8 between tiles
+    check(small(1, 2, 1, 256, 1024, 128, True, q_scale=6.0, seed=11))
+
+
+def test_workload2_causal_gqa_prefill_full():
+    check(wl.WORKLOADS[2])
+
+
+@pytest.mark.slow
+def test_workload3_llama70b_prefill_sampled_rows():
+    w = wl.WORKLOADS[3]
+    rng = np.random.default_rng(3)
+    n_rows = w.B * w.Hq * w.Sq
+    rows = np.unique(np.concatenate([
+        rng.integers(0, n_rows, 1500),
+        np.arange(0, 128),                                   # head 0, first tile (diagonal)
+        (w.Hq - 1) * w.Sq + np.arange(w.Sq - 130, w.Sq),     # last head, last rows
+    ]))
+    check(w, rows=rows)
+
+
+def test_constant_v_and_causal_row0():
+    w = small(1, 4, 2, 256, 256, 128, True, seed=5)
+    q, k, v = wl.prefill_inputs(w)
+    v[:] = 0.8125                      # exactly representable in bf16
+    o, _ = run_gpu(q, k, v, True, w.scale)
+    assert np.abs(o - 0.8125).max() <= 1e-2
+    v2 = wl.prefill_inputs(w)[2]
+    o2, lse2 = run_gpu(q, k, v2, True, w.scale)
+    # causal row 0 sees key 0 only: O = V[0] exactly (p = 1), LSE = scale * q0 . k0
+    for h in range(4):
+        np.testing.assert_array_equal(o2[0, h, 0], v2[0, h // 2, 0].float().numpy())
+        dot = float((q[0, h, 0].double() * k[0, h // 2, 0].double()).sum())
+        assert abs(lse2[0, h, 0] - w.scale * dot) < 1e-3
+
+
+def test_deterministic_repeat():
+    w = small(1, 8, 2, 512, 512, 128, True, seed=9)
+    q, k, v = (t.cuda() for t in wl.prefill_inputs(w))
+    o1, l1 = gb.attn_fwd(q, k, v, causal=True)
+    o2, l2 = gb.attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_gpu_rejects_bad_arguments_without_launch():
+    q = torch.zeros(1, 2, 64, 96, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(gb.GbAttnError):
+        gb.attn_fwd(q, q[:, :1], q[:, :1], causal=False)
