@@ -217,6 +217,10 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 if (mbar_wait(&empty[stage], phase ^ 1u, kErrWaitProducer, p.err)) {
                     info[stage].done = 1;
                     mbar_arrive(&full[stage]);
+                    // the marker is this stage's newest phase: the drain must wait for it,
+                    // not for the older fill (whose parity the barrier has now passed twice)
+                    filled |= 1u << stage;
+                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                 }
             }
             // drain: never leave the CTA with a TMA copy still writing its shared memory
