@@ -21,8 +21,11 @@
 //   lane is wasted on padding heads).  The S^T accumulator fragment is turned into the
 //   P^T operand fragment in registers with movmatrix.  Each warp keeps its own running
 //   (m, l, O); at the end of a split the four states merge through shared memory and the
-//   normalised partial (lse_s, O_s / l_s) goes to the workspace.
-//   combine kernel: one warp per (b, query head) merges the partials of its splits.
+//   normalised partial (lse_s, O_s / l_s) goes to the workspace.  The merge of the splits
+//   is fused: each finished split bumps a per-(b, KV head, head chunk) counter, and the
+//   CTA that finishes the group's last split folds all partials into the final O and LSE
+//   (data-driven, no grid-wide barrier; "ADR-0060" section 4.3).  A group with a single
+//   split writes its result directly.
 //   Decode is HBM bound (8 flop per byte of KV), so these contractions stay on the
 //   warp-level tensor path; the streaming design is what sets the speed.
 #include "common.cuh"
@@ -41,6 +44,7 @@ constexpr int kHeads = 8;                  // query heads per work item (MMA N)
 struct StageInfo {
     int b, kvh, hc, s;
     int tile, ntok, last, done;
+    int n_ne, pad0, pad1, pad2;   // non-empty splits of the group
 };
 
 template <int D>
@@ -53,11 +57,12 @@ struct Layout {
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kInfoOff = kRingBytes;
     static constexpr int kBarOff = kInfoOff + kStages * (int)sizeof(StageInfo);
-    static constexpr int kNumBars = 2 * kStages + 2;
+    static constexpr int kNumBars = 2 * kStages + 3;
     static constexpr int kRedMOff = kBarOff + kNumBars * 8;
     static constexpr int kRedLOff = kRedMOff + kConsumerWarps * kHeads * 4;
     static constexpr int kRedOOff = kRedLOff + kConsumerWarps * kHeads * 4;
-    static constexpr int kBytes = kRedOOff + kConsumerWarps * kHeads * D * 4;
+    static constexpr int kFlagOff = kRedOOff + kConsumerWarps * kHeads * D * 4;
+    static constexpr int kBytes = kFlagOff + 16;
     static constexpr int kAlloc = kBytes + 1024;                // slack for 1024-B alignment
     static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
 };
@@ -110,10 +115,37 @@ __device__ __forceinline__ void split_range(int len, int n, int s, int& t0, int&
     t1 = (int)min((long long)len, a + c);
 }
 
+// Number of non-empty splits: the first ceil(len / C) of them.
+__device__ __forceinline__ int nonempty_splits(int len, int n) {
+    if (len <= 0) return 0;
+    int c = (len + n - 1) / n;
+    c = ((c + kSplitAlign - 1) / kSplitAlign) * kSplitAlign;
+    return (len + c - 1) / c;
+}
+
 __device__ __forceinline__ int splits_for(int len, int fixed_splits) {
     if (fixed_splits > 0) return fixed_splits;
     int n = (len + kAutoChunk - 1) / kAutoChunk;
     return max(1, min(kMaxSplits, n));
+}
+
+// Final output of one (b, query head): `per` consecutive columns of O (bf16) starting at
+// d0, plus the LSE (natural log) from its log2 value when `with_lse`.
+template <int per>
+__device__ __forceinline__ void store_final(const DecodeParams& p, long long row, int d0,
+                                            const float* ov, bool with_lse, float lse2) {
+    __nv_bfloat16* dst = p.o + row * (per * 16) + d0;
+    if constexpr (per == 8) {
+        uint4 w;
+        w.x = pack_bf16(ov[0], ov[1]); w.y = pack_bf16(ov[2], ov[3]);
+        w.z = pack_bf16(ov[4], ov[5]); w.w = pack_bf16(ov[6], ov[7]);
+        *reinterpret_cast<uint4*>(dst) = w;
+    } else {
+        uint2 w;
+        w.x = pack_bf16(ov[0], ov[1]); w.y = pack_bf16(ov[2], ov[3]);
+        *reinterpret_cast<uint2*>(dst) = w;
+    }
+    if (with_lse && p.lse != nullptr) p.lse[row] = lse2 * 0.69314718055994531f;
 }
 
 template <int D>
@@ -129,6 +161,8 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
     uint64_t* empty = bars + kStages;        // [kStages] consumers -> producer (4 arrivals)
     uint64_t* sync_a = bars + 2 * kStages;   // consumer-warp rendezvous at a split's end
     uint64_t* sync_b = sync_a + 1;
+    uint64_t* sync_c = sync_a + 2;
+    int* last_flag = reinterpret_cast<int*>(smem + L::kFlagOff);
     float* red_m = reinterpret_cast<float*>(smem + L::kRedMOff);
     float* red_l = reinterpret_cast<float*>(smem + L::kRedLOff);
     float* red_o = reinterpret_cast<float*>(smem + L::kRedOOff);
@@ -141,6 +175,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
         }
         mbar_init(sync_a, kConsumerWarps);
         mbar_init(sync_b, kConsumerWarps);
+        mbar_init(sync_c, kConsumerWarps);
         fence_barrier_init();
     }
     __syncthreads();
@@ -167,15 +202,23 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 len = max(0, min(len, p.Lmax));
                 const int nb = splits_for(len, p.fixed_splits);
                 if (s >= nb) continue;
-                int t0, t1;
-                split_range(len, nb, s, t0, t1);
+                const int n_ne = nonempty_splits(len, nb);
                 const int h0 = kvh * p.G + hc * kHeads;
                 const int gcnt = min(kHeads, p.G - hc * kHeads);
-                if (t1 <= t0) {      // empty split: its partial carries no weight
-                    for (int g = 0; g < gcnt; ++g)
-                        p.ws_lse[((long long)b * p.Hq + h0 + g) * p.n_slots + s] = -INFINITY;
+                if (s >= n_ne) {
+                    // empty split: no partial.  A sequence with no keys at all gets
+                    // O = 0, LSE = -inf from its split 0.
+                    if (s == 0) {
+                        for (int g = 0; g < gcnt; ++g) {
+                            uint4* dst = reinterpret_cast<uint4*>(p.o + ((long long)b * p.Hq + h0 + g) * D);
+                            for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+                            if (p.lse != nullptr) p.lse[(long long)b * p.Hq + h0 + g] = -INFINITY;
+                        }
+                    }
                     continue;
                 }
+                int t0, t1;
+                split_range(len, nb, s, t0, t1);
                 const int ntiles = (t1 - t0 + kKeysPerStage - 1) / kKeysPerStage;
                 const int zkv = b * p.Hkv + kvh;
                 for (int tile = 0; tile < ntiles; ++tile) {
@@ -190,6 +233,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                     si.ntok = min(kKeysPerStage, t1 - y);
                     si.last = (tile == ntiles - 1);
                     si.done = 0;
+                    si.n_ne = n_ne;
                     uint8_t* st = smem + stage * L::kStageBytes;
                     const uint32_t bytes = L::kKBytes + L::kVBytes + (tile == 0 ? L::kQBytes : 0);
                     mbar_arrive_expect_tx(&full[stage], bytes);
@@ -236,7 +280,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
         float acc[D / 16][4];
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
         int stage = 0;
-        uint32_t phase = 0, sync_phase = 0;
+        uint32_t phase = 0, sync_phase = 0, sync_c_phase = 0;
         const int R0 = warp * 16;   // this warp's 16 keys within a stage
         while (true) {
             if (!mbar_wait(&full[stage], phase, kErrWaitConsumer, p.err)) break;
@@ -366,104 +410,89 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sync_a);
                 if (!mbar_wait(sync_a, sync_phase, kErrWaitConsumer, p.err)) break;
-                {
-                    const int t = threadIdx.x;          // 0..127
-                    const int head = t >> 4;
-                    constexpr int per = D / 16;
-                    const int d0 = (t & 15) * per;
-                    if (head < gcnt) {
-                        float M = -INFINITY;
+                const int t = threadIdx.x;              // 0..127
+                const int head = t >> 4;
+                constexpr int per = D / 16;
+                const int d0 = (t & 15) * per;
+                const int hq = si.kvh * p.G + si.hc * kHeads + head;
+                const long long row = (long long)si.b * p.Hq + hq;
+                if (head < gcnt) {
+                    float M = -INFINITY;
+                    #pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * kHeads + head]);
+                    float wt[kConsumerWarps], Ltot = 0.f;
+                    #pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) {
+                        const float mw = red_m[w * kHeads + head];
+                        wt[w] = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
+                        Ltot += wt[w] * red_l[w * kHeads + head];
+                    }
+                    const float inv = 1.f / Ltot;
+                    float ov[per];
+                    #pragma unroll
+                    for (int u = 0; u < per; ++u) {
+                        float sum = 0.f;
                         #pragma unroll
-                        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * kHeads + head]);
-                        float wt[kConsumerWarps], Ltot = 0.f;
-                        #pragma unroll
-                        for (int w = 0; w < kConsumerWarps; ++w) {
-                            const float mw = red_m[w * kHeads + head];
-                            wt[w] = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
-                            Ltot += wt[w] * red_l[w * kHeads + head];
-                        }
-                        const float inv = 1.f / Ltot;
-                        const int hq = si.kvh * p.G + si.hc * kHeads + head;
-                        const long long slot = ((long long)si.b * p.Hq + hq) * p.n_slots + si.s;
+                        for (int w = 0; w < kConsumerWarps; ++w)
+                            sum += wt[w] * red_o[(w * kHeads + head) * D + d0 + u];
+                        ov[u] = sum * inv;
+                    }
+                    if (si.n_ne == 1) {
+                        store_final<per>(p, row, d0, ov, (t & 15) == 0, M + __log2f(Ltot));
+                    } else {
+                        const long long slot = row * p.n_slots + si.s;
                         float* dst = p.ws_o + slot * D + d0;
                         #pragma unroll
-                        for (int e = 0; e < per; e += 4) {
-                            float4 r;
-                            float* rr = &r.x;
-                            #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                float sum = 0.f;
-                                #pragma unroll
-                                for (int w = 0; w < kConsumerWarps; ++w)
-                                    sum += wt[w] * red_o[(w * kHeads + head) * D + d0 + e + u];
-                                rr[u] = sum * inv;
-                            }
-                            *reinterpret_cast<float4*>(dst + e) = r;
-                        }
+                        for (int e = 0; e < per; e += 4)
+                            *reinterpret_cast<float4*>(dst + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
                         if ((t & 15) == 0) p.ws_lse[slot] = M + __log2f(Ltot);
+                        __threadfence();
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sync_b);
                 if (!mbar_wait(sync_b, sync_phase, kErrWaitConsumer, p.err)) break;
                 sync_phase ^= 1u;
+                if (si.n_ne > 1) {
+                    // count this split in; the CTA that completes the group merges it
+                    if (t == 0) {
+                        int* cnt = p.group_cnt + (si.b * p.Hkv + si.kvh) * p.n_hc + si.hc;
+                        *last_flag = (atomicAdd(cnt, 1) == si.n_ne - 1);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sync_c);
+                    if (!mbar_wait(sync_c, sync_c_phase, kErrWaitConsumer, p.err)) break;
+                    sync_c_phase ^= 1u;
+                    if (*last_flag && head < gcnt) {
+                        __threadfence();
+                        const float* lse_s = p.ws_lse + row * p.n_slots;
+                        const float* o_s = p.ws_o + row * p.n_slots * D + d0;
+                        float M = -INFINITY;
+                        for (int s2 = 0; s2 < si.n_ne; ++s2) M = fmaxf(M, __ldcg(lse_s + s2));
+                        float acc2[per], Ltot = 0.f;
+                        #pragma unroll
+                        for (int u = 0; u < per; ++u) acc2[u] = 0.f;
+                        for (int s2 = 0; s2 < si.n_ne; ++s2) {
+                            const float w = ex2_approx(__ldcg(lse_s + s2) - M);
+                            Ltot += w;
+                            #pragma unroll
+                            for (int e = 0; e < per; e += 4) {
+                                const float4 x = __ldcg(reinterpret_cast<const float4*>(o_s + (long long)s2 * D + e));
+                                acc2[e] += w * x.x; acc2[e + 1] += w * x.y;
+                                acc2[e + 2] += w * x.z; acc2[e + 3] += w * x.w;
+                            }
+                        }
+                        const float inv = 1.f / Ltot;
+                        #pragma unroll
+                        for (int u = 0; u < per; ++u) acc2[u] *= inv;
+                        store_final<per>(p, row, d0, acc2, (t & 15) == 0, M + __log2f(Ltot));
+                    }
+                }
             }
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
     }
     __syncthreads();
-}
-
-// One warp per (b, query head): O = sum_s w_s O_s / sum_s w_s, w_s = 2^(lse_s - max lse).
-template <int D>
-__global__ void __launch_bounds__(256)
-decode_combine_kernel(const __grid_constant__ DecodeParams p) {
-    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= p.B * p.Hq) return;
-    const int b = gw / p.Hq;
-    int len = __ldg(&p.kv_lens[b]);
-    len = max(0, min(len, p.Lmax));
-    const int nb = splits_for(len, p.fixed_splits);
-    const float* lse_s = p.ws_lse + (long long)gw * p.n_slots;
-    const float* o_s = p.ws_o + (long long)gw * p.n_slots * D;
-    float M = -INFINITY;
-    for (int s = lane; s < nb; s += 32) M = fmaxf(M, lse_s[s]);
-    #pragma unroll
-    for (int w = 16; w > 0; w >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, w));
-    constexpr int per = D / 32;
-    float acc[per];
-    #pragma unroll
-    for (int e = 0; e < per; ++e) acc[e] = 0.f;
-    float Ltot = 0.f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < nb; ++s) {
-            const float ls = lse_s[s];
-            if (ls == -INFINITY) continue;
-            const float w = ex2_approx(ls - M);
-            Ltot += w;
-            const float* src = o_s + (long long)s * D + lane * per;
-            if constexpr (per == 4) {
-                const float4 x = *reinterpret_cast<const float4*>(src);
-                acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
-            } else {
-                const float2 x = *reinterpret_cast<const float2*>(src);
-                acc[0] += w * x.x; acc[1] += w * x.y;
-            }
-        }
-    }
-    const float inv = Ltot > 0.f ? 1.f / Ltot : 0.f;
-    __nv_bfloat16* dst = p.o + (long long)gw * D + lane * per;
-    if constexpr (per == 4) {
-        uint2 packed;
-        packed.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-        packed.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-        *reinterpret_cast<uint2*>(dst) = packed;
-    } else {
-        *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
-    }
-    if (p.lse != nullptr && lane == 0)
-        p.lse[gw] = (Ltot > 0.f) ? (M + __log2f(Ltot)) * 0.69314718055994531f : -INFINITY;
 }
 
 }  // namespace
@@ -474,9 +503,14 @@ int decode_slots(int Lmax, int num_splits) {
     return n < 1 ? 1 : (n > kMaxSplits ? kMaxSplits : n);
 }
 
-size_t decode_workspace_bytes(int B, int Hq, int d, int n_slots) {
+size_t decode_counter_bytes(int B, int Hkv, int n_hc) {
+    return (((size_t)1 + (size_t)B * Hkv * n_hc) * 4 + 255) / 256 * 256;
+}
+
+size_t decode_workspace_bytes(int B, int Hq, int Hkv, int d, int n_slots) {
+    const int n_hc = (Hq / Hkv + 7) / 8;
     const size_t rows = (size_t)B * Hq * n_slots;
-    size_t bytes = 256;                                  // work counter
+    size_t bytes = decode_counter_bytes(B, Hkv, n_hc);   // work queue + group counters
     bytes += ((rows * 4 + 255) / 256) * 256;             // lse partials
     bytes += rows * (size_t)d * 4;                       // O partials
     return bytes;
@@ -484,37 +518,23 @@ size_t decode_workspace_bytes(int B, int Hq, int d, int n_slots) {
 
 cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
                                   cudaStream_t stream) {
-    cudaError_t err = cudaMemsetAsync(p.counter, 0, sizeof(int), stream);
+    cudaError_t err = cudaMemsetAsync(p.counter, 0, decode_counter_bytes(p.B, p.Hkv, p.n_hc),
+                                      stream);
     if (err != cudaSuccess) return err;
     const int grid = p.n_items < num_sms ? p.n_items : num_sms;
+    if (grid <= 0) return cudaSuccess;
     if (d == 128) {
         constexpr int smem = Layout<128>::kAlloc;
-        static bool attr = false;
-        if (!attr) {
-            err = cudaFuncSetAttribute(decode_split_kernel<128>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            if (err != cudaSuccess) return err;
-            attr = true;
-        }
-        if (grid > 0) decode_split_kernel<128><<<grid, kThreads, smem, stream>>>(p);
-        err = cudaGetLastError();
+        err = cudaFuncSetAttribute(decode_split_kernel<128>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (err != cudaSuccess) return err;
-        const int cblocks = (p.B * p.Hq + 7) / 8;
-        decode_combine_kernel<128><<<cblocks, 256, 0, stream>>>(p);
+        decode_split_kernel<128><<<grid, kThreads, smem, stream>>>(p);
     } else {
         constexpr int smem = Layout<64>::kAlloc;
-        static bool attr = false;
-        if (!attr) {
-            err = cudaFuncSetAttribute(decode_split_kernel<64>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            if (err != cudaSuccess) return err;
-            attr = true;
-        }
-        if (grid > 0) decode_split_kernel<64><<<grid, kThreads, smem, stream>>>(p);
-        err = cudaGetLastError();
+        err = cudaFuncSetAttribute(decode_split_kernel<64>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (err != cudaSuccess) return err;
-        const int cblocks = (p.B * p.Hq + 7) / 8;
-        decode_combine_kernel<64><<<cblocks, 256, 0, stream>>>(p);
+        decode_split_kernel<64><<<grid, kThreads, smem, stream>>>(p);
     }
     return cudaGetLastError();
 }

@@ -182,52 +182,73 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
         }
     } else if (warp == 1) {
         // ================================= MMA issuer =================================
+        // Tensor-pipe order (ping-pong between the two Q tiles):
+        //   S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) S0(2) PV1(1) S1(2) | ...
+        // While softmax 0 works on S0(j+1) the pipe runs PV1(j) and S1(j+1), and the other
+        // way round, so neither softmax leaves the tensor cores idle.  S_t(j+1) overwrites
+        // P_t(j) in TMEM; it is issued after PV_t(j), and tcgen05.mma executes in order.
         if (lane == 0) {
             constexpr uint32_t idesc_s = make_idesc_bf16(kBlockM, kBlockN, 0, 0);
             constexpr uint32_t idesc_pv = make_idesc_bf16(kBlockM, D, 0, 1);
             const uint32_t q_base = smem_u32(smem + L::kQ0);
             const uint32_t k_base = smem_u32(smem + L::kK0);
             const uint32_t v_base = smem_u32(smem + L::kV0);
-            const uint32_t col_s[2] = {L::kColS0, L::kColS1};
-            const uint32_t col_o[2] = {L::kColO0, L::kColO1};
+            const int n0 = td[0].n_kv, n1 = td[1].n_kv;
+
+            auto issue_s = [&](int t, int j) {
+                const uint32_t qa = q_base + t * L::kTileBytes;
+                const uint32_t kb = k_base + (j & 1) * L::kTileBytes;
+                const uint32_t dst = tmem + (t == 0 ? L::kColS0 : L::kColS1);
+                #pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
+                    mma_bf16_ss(dst, make_sdesc_sw128(qa + off, 16, 1024),
+                                make_sdesc_sw128(kb + off, 16, 1024), idesc_s, kk > 0);
+                }
+                mma_commit(&s_full[t]);
+            };
+            auto issue_pv = [&](int t, int j) -> bool {
+                if (!mbar_wait(&p_ready[t], j & 1, kErrWaitMma, p.err)) return false;
+                tc_fence_after();
+                const uint32_t vb = v_base + (j & 1) * L::kTileBytes;
+                const uint32_t col_s = t == 0 ? L::kColS0 : L::kColS1;
+                const uint32_t dst = tmem + (t == 0 ? L::kColO0 : L::kColO1);
+                #pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    mma_bf16_ts(dst, tmem + col_s + kk * 8,
+                                make_sdesc_sw128(vb + kk * 16 * 128, L::kBoxBytes, 1024),
+                                idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&o_done[t]);
+                return true;
+            };
+
             bool ok = mbar_wait(q_full, 0, kErrWaitMma, p.err);
             tc_fence_after();
+            if (ok && n_kv_max > 0) {
+                ok = mbar_wait(&k_full[0], 0, kErrWaitMma, p.err);
+                tc_fence_after();
+                if (ok) {
+                    if (n0 > 0) issue_s(0, 0);
+                    if (n1 > 0) issue_s(1, 0);
+                    mma_commit(&k_empty[0]);
+                }
+            }
             for (int j = 0; j < n_kv_max && ok; ++j) {
-                const int slot = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
-                if (!mbar_wait(&k_full[slot], ph, kErrWaitMma, p.err)) break;
+                const bool next = j + 1 < n_kv_max;
+                if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, kErrWaitMma, p.err)) break;
                 tc_fence_after();
-                #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (j >= td[t].n_kv) continue;
-                    const uint32_t qa = q_base + t * L::kTileBytes;
-                    const uint32_t kb = k_base + slot * L::kTileBytes;
-                    #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                        mma_bf16_ss(tmem + col_s[t], make_sdesc_sw128(qa + off, 16, 1024),
-                                    make_sdesc_sw128(kb + off, 16, 1024), idesc_s, kk > 0);
-                    }
-                    mma_commit(&s_full[t]);
-                }
-                mma_commit(&k_empty[slot]);
-                if (!mbar_wait(&v_full[slot], ph, kErrWaitMma, p.err)) break;
-                tc_fence_after();
-                #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (j >= td[t].n_kv) continue;
-                    if (!mbar_wait(&p_ready[t], j & 1, kErrWaitMma, p.err)) { ok = false; break; }
+                if (j < n0 && !issue_pv(0, j)) break;
+                if (next) {
+                    if (!mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, kErrWaitMma, p.err)) break;
                     tc_fence_after();
-                    const uint32_t vb = v_base + slot * L::kTileBytes;
-                    #pragma unroll
-                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                        mma_bf16_ts(tmem + col_o[t], tmem + col_s[t] + kk * 8,
-                                    make_sdesc_sw128(vb + kk * 16 * 128, L::kBoxBytes, 1024),
-                                    idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(&o_done[t]);
+                    if (j + 1 < n0) issue_s(0, j + 1);
                 }
-                mma_commit(&v_empty[slot]);
+                if (j < n1 && !issue_pv(1, j)) break;
+                mma_commit(&v_empty[j & 1]);
+                if (next) {
+                    if (j + 1 < n1) issue_s(1, j + 1);
+                    mma_commit(&k_empty[(j + 1) & 1]);
+                }
             }
         }
     } else if (warp >= kSoftmaxWarp0) {
@@ -251,49 +272,43 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
                 tc_fence_after();
                 const int kbase = j * kBlockN;
                 const bool masked = kbase + kBlockN > lim;
-                // pass 1: row max of the raw scores
-                float mx = -INFINITY;
-                #pragma unroll
-                for (int ch = 0; ch < kBlockN / 32; ++ch) {
-                    uint32_t rr[32];
-                    tmem_ld32(t_s + ch * 32, rr);
-                    tmem_wait_ld();
-                    if (!masked) {
-                        #pragma unroll
-                        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(rr[e]));
-                    } else {
-                        #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (kbase + ch * 32 + e < lim) mx = fmaxf(mx, __uint_as_float(rr[e]));
-                    }
+                uint32_t sr[kBlockN];
+                tmem_ld128(t_s, sr);
+                if (masked) {
+                    #pragma unroll
+                    for (int e = 0; e < kBlockN; ++e)
+                        if (kbase + e >= lim) sr[e] = __float_as_uint(-INFINITY);
                 }
+                // row max of the raw scores (4 independent chains)
+                float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+                float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+                #pragma unroll
+                for (int e = 4; e < kBlockN; e += 4) {
+                    mx0 = fmaxf(mx0, __uint_as_float(sr[e]));
+                    mx1 = fmaxf(mx1, __uint_as_float(sr[e + 1]));
+                    mx2 = fmaxf(mx2, __uint_as_float(sr[e + 2]));
+                    mx3 = fmaxf(mx3, __uint_as_float(sr[e + 3]));
+                }
+                const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
                 const float mt = mx * c;
                 float m_new = m;
                 if (mt > m + kRescaleThreshold) m_new = mt;   // also taken when m = -inf
                 const float base = (m_new == -INFINITY) ? 0.f : m_new;
                 const float corr = (m == -INFINITY) ? 0.f : ex2_approx(m - base);
                 const float nb = -base;
-                // pass 2: P = 2^(s*c - m), row sum, P -> bf16 over S in TMEM
-                float sum = 0.f;
+                // P = 2^(s*c - m), row sum, P -> bf16 over S in TMEM
+                float sum0 = 0.f, sum1 = 0.f;
+                uint32_t pk[kBlockN / 2];
                 #pragma unroll
-                for (int ch = 0; ch < kBlockN / 32; ++ch) {
-                    uint32_t rr[32];
-                    tmem_ld32(t_s + ch * 32, rr);
-                    tmem_wait_ld();
-                    uint32_t pk[16];
-                    #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float p0 = ex2_approx(fmaf(__uint_as_float(rr[e]), c, nb));
-                        float p1 = ex2_approx(fmaf(__uint_as_float(rr[e + 1]), c, nb));
-                        if (masked) {
-                            if (kbase + ch * 32 + e >= lim) p0 = 0.f;
-                            if (kbase + ch * 32 + e + 1 >= lim) p1 = 0.f;
-                        }
-                        sum += p0 + p1;
-                        pk[e >> 1] = pack_bf16(p0, p1);
-                    }
-                    tmem_st16(t_s + ch * 16, pk);
+                for (int e = 0; e < kBlockN; e += 2) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[e]), c, nb));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), c, nb));
+                    sum0 += p0;
+                    sum1 += p1;
+                    pk[e >> 1] = pack_bf16(p0, p1);
                 }
+                const float sum = sum0 + sum1;
+                tmem_st64(t_s, pk);
                 tmem_wait_st();
                 l = l * corr + sum;
                 m = m_new;
