@@ -121,6 +121,29 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
                         size_t ws_bytes, void* stream);
 
 /*
+ * attn_decode_splitkv_noalloc -- attn_decode_splitkv for callers that cannot allocate
+ * device memory, so cannot pass a workspace: a plugin inside a framework that owns all
+ * device allocations and offers no scratch, or a serving loop that must not allocate
+ * once running because an allocation can synchronise the device.  The pages describe
+ * no counterpart; this is a library-level addition.
+ *
+ * Same arguments, layouts and results as attn_decode_splitkv, without the workspace.
+ * The scratch is a fixed 8 MiB array inside the library (reserved on every GPU that
+ * loads the library, until the process exits).  The call allocates nothing itself.
+ *  - Sizes whose attn_decode_workspace_size(...) exceeds 8 MiB (8388608 bytes) are
+ *    rejected with GBATTN_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the array's device address for that device;
+ *    make that first call before any stream capture starts.
+ *  - Every call shares the one array: calls whose GPU work may overlap (different
+ *    streams, or unordered host threads) race and give wrong results.  The counters
+ *    that must start at zero are cleared on `stream` by each call.
+ */
+int attn_decode_splitkv_noalloc(const void* q, const void* kcache, const void* vcache,
+                                const int* kv_lens, void* o, float* lse, int B, int Hq,
+                                int Hkv, int Lmax, int d, float scale, int num_splits,
+                                void* stream);
+
+/*
  * attn_last_device_error -- synchronise `stream`, then read and clear the device error
  * word that bounded waits inside the kernels set when they give up (they never trap).
  * Returns GBATTN_OK, GBATTN_ERR_TIMEOUT (the word was set) or GBATTN_ERR_CUDA.

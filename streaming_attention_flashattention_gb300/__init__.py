@@ -41,6 +41,7 @@ EXPORTS = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "attn_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "attn_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "attn_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_last_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_int)]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_version": (_I, []),
@@ -176,6 +177,34 @@ def attn_decode_splitkv(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Ten
                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                  _stream_ptr(stream))
     _check("attn_decode_splitkv", st)
+    return out, lse
+
+
+# Scratch the no-allocation decode entry point holds (bytes), as documented in gbattn.h.
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def attn_decode_splitkv_noalloc(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
+                                kv_lens: torch.Tensor, out: torch.Tensor,
+                                lse: torch.Tensor, num_splits: int = 0,
+                                scale: float | None = None, stream=None):
+    """attn_decode_splitkv without a workspace: the library's own fixed scratch is used, so
+    nothing is allocated (the caller passes preallocated `out` and `lse`).  Calls must be
+    ordered on one stream; see include/gbattn.h."""
+    lib = load_library()
+    for n, t in (("q", q), ("kcache", kcache), ("vcache", vcache), ("out", out)):
+        _dev_tensor(n, t, (torch.bfloat16,))
+    _dev_tensor("kv_lens", kv_lens, (torch.int32,))
+    _dev_tensor("lse", lse, (torch.float32,))
+    B, Hq, _, d = q.shape
+    _, Hkv, Lmax, _ = kcache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = lib.attn_decode_splitkv_noalloc(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
+                                         kv_lens.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                         B, Hq, Hkv, Lmax, d, float(scale), int(num_splits),
+                                         _stream_ptr(stream))
+    _check("attn_decode_splitkv_noalloc", st)
     return out, lse
 
 
