@@ -11,8 +11,8 @@ Printed JSON line (rank 0):
   e2e        the same metric with pinned-host inputs copied in and outputs copied out
              inside the timed region, every step
   cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload
-L2 is flushed (512 MiB write) before the prefill and again before the decode of every
-step, outside the kernels' event windows.
+L2 is flushed (a 512 MiB write, then a read of it so no dirty lines remain) before the
+prefill and again before the decode of every step, outside the kernels' event windows.
 
 --impl reference times the fp64 CPU oracle instead (a bounded row sample per step).
 Multi-GPU (torchrun, N > 1): N independent replicas, weak scaling, no collective on the
@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_FLUSH_BYTES = 512 << 20
 # DRAM bytes per launch from the committed ncu captures (profiles/); None when the kernel
 # changed after the capture.
-NCU_TRAFFIC = {"prefill": None, "decode": None}
+NCU_TRAFFIC = {"prefill": 266_901_760, "decode": None}
 
 
 def prefill_flops(w: wl.Workload) -> float:
@@ -193,7 +193,7 @@ def config_dict(args):
                         "q_scale": PREFILL.q_scale},
             "decode": {"B": DECODE.B, "Hq": DECODE.Hq, "Hkv": DECODE.Hkv, "kv_len": DECODE.len_hi,
                        "d": DECODE.d, "num_splits": DECODE.num_splits},
-            "parallelism": f"replicas{args.gpus}", "l2": "flushed before each of the two calls of every step (512 MiB write)"}
+            "parallelism": f"replicas{args.gpus}", "l2": "flushed before each of the two calls of every step (512 MiB write, then read back)"}
 
 
 # ---------------------------------------------------------------------------------------
@@ -224,7 +224,17 @@ def run_gpu(args, rank, world, local_rank):
     ws = torch.empty(gb.attn_decode_workspace_size(DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.Skv,
                                                    DECODE.d, DECODE.num_splits),
                      dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    class _Flush:
+        """Evict L2: write a buffer 4x its size, then read it back so that no dirty
+        lines are left for the next timed kernel to write back."""
+
+        def zero_(self):
+            flush_buf.zero_()
+            flush_buf.sum()
+
+    flush = _Flush()
     stream = torch.cuda.current_stream(dev)
 
     def step(evs=None):

@@ -37,6 +37,7 @@ constexpr int kBlockN = 128;              // keys per K/V tile
 constexpr int kThreads = 12 * 32;
 constexpr int kSoftmaxWarp0 = 4;          // warps 4..7 -> tile 0, 8..11 -> tile 1
 constexpr float kRescaleThreshold = 8.0f; // log2 units: rescale O only if max grows > 2^8
+static_assert(kBlockN == 128, "the softmax row reductions assume 128 columns");
 
 template <int D>
 struct PLayout {
@@ -279,32 +280,35 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
                     for (int e = 0; e < kBlockN; ++e)
                         if (kbase + e >= lim) sr[e] = __float_as_uint(-INFINITY);
                 }
-                // row max of the raw scores (4 independent chains)
-                float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-                float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+                // row max of the raw scores: 4 independent chains of 3-input max, chain k
+                // covering columns [32k, 32k + 32)
+                float mxc[4];
                 #pragma unroll
-                for (int e = 4; e < kBlockN; e += 4) {
-                    mx0 = fmaxf(mx0, __uint_as_float(sr[e]));
-                    mx1 = fmaxf(mx1, __uint_as_float(sr[e + 1]));
-                    mx2 = fmaxf(mx2, __uint_as_float(sr[e + 2]));
-                    mx3 = fmaxf(mx3, __uint_as_float(sr[e + 3]));
+                for (int k = 0; k < 4; ++k) {
+                    float v = fmaxf(__uint_as_float(sr[32 * k]), __uint_as_float(sr[32 * k + 1]));
+                    #pragma unroll
+                    for (int i = 2; i < 32; i += 2)
+                        v = fmax3(v, __uint_as_float(sr[32 * k + i]), __uint_as_float(sr[32 * k + i + 1]));
+                    mxc[k] = v;
                 }
-                const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+                const float mx0 = mxc[0], mx1 = mxc[1], mx2 = mxc[2], mx3 = mxc[3];
+                const float mx = fmax3(mx0, mx1, fmaxf(mx2, mx3));
                 const float mt = mx * c;
                 float m_new = m;
                 if (mt > m + kRescaleThreshold) m_new = mt;   // also taken when m = -inf
                 const float base = (m_new == -INFINITY) ? 0.f : m_new;
                 const float corr = (m == -INFINITY) ? 0.f : ex2_approx(m - base);
                 const float nb = -base;
-                // P = 2^(s*c - m), row sum, P -> bf16 over S in TMEM
+                // P = 2^(s*c - m) (packed fp32x2 FMA for the argument), row sum, P -> bf16
                 float sum0 = 0.f, sum1 = 0.f;
                 uint32_t pk[kBlockN / 2];
                 #pragma unroll
                 for (int e = 0; e < kBlockN; e += 2) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[e]), c, nb));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), c, nb));
-                    sum0 += p0;
-                    sum1 += p1;
+                    float a0, a1;
+                    fma2(a0, a1, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]), c, c, nb, nb);
+                    const float p0 = ex2_approx(a0);
+                    const float p1 = ex2_approx(a1);
+                    add2(sum0, sum1, p0, p1);
                     pk[e >> 1] = pack_bf16(p0, p1);
                 }
                 const float sum = sum0 + sum1;
