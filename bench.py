@@ -354,14 +354,14 @@ def run_gpu(args, rank, world, local_rank):
                    "roofline": {"bound": "hbm", "achieved": per_gpu_bw, "peak": peak_bw,
                                 "unit": "GB/s", "frac": per_gpu_bw / peak_bw,
                                 "traffic": NCU_TRAFFIC["decode"],
-                                "kernel": "decode_split_kernel<128> (split-KV + fused LSE merge)",
+                                "kernel": "decode_split_kernel<128> + decode_combine_kernel<128> (PDL)",
                                 "peak_source": f"{peak_src} HBM copy"}},
         "e2e": {"value": (flops / (e2e_pre * 1e-3) / 1e12 * world) if not args.no_e2e else None,
                 "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "decode_gbs": (dbytes / (e2e_dec * 1e-3) / 1e9 * world) if not args.no_e2e else None,
                 "ms_per_step": e2e_pre + e2e_dec},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:

@@ -21,11 +21,14 @@
 //   lane is wasted on padding heads).  The S^T accumulator fragment is turned into the
 //   P^T operand fragment in registers with movmatrix.  Each warp keeps its own running
 //   (m, l, O); at the end of a split the four states merge through shared memory and the
-//   normalised partial (lse_s, O_s / l_s) goes to the workspace.  The merge of the splits
-//   is fused: each finished split bumps a per-(b, KV head, head chunk) counter, and the
-//   CTA that finishes the group's last split folds all partials into the final O and LSE
-//   (data-driven, no grid-wide barrier; "ADR-0060" section 4.3).  A group with a single
-//   split writes its result directly.
+//   normalised partial (lse_s, O_s / l_s) goes to the workspace; a group with a single
+//   split writes its final O and LSE directly.
+//   combine kernel: one thread per (b, query head, 4 output columns) folds the partials of
+//   the splits.  It is launched with programmatic dependent launch: its CTAs are
+//   scheduled while the split kernel drains and wait on the device (griddepcontrol.wait)
+//   for the partials, so no launch gap sits between the two.  Keeping the merge out of the
+//   split kernel keeps fences and atomics off the consumer warps, whose stalls would stop
+//   the TMA ring.
 //   Decode is HBM bound (8 flop per byte of KV), so these contractions stay on the
 //   warp-level tensor path; the streaming design is what sets the speed.
 #include "common.cuh"
@@ -44,7 +47,7 @@ constexpr int kHeads = 8;                  // query heads per work item (MMA N)
 struct StageInfo {
     int b, kvh, hc, s;
     int tile, ntok, last, done;
-    int n_ne, pad0, pad1, pad2;   // non-empty splits of the group
+    int n_ne, pad0, pad1, pad2;   // non-empty splits of the sequence
 };
 
 template <int D>
@@ -57,12 +60,11 @@ struct Layout {
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kInfoOff = kRingBytes;
     static constexpr int kBarOff = kInfoOff + kStages * (int)sizeof(StageInfo);
-    static constexpr int kNumBars = 2 * kStages + 3;
+    static constexpr int kNumBars = 2 * kStages + 2;
     static constexpr int kRedMOff = kBarOff + kNumBars * 8;
     static constexpr int kRedLOff = kRedMOff + kConsumerWarps * kHeads * 4;
     static constexpr int kRedOOff = kRedLOff + kConsumerWarps * kHeads * 4;
-    static constexpr int kFlagOff = kRedOOff + kConsumerWarps * kHeads * D * 4;
-    static constexpr int kBytes = kFlagOff + 16;
+    static constexpr int kBytes = kRedOOff + kConsumerWarps * kHeads * D * 4;
     static constexpr int kAlloc = kBytes + 1024;                // slack for 1024-B alignment
     static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
 };
@@ -161,8 +163,6 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
     uint64_t* empty = bars + kStages;        // [kStages] consumers -> producer (4 arrivals)
     uint64_t* sync_a = bars + 2 * kStages;   // consumer-warp rendezvous at a split's end
     uint64_t* sync_b = sync_a + 1;
-    uint64_t* sync_c = sync_a + 2;
-    int* last_flag = reinterpret_cast<int*>(smem + L::kFlagOff);
     float* red_m = reinterpret_cast<float*>(smem + L::kRedMOff);
     float* red_l = reinterpret_cast<float*>(smem + L::kRedLOff);
     float* red_o = reinterpret_cast<float*>(smem + L::kRedOOff);
@@ -175,7 +175,6 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
         }
         mbar_init(sync_a, kConsumerWarps);
         mbar_init(sync_b, kConsumerWarps);
-        mbar_init(sync_c, kConsumerWarps);
         fence_barrier_init();
     }
     __syncthreads();
@@ -193,11 +192,13 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
             while (ok) {
                 const int item = atomicAdd(p.counter, 1);
                 if (item >= p.n_items) break;
+                // group-major order (split innermost): a group's splits run side by side on
+                // different CTAs
                 int rem = item;
+                const int s = rem % p.n_slots; rem /= p.n_slots;
                 const int hc = rem % p.n_hc; rem /= p.n_hc;
                 const int kvh = rem % p.Hkv; rem /= p.Hkv;
-                const int b = rem % p.B; rem /= p.B;
-                const int s = rem;
+                const int b = rem;
                 int len = __ldg(&p.kv_lens[b]);
                 len = max(0, min(len, p.Lmax));
                 const int nb = splits_for(len, p.fixed_splits);
@@ -267,6 +268,8 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                 }
             }
+            // this CTA takes no more work: let the combine grid start being scheduled
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             // drain: never leave the CTA with a TMA copy still writing its shared memory
             for (int i = 0; i < kStages; ++i)
                 if (filled & (1u << i)) mbar_wait(&full[i], (fill_parity >> i) & 1u, kErrWaitDrain, p.err);
@@ -280,7 +283,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
         float acc[D / 16][4];
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
         int stage = 0;
-        uint32_t phase = 0, sync_phase = 0, sync_c_phase = 0;
+        uint32_t phase = 0, sync_phase = 0;
         const int R0 = warp * 16;   // this warp's 16 keys within a stage
         while (true) {
             if (!mbar_wait(&full[stage], phase, kErrWaitConsumer, p.err)) break;
@@ -446,53 +449,71 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                         for (int e = 0; e < per; e += 4)
                             *reinterpret_cast<float4*>(dst + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
                         if ((t & 15) == 0) p.ws_lse[slot] = M + __log2f(Ltot);
-                        __threadfence();
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sync_b);
                 if (!mbar_wait(sync_b, sync_phase, kErrWaitConsumer, p.err)) break;
                 sync_phase ^= 1u;
-                if (si.n_ne > 1) {
-                    // count this split in; the CTA that completes the group merges it
-                    if (t == 0) {
-                        int* cnt = p.group_cnt + (si.b * p.Hkv + si.kvh) * p.n_hc + si.hc;
-                        *last_flag = (atomicAdd(cnt, 1) == si.n_ne - 1);
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(sync_c);
-                    if (!mbar_wait(sync_c, sync_c_phase, kErrWaitConsumer, p.err)) break;
-                    sync_c_phase ^= 1u;
-                    if (*last_flag && head < gcnt) {
-                        __threadfence();
-                        const float* lse_s = p.ws_lse + row * p.n_slots;
-                        const float* o_s = p.ws_o + row * p.n_slots * D + d0;
-                        float M = -INFINITY;
-                        for (int s2 = 0; s2 < si.n_ne; ++s2) M = fmaxf(M, __ldcg(lse_s + s2));
-                        float acc2[per], Ltot = 0.f;
-                        #pragma unroll
-                        for (int u = 0; u < per; ++u) acc2[u] = 0.f;
-                        for (int s2 = 0; s2 < si.n_ne; ++s2) {
-                            const float w = ex2_approx(__ldcg(lse_s + s2) - M);
-                            Ltot += w;
-                            #pragma unroll
-                            for (int e = 0; e < per; e += 4) {
-                                const float4 x = __ldcg(reinterpret_cast<const float4*>(o_s + (long long)s2 * D + e));
-                                acc2[e] += w * x.x; acc2[e + 1] += w * x.y;
-                                acc2[e + 2] += w * x.z; acc2[e + 3] += w * x.w;
-                            }
-                        }
-                        const float inv = 1.f / Ltot;
-                        #pragma unroll
-                        for (int u = 0; u < per; ++u) acc2[u] *= inv;
-                        store_final<per>(p, row, d0, acc2, (t & 15) == 0, M + __log2f(Ltot));
-                    }
-                }
             }
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
     }
     __syncthreads();
+}
+
+// One thread per (b, query head, 4 output columns): O = sum_s w_s O_s / sum_s w_s with
+// w_s = 2^(lse_s - max lse) over the non-empty splits, in one pass of 8 splits at a time.
+template <int D>
+__global__ void __launch_bounds__(256)
+decode_combine_kernel(const __grid_constant__ DecodeParams p) {
+    constexpr int kGroups = D / 4;
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long row = idx / kGroups;
+    const int cg = (int)(idx % kGroups);
+    // the partials come from the split kernel launched just before this one
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (row >= (long long)p.B * p.Hq) return;
+    const int b = (int)(row / p.Hq);
+    int len = __ldg(&p.kv_lens[b]);
+    len = max(0, min(len, p.Lmax));
+    const int n_ne = nonempty_splits(len, splits_for(len, p.fixed_splits));
+    if (n_ne <= 1) return;      // written directly by the split kernel
+    const float* lse_s = p.ws_lse + row * p.n_slots;
+    const float* o_s = p.ws_o + row * p.n_slots * D + cg * 4;
+    constexpr int kChunk = 8;
+    float M = -INFINITY, Ltot = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < n_ne; s0 += kChunk) {
+        float ls[kChunk];
+        float4 ox[kChunk];
+        #pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const bool in = s0 + i < n_ne;
+            ls[i] = in ? __ldcg(lse_s + s0 + i) : -INFINITY;
+            ox[i] = in ? __ldcg(reinterpret_cast<const float4*>(o_s + (long long)(s0 + i) * D))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float Mc = M;
+        #pragma unroll
+        for (int i = 0; i < kChunk; ++i) Mc = fmaxf(Mc, ls[i]);
+        const float sc = (M == -INFINITY) ? 0.f : ex2_approx(M - Mc);
+        Ltot *= sc;
+        acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+        #pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const float w = (ls[i] == -INFINITY) ? 0.f : ex2_approx(ls[i] - Mc);
+            Ltot += w;
+            acc.x += w * ox[i].x; acc.y += w * ox[i].y; acc.z += w * ox[i].z; acc.w += w * ox[i].w;
+        }
+        M = Mc;
+    }
+    const float inv = 1.f / Ltot;
+    uint2 packed;
+    packed.x = pack_bf16(acc.x * inv, acc.y * inv);
+    packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(p.o + row * D + cg * 4) = packed;
+    if (cg == 0 && p.lse != nullptr) p.lse[row] = (M + __log2f(Ltot)) * 0.69314718055994531f;
 }
 
 }  // namespace
@@ -503,40 +524,51 @@ int decode_slots(int Lmax, int num_splits) {
     return n < 1 ? 1 : (n > kMaxSplits ? kMaxSplits : n);
 }
 
-size_t decode_counter_bytes(int B, int Hkv, int n_hc) {
-    return (((size_t)1 + (size_t)B * Hkv * n_hc) * 4 + 255) / 256 * 256;
-}
+size_t decode_counter_bytes() { return 256; }
 
-size_t decode_workspace_bytes(int B, int Hq, int Hkv, int d, int n_slots) {
-    const int n_hc = (Hq / Hkv + 7) / 8;
+size_t decode_workspace_bytes(int B, int Hq, int d, int n_slots) {
     const size_t rows = (size_t)B * Hq * n_slots;
-    size_t bytes = decode_counter_bytes(B, Hkv, n_hc);   // work queue + group counters
+    size_t bytes = decode_counter_bytes();               // work queue counter
     bytes += ((rows * 4 + 255) / 256) * 256;             // lse partials
     bytes += rows * (size_t)d * 4;                       // O partials
     return bytes;
 }
 
+namespace {
+
+template <int D>
+cudaError_t launch_pair(const DecodeParams& p, int grid, cudaStream_t stream) {
+    constexpr int smem = Layout<D>::kAlloc;
+    cudaError_t err = cudaFuncSetAttribute(decode_split_kernel<D>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    decode_split_kernel<D><<<grid, kThreads, smem, stream>>>(p);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    // combine: programmatic dependent launch on the same stream
+    const long long threads = (long long)p.B * p.Hq * (D / 4);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((threads + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, p);
+}
+
+}  // namespace
+
 cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
                                   cudaStream_t stream) {
-    cudaError_t err = cudaMemsetAsync(p.counter, 0, decode_counter_bytes(p.B, p.Hkv, p.n_hc),
-                                      stream);
+    cudaError_t err = cudaMemsetAsync(p.counter, 0, decode_counter_bytes(), stream);
     if (err != cudaSuccess) return err;
     const int grid = p.n_items < num_sms ? p.n_items : num_sms;
     if (grid <= 0) return cudaSuccess;
-    if (d == 128) {
-        constexpr int smem = Layout<128>::kAlloc;
-        err = cudaFuncSetAttribute(decode_split_kernel<128>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (err != cudaSuccess) return err;
-        decode_split_kernel<128><<<grid, kThreads, smem, stream>>>(p);
-    } else {
-        constexpr int smem = Layout<64>::kAlloc;
-        err = cudaFuncSetAttribute(decode_split_kernel<64>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (err != cudaSuccess) return err;
-        decode_split_kernel<64><<<grid, kThreads, smem, stream>>>(p);
-    }
-    return cudaGetLastError();
+    return d == 128 ? launch_pair<128>(p, grid, stream) : launch_pair<64>(p, grid, stream);
 }
 
 }  // namespace gbattn

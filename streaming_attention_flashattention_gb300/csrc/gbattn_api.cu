@@ -158,7 +158,7 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int n
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lmax <= 0 || (d != 64 && d != 128)) return 0;
     if (num_splits < 0 || num_splits > kMaxSplits) return 0;
     if (Hq % Hkv != 0) return 0;
-    return decode_workspace_bytes(B, Hq, Hkv, d, decode_slots(Lmax, num_splits));
+    return decode_workspace_bytes(B, Hq, d, decode_slots(Lmax, num_splits));
 }
 
 int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
@@ -175,7 +175,7 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
         (lse && !aligned16(lse)) || (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
         return GBATTN_ERR_MISALIGNED;
     const int n_slots = decode_slots(Lmax, num_splits);
-    const size_t need = decode_workspace_bytes(B, Hq, Hkv, d, n_slots);
+    const size_t need = decode_workspace_bytes(B, Hq, d, n_slots);
     if (!workspace || ws_bytes < need) return GBATTN_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GBATTN_ERR_MISALIGNED;
     const int G = Hq / Hkv;
@@ -194,9 +194,8 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
         return GBATTN_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const size_t rows = (size_t)B * Hq * n_slots;
-    const size_t cnt_bytes = decode_counter_bytes(B, Hkv, n_hc);
+    const size_t cnt_bytes = decode_counter_bytes();
     p.counter = reinterpret_cast<int*>(ws);
-    p.group_cnt = p.counter + 1;
     p.ws_lse = reinterpret_cast<float*>(ws + cnt_bytes);
     p.ws_o = reinterpret_cast<float*>(ws + cnt_bytes + ((rows * 4 + 255) / 256) * 256);
     p.kv_lens = kv_lens;

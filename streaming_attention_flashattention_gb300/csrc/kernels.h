@@ -43,7 +43,6 @@ struct DecodeParams {
     __nv_bfloat16* o;     // [B, Hq, d]
     float* lse;           // [B, Hq] or null
     int* counter;         // work queue counter (zeroed before the split kernel)
-    int* group_cnt;       // finished splits per (b, kv head, head chunk), zeroed likewise
     float* ws_lse;        // [B, Hq, n_slots] log2-domain partial lse
     float* ws_o;          // [B, Hq, n_slots, d] normalised partial outputs
     int B, Hq, Hkv, Lmax, G;
@@ -59,8 +58,8 @@ constexpr int kAutoChunk = 4096;
 constexpr int kMaxSplits = 256;
 constexpr int kSplitAlign = 64;
 
-size_t decode_counter_bytes(int B, int Hkv, int n_hc);
-size_t decode_workspace_bytes(int B, int Hq, int Hkv, int d, int n_slots);
+size_t decode_counter_bytes();
+size_t decode_workspace_bytes(int B, int Hq, int d, int n_slots);
 int decode_slots(int Lmax, int num_splits);
 cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
                                   cudaStream_t stream);
