@@ -186,6 +186,16 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank timings (the slowest rank sets the step time).  A
+    no-op when torch.distributed is not initialised (one process)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 def config_dict(args):
     return {"workload": f"{PREFILL.name} + {DECODE.name}",
             "prefill": {"B": PREFILL.B, "Hq": PREFILL.Hq, "Hkv": PREFILL.Hkv, "Sq": PREFILL.Sq,
@@ -278,10 +288,7 @@ def run_gpu(args, rank, world, local_rank):
     pre_avg = sum(pre_ms) / len(pre_ms)
     dec_avg = sum(dec_ms) / len(dec_ms)
     step_ms = pre_avg + dec_avg
-    times = torch.tensor([pre_avg, dec_avg, step_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
-    pre_avg, dec_avg, step_ms = (float(x) for x in times.cpu())
+    pre_avg, dec_avg, step_ms = max_over_ranks([pre_avg, dec_avg, step_ms], dev)
 
     st, word = gb.attn_last_device_error()
     if st != 0:

@@ -147,9 +147,21 @@ int attn_decode_splitkv_noalloc(const void* q, const void* kcache, const void* v
  * attn_last_device_error -- synchronise `stream`, then read and clear the device error
  * word that bounded waits inside the kernels set when they give up (they never trap).
  * Returns GBATTN_OK, GBATTN_ERR_TIMEOUT (the word was set) or GBATTN_ERR_CUDA.
- * If detail != NULL it receives the raw word (which wait gave up).
+ * If detail != NULL it receives the raw word (which wait gave up): 1 producer (free ring
+ * slot), 2 consumer (filled slot), 3 MMA issuer, 4 softmax warps, 5 exit drain of
+ * in-flight copies, 6 the self-test wait.
  */
 int attn_last_device_error(void* stream, int* detail);
+
+/*
+ * attn_selftest_bounded_wait -- exercise the failure path of the device-side waits without
+ * hanging or faulting the GPU: launches a one-thread kernel on `stream` whose mbarrier
+ * wait can never be satisfied; after about 2e6 cycles (~1 ms) the wait gives up, records
+ * word 6 in the device error word and the kernel returns normally.  A following
+ * attn_last_device_error() then reports GBATTN_ERR_TIMEOUT with detail 6 (and clears
+ * the word); the context stays usable.  Returns GBATTN_OK if the kernel was launched.
+ */
+int attn_selftest_bounded_wait(void* stream);
 
 /* Human-readable text for a status code (static storage, never NULL). */
 const char* attn_status_string(int status);

@@ -43,6 +43,7 @@ EXPORTS = {
     "attn_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "attn_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_last_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_int)]),
+    "attn_selftest_bounded_wait": (_I, [_P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_version": (_I, []),
 }
@@ -206,6 +207,13 @@ def attn_decode_splitkv_noalloc(q: torch.Tensor, kcache: torch.Tensor, vcache: t
                                          _stream_ptr(stream))
     _check("attn_decode_splitkv_noalloc", st)
     return out, lse
+
+
+def attn_selftest_bounded_wait(stream=None) -> None:
+    """Launch the never-satisfied bounded wait (see include/gbattn.h); read the outcome with
+    attn_last_device_error()."""
+    _check("attn_selftest_bounded_wait",
+           load_library().attn_selftest_bounded_wait(_stream_ptr(stream)))
 
 
 def attn_last_device_error(stream=None) -> tuple[int, int]:

@@ -24,6 +24,7 @@ enum : int {
     kErrWaitMma = 3,         // MMA issuer gave up waiting for operands / P
     kErrWaitSoftmax = 4,     // softmax warps gave up waiting for S or O
     kErrWaitDrain = 5,       // drain of in-flight copies at exit gave up
+    kErrSelfTest = 6,        // the self-test wait that is never satisfied gave up (expected)
 };
 
 // A wait gives up after this many clock cycles (~1 s at 2 GHz).  Correct code never gets
@@ -81,7 +82,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // recording `err`) if the wait runs past kWaitLimitCycles or another part of the grid
 // already recorded an error.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int err,
-                                          int* err_word) {
+                                          int* err_word,
+                                          long long limit_cycles = kWaitLimitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     uint32_t spins = 0;
@@ -89,7 +91,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int er
         if (mbar_try_wait(bar, parity)) return true;
         if ((++spins & 1023u) == 0) {
             if (device_error_set(err_word)) return false;
-            if (clock64() - t0 > kWaitLimitCycles) {
+            if (clock64() - t0 > limit_cycles) {
                 record_error(err_word, err);
                 return false;
             }

@@ -78,6 +78,15 @@ int sm_count() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// One thread waits on an mbarrier that nothing ever arrives on; the bounded wait gives up
+// after `limit` cycles, records kErrSelfTest and the kernel returns normally.
+__global__ void selftest_wait_kernel(int* err_word, long long limit) {
+    __shared__ uint64_t bar;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    mbar_wait(&bar, 0, kErrSelfTest, err_word, limit);
+}
+
 constexpr long long kIntMax = 2147483647LL;
 
 }  // namespace
@@ -211,6 +220,13 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
     if (!p.err) return GBATTN_ERR_CUDA;
     cudaError_t e = launch_decode_splitkv(p, d, nsm, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+int attn_selftest_bounded_wait(void* stream) {
+    int* err = device_error_word();
+    if (!err) return GBATTN_ERR_CUDA;
+    selftest_wait_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(err, 2000000LL);
+    return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 
 int attn_last_device_error(void* stream, int* detail) {

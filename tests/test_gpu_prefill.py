@@ -144,3 +144,16 @@ def test_gpu_rejects_bad_arguments_without_launch():
     q = torch.zeros(1, 2, 64, 96, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(gb.GbAttnError):
         gb.attn_fwd(q, q[:, :1], q[:, :1], causal=False)
+
+
+def test_bounded_wait_expiry_is_reported_and_context_survives():
+    """A device wait that can never be satisfied gives up, reports GBATTN_ERR_TIMEOUT with
+    the self-test code through the error word, and later work still runs correctly."""
+    st, word = gb.attn_last_device_error()
+    assert st == 0, f"error word already set: {word}"
+    gb.attn_selftest_bounded_wait()
+    st, word = gb.attn_last_device_error()
+    assert st == gb.GBATTN_ERR_TIMEOUT and word == 6
+    st, word = gb.attn_last_device_error()          # read-and-clear
+    assert st == 0 and word == 0
+    check(small(1, 4, 2, 200, 200, 128, True, seed=13))
