@@ -12,8 +12,9 @@
 //   section 2.1 -- each range is one contiguous block of the cache.
 //
 // GB300 mapping.
-//   split kernel: persistent CTAs (one per SM) pull work items (sequence b, KV head,
-//   head chunk, split s) from a device counter.  One producer warp streams the split's
+//   split kernel: persistent CTAs (one per SM) take work items (sequence b, KV head,
+//   head chunk, split s): round-robin for a fixed split count, from a device counter for
+//   automatic (length-dependent) splits.  One producer warp streams the split's
 //   K and V through a 5-stage shared-memory ring with 3-D TMA copies (64 keys x d,
 //   128-byte swizzle) and mbarrier handoff.  Four consumer warps take 16 keys each per
 //   stage and run S^T = K Q^T and O^T += V^T P^T on mma.sync m16n8k16 with the G <= 8
@@ -189,9 +190,14 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;   // per-stage bits for the exit drain
             bool ok = true;
-            while (ok) {
-                const int item = atomicAdd(p.counter, 1);
-                if (item >= p.n_items) break;
+            // Work distribution: with a fixed split count every item is the same size and a
+            // static round-robin is already balanced (no counter, no reset before the
+            // launch); with automatic splits the sizes follow the ragged lengths and items
+            // are pulled from a device counter instead.
+            const bool dynamic = p.fixed_splits == 0;
+            int item = dynamic ? atomicAdd(p.counter, 1) : (int)blockIdx.x;
+            for (; ok && item < p.n_items;
+                 item = dynamic ? atomicAdd(p.counter, 1) : item + (int)gridDim.x) {
                 // group-major order (split innermost): a group's splits run side by side on
                 // different CTAs
                 int rem = item;
@@ -564,8 +570,10 @@ cudaError_t launch_pair(const DecodeParams& p, int grid, cudaStream_t stream) {
 
 cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
                                   cudaStream_t stream) {
-    cudaError_t err = cudaMemsetAsync(p.counter, 0, decode_counter_bytes(), stream);
-    if (err != cudaSuccess) return err;
+    if (p.fixed_splits == 0) {   // the work counter of the automatic mode starts at zero
+        cudaError_t err = cudaMemsetAsync(p.counter, 0, decode_counter_bytes(), stream);
+        if (err != cudaSuccess) return err;
+    }
     const int grid = p.n_items < num_sms ? p.n_items : num_sms;
     if (grid <= 0) return cudaSuccess;
     return d == 128 ? launch_pair<128>(p, grid, stream) : launch_pair<64>(p, grid, stream);
