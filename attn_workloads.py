@@ -67,6 +67,15 @@ WORKLOADS = {
 }
 
 
+# Beyond the five reference workloads: chunked prefill of a Llama3-70B-shaped context
+# (a 2048-token chunk at the end of a 16384-token context held in a 32768-row cache).
+EXTRA_WORKLOADS = {
+    6: Workload("llama3-70b-chunked-prefill-q2048-ctx16384", "chunk", B=1, Hq=64, Hkv=8, d=128,
+                dtype="bf16", Sq=2048, Skv=32768, causal=True, len_lo=16384, len_hi=16384,
+                seed=1006),
+}
+
+
 def _gen(seed: int) -> torch.Generator:
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
@@ -121,6 +130,20 @@ def decode_inputs(w: Workload, pad_value: float = float("nan")):
             kc[b, :, n:] = pad_value
             vc[b, :, n:] = pad_value
     return q, kc, vc, lens
+
+
+def chunk_inputs(w: Workload, pad_value: float = float("nan")):
+    """Chunked prefill: Q [B,Hq,Sq,d] and caches [B,Hkv,Lmax,d] (Lmax = w.Skv) whose first
+    w.len_hi rows are drawn; the rest hold `pad_value` (NaN: any read of them shows)."""
+    ctx = w.len_hi
+    g = _gen(w.seed)
+    q = _cast(torch.randn((w.B, w.Hq, w.Sq, w.d), generator=g, dtype=torch.float32), w.dtype)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    kc = torch.full((w.B, w.Hkv, w.Skv, w.d), pad_value, dtype=tdt)
+    vc = torch.full((w.B, w.Hkv, w.Skv, w.d), pad_value, dtype=tdt)
+    kc[:, :, :ctx] = _cast(torch.randn((w.B, w.Hkv, ctx, w.d), generator=g), w.dtype)
+    vc[:, :, :ctx] = _cast(torch.randn((w.B, w.Hkv, ctx, w.d), generator=g), w.dtype)
+    return q, kc, vc, ctx
 
 
 def to_oracle(x: torch.Tensor) -> np.ndarray:

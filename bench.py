@@ -53,6 +53,16 @@ def prefill_flops(w: wl.Workload) -> float:
     return f / 2 if w.causal else f
 
 
+def chunk_flops(w: wl.Workload) -> float:
+    """4 d B Hq x (visible keys summed over the chunk's rows); chunk at the context's end."""
+    ctx = w.len_hi
+    if w.causal:
+        vis = w.Sq * (ctx - w.Sq) + w.Sq * (w.Sq + 1) / 2
+    else:
+        vis = w.Sq * ctx
+    return 4.0 * w.d * w.B * w.Hq * vis
+
+
 def decode_bytes(w: wl.Workload, lens) -> float:
     kv = float(sum(int(x) for x in lens)) * w.Hkv * w.d * 2 * 2
     q_o = 2.0 * w.B * w.Hq * w.d * 2
@@ -290,6 +300,29 @@ def run_gpu(args, rank, world, local_rank):
     step_ms = pre_avg + dec_avg
     pre_avg, dec_avg, step_ms = max_over_ranks([pre_avg, dec_avg, step_ms], dev)
 
+    # chunked prefill against a KV cache (a widening beyond the step's two calls)
+    chunk = None
+    if not args.no_chunk:
+        wc = wl.EXTRA_WORKLOADS[6]
+        cq, ckc, cvc, cctx = (x.to(dev) if torch.is_tensor(x) else x for x in wl.chunk_inputs(wc))
+        co = torch.empty_like(cq)
+        clse = torch.empty(cq.shape[:3], dtype=torch.float32, device=dev)
+        for _ in range(3):
+            gb.attn_prefill_kvcache(cq, ckc, cvc, cctx, causal=wc.causal, scale=wc.scale, out=co, lse=clse)
+        cms = []
+        for _ in range(10):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gb.attn_prefill_kvcache(cq, ckc, cvc, cctx, causal=wc.causal, scale=wc.scale, out=co, lse=clse)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            cms.append(e0.elapsed_time(e1))
+        cm = max_over_ranks([sum(cms) / len(cms)], dev)[0]
+        chunk = {"workload": wc.name, "ms": cm, "value": chunk_flops(wc) / (cm * 1e-3) / 1e12,
+                 "unit": "TFLOP/s"}
+        del cq, ckc, cvc, co, clse
+
     st, word = gb.attn_last_device_error()
     if st != 0:
         raise RuntimeError(f"device error word {word} during the timed steps")
@@ -347,6 +380,8 @@ def run_gpu(args, rank, world, local_rank):
     peak_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     per_gpu_tf = flops / (pre_avg * 1e-3) / 1e12
     per_gpu_bw = dbytes / (dec_avg * 1e-3) / 1e9
+    if chunk is not None:
+        chunk["frac"] = chunk["value"] / peak_tf      # per GPU
     line = {
         "metric": "prefill attn TFLOP/s & decode KV GB/s at 1 GB300, % of roofline",
         "value": pre_tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -369,6 +404,7 @@ def run_gpu(args, rank, world, local_rank):
                 "decode_gbs": (dbytes / (e2e_dec * 1e-3) / 1e9 * world) if not args.no_e2e else None,
                 "ms_per_step": e2e_pre + e2e_dec},
         "gpu_launches": 3 * args.steps,
+        "chunked_prefill": chunk,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
@@ -384,6 +420,7 @@ def main():
     ap.add_argument("--impl", choices=["gbattn", "reference"], default="gbattn")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-chunk", action="store_true", help="skip the chunked-prefill measurement")
     ap.add_argument("--prefill", type=int, default=3, help="prefill workload index (1-3)")
     ap.add_argument("--decode", type=int, default=4, help="decode workload index (4-5)")
     args = ap.parse_args()

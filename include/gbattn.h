@@ -82,6 +82,27 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              void* stream);
 
 /*
+ * attn_prefill_kvcache -- chunked prefill against a KV cache: a chunk of Sq new queries
+ * attends to the first Skv rows of a cache of capacity Lmax (the chunk's own keys are the
+ * last Sq of those rows; "ADR-0060" section 0.5.2: T_q = the chunk width for a
+ * prefill/chunk launch, and section 5.4 for the tile classes).
+ *
+ *   q       [B, Hq, Sq, d]      device, bf16    the chunk's post-RoPE queries
+ *   kcache  [B, Hkv, Lmax, d]   device, bf16    key cache; rows [0, Skv) are used, rows
+ *                                               [Skv, Lmax) are never read
+ *   vcache  [B, Hkv, Lmax, d]   device, bf16    value cache, same rows
+ *   o       [B, Hq, Sq, d]      device, bf16    output (written)
+ *   lse     [B, Hq, Sq]         device, fp32    log-sum-exp (written); may be NULL
+ *
+ * Same kernel and numerics as attn_fwd (bf16); causal is bottom-right: query i of the chunk
+ * sits at position Skv - Sq + i.  Requirements: 1 <= Skv <= Lmax, Hq % Hkv == 0,
+ * d in {64, 128}, causal requires Sq <= Skv, pointers 16-byte aligned.
+ */
+int attn_prefill_kvcache(const void* q, const void* kcache, const void* vcache, void* o,
+                         float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int Lmax, int d,
+                         float scale, int causal, void* stream);
+
+/*
  * attn_decode_workspace_size -- bytes of device workspace attn_decode_splitkv needs.
  * Holds the per-split partial results (lse_s and O_s / l_s, fp32) and a work counter.
  * num_splits > 0: fixed split count; 0: automatic (one split per 4096 keys).

@@ -39,6 +39,7 @@ _F = ctypes.c_float
 _SZ = ctypes.c_size_t
 EXPORTS = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "attn_prefill_kvcache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "attn_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "attn_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
@@ -136,6 +137,30 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool,
                       B, Hq, Hkv, Sq, Skv, d, float(scale), 1 if causal else 0, dtype,
                       _stream_ptr(stream))
     _check("attn_fwd", st)
+    return out, lse
+
+
+def attn_prefill_kvcache(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
+                         kv_len: int, causal: bool = True, scale: float | None = None,
+                         out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                         stream=None):
+    """Chunked prefill: q [B,Hq,Sq,d] against the first kv_len rows of caches [B,Hkv,Lmax,d]
+    (bf16).  Returns (out [B,Hq,Sq,d] bf16, lse [B,Hq,Sq] fp32)."""
+    lib = load_library()
+    for n, t in (("q", q), ("kcache", kcache), ("vcache", vcache)):
+        _dev_tensor(n, t, (torch.bfloat16,))
+    B, Hq, Sq, d = q.shape
+    _, Hkv, Lmax, _ = kcache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    st = lib.attn_prefill_kvcache(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
+                                  out.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Sq, int(kv_len),
+                                  Lmax, d, float(scale), 1 if causal else 0, _stream_ptr(stream))
+    _check("attn_prefill_kvcache", st)
     return out, lse
 
 

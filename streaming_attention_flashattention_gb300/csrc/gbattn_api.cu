@@ -51,12 +51,15 @@ EncodeTiledFn encode_fn() {
 }
 
 // 3-D bf16 tensor map with a 128-byte swizzle: dims innermost first, box (64, rows, 1).
+// d1_stride: rows between consecutive d2 planes (>= d1; larger for a cache whose
+// capacity exceeds the valid length d1 -- the rows past d1 are then out of bounds).
 bool make_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
-                      uint64_t d2, uint32_t box_rows) {
+                      uint64_t d2, uint32_t box_rows, uint64_t d1_stride = 0) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    if (d1_stride == 0) d1_stride = d1;
     const cuuint64_t dims[3] = {d0, d1, d2};
-    const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    const cuuint64_t strides[2] = {d0 * 2, d0 * d1_stride * 2};
     const cuuint32_t box[3] = {64, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
@@ -88,6 +91,32 @@ __global__ void selftest_wait_kernel(int* err_word, long long limit) {
 }
 
 constexpr long long kIntMax = 2147483647LL;
+
+// bf16 tcgen05 prefill; K/V rows of one head are `kv_stride` rows apart (>= Skv).
+int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int Hq, int Hkv, int Sq, int Skv, int kv_stride, int d, float scale,
+                        int causal, cudaStream_t st) {
+    PrefillParams p{};
+    if (!make_map_bf16_3d(&p.tmap_q, q, d, Sq, (uint64_t)B * Hq, 128) ||
+        !make_map_bf16_3d(&p.tmap_k, k, d, Skv, (uint64_t)B * Hkv, 128, kv_stride) ||
+        !make_map_bf16_3d(&p.tmap_v, v, d, Skv, (uint64_t)B * Hkv, 128, kv_stride))
+        return GBATTN_ERR_CUDA;
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv;
+    p.G = Hq / Hkv;
+    p.n_qblk = (Sq + 127) / 128;
+    const long long per_group = ((long long)p.n_qblk * p.G + 1) / 2;
+    const long long n_pairs = per_group * B * Hkv;
+    if (n_pairs > kIntMax) return GBATTN_ERR_TOO_LARGE;
+    p.n_pairs = (int)n_pairs;
+    p.causal = causal;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = device_error_word();
+    if (!p.err) return GBATTN_ERR_CUDA;
+    cudaError_t e = launch_attn_fwd_bf16(p, d, st);
+    return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
 
 }  // namespace
 }  // namespace gbattn
@@ -141,26 +170,27 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
         return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
     }
 
-    PrefillParams p{};
-    if (!make_map_bf16_3d(&p.tmap_q, q, d, Sq, (uint64_t)B * Hq, 128) ||
-        !make_map_bf16_3d(&p.tmap_k, k, d, Skv, (uint64_t)B * Hkv, 128) ||
-        !make_map_bf16_3d(&p.tmap_v, v, d, Skv, (uint64_t)B * Hkv, 128))
-        return GBATTN_ERR_CUDA;
-    p.o = static_cast<__nv_bfloat16*>(o);
-    p.lse = lse;
-    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv;
-    p.G = Hq / Hkv;
-    p.n_qblk = (Sq + 127) / 128;
-    const long long per_group = ((long long)p.n_qblk * p.G + 1) / 2;
-    const long long n_pairs = per_group * B * Hkv;
-    if (n_pairs > kIntMax) return GBATTN_ERR_TOO_LARGE;
-    p.n_pairs = (int)n_pairs;
-    p.causal = causal;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.err = device_error_word();
-    if (!p.err) return GBATTN_ERR_CUDA;
-    cudaError_t e = launch_attn_fwd_bf16(p, d, st);
-    return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+    return launch_prefill_bf16(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, Skv, d, scale, causal, st);
+}
+
+int attn_prefill_kvcache(const void* q, const void* kcache, const void* vcache, void* o,
+                         float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int Lmax, int d,
+                         float scale, int causal, void* stream) {
+    if (!q || !kcache || !vcache || !o) return GBATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || Lmax <= 0 || d <= 0)
+        return GBATTN_ERR_INVALID_ARG;
+    if (Skv > Lmax || Hq % Hkv != 0) return GBATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || scale != scale) return GBATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return GBATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return GBATTN_ERR_UNSUPPORTED;
+    if (causal && Sq > Skv) return GBATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
+        (lse && !aligned16(lse)))
+        return GBATTN_ERR_MISALIGNED;
+    if ((long long)B * Hq * Sq > kIntMax || (long long)B * Hkv * Lmax > kIntMax)
+        return GBATTN_ERR_TOO_LARGE;
+    return launch_prefill_bf16(q, kcache, vcache, o, lse, B, Hq, Hkv, Sq, Skv, Lmax, d, scale,
+                               causal, static_cast<cudaStream_t>(stream));
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int num_splits) {
