@@ -68,11 +68,16 @@ WORKLOADS = {
 
 
 # Beyond the five reference workloads: chunked prefill of a Llama3-70B-shaped context
-# (a 2048-token chunk at the end of a 16384-token context held in a 32768-row cache).
+# (a 2048-token chunk at the end of a 16384-token context held in a 32768-row cache), and
+# multi-token decode.
 EXTRA_WORKLOADS = {
     6: Workload("llama3-70b-chunked-prefill-q2048-ctx16384", "chunk", B=1, Hq=64, Hkv=8, d=128,
                 dtype="bf16", Sq=2048, Skv=32768, causal=True, len_lo=16384, len_hi=16384,
                 seed=1006),
+    # speculative decode: 4 new tokens per sequence against a 32768-key cache
+    7: Workload("llama3-70b-multitoken-decode-b4-tq4-l32768", "multitoken", B=4, Hq=64, Hkv=8,
+                d=128, dtype="bf16", Sq=4, Skv=32768, num_splits=16, len_lo=32768,
+                len_hi=32768, seed=1007),
 }
 
 
@@ -144,6 +149,24 @@ def chunk_inputs(w: Workload, pad_value: float = float("nan")):
     kc[:, :, :ctx] = _cast(torch.randn((w.B, w.Hkv, ctx, w.d), generator=g), w.dtype)
     vc[:, :, :ctx] = _cast(torch.randn((w.B, w.Hkv, ctx, w.d), generator=g), w.dtype)
     return q, kc, vc, ctx
+
+
+def multitoken_inputs(w: Workload, pad_value: float = float("nan")):
+    """Multi-token decode: Q [B,Hq,Tq,d] (Tq = w.Sq), caches [B,Hkv,Lmax,d], kv_lens [B]."""
+    lens = decode_lengths(w)
+    g = _gen(w.seed + 7919)
+    q = _cast(torch.randn((w.B, w.Hq, w.Sq, w.d), generator=g, dtype=torch.float32), w.dtype)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    kc = torch.empty((w.B, w.Hkv, w.Skv, w.d), dtype=tdt)
+    vc = torch.empty((w.B, w.Hkv, w.Skv, w.d), dtype=tdt)
+    for b in range(w.B):
+        n = int(lens[b])
+        kc[b, :, :n] = _cast(torch.randn((w.Hkv, n, w.d), generator=g), w.dtype)
+        vc[b, :, :n] = _cast(torch.randn((w.Hkv, n, w.d), generator=g), w.dtype)
+        if n < w.Skv:
+            kc[b, :, n:] = pad_value
+            vc[b, :, n:] = pad_value
+    return q, kc, vc, lens
 
 
 def to_oracle(x: torch.Tensor) -> np.ndarray:

@@ -323,6 +323,34 @@ def run_gpu(args, rank, world, local_rank):
                  "unit": "TFLOP/s"}
         del cq, ckc, cvc, co, clse
 
+    # multi-token decode (4 new tokens per sequence)
+    mtok = None
+    if not args.no_chunk:
+        wm = wl.EXTRA_WORKLOADS[7]
+        mq, mkc, mvc, mkl_c = wl.multitoken_inputs(wm)
+        mq, mkc, mvc, mkl = mq.to(dev), mkc.to(dev), mvc.to(dev), mkl_c.to(dev)
+        mo = torch.empty_like(mq)
+        mlse = torch.empty(mq.shape[:3], dtype=torch.float32, device=dev)
+        mws = torch.empty(gb.load_library().attn_decode_multitoken_workspace_size(
+            wm.B, wm.Hq, wm.Hkv, wm.Sq, wm.Skv, wm.d, wm.num_splits), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            gb.attn_decode_multitoken(mq, mkc, mvc, mkl, num_splits=wm.num_splits, scale=wm.scale,
+                                      out=mo, lse=mlse, workspace=mws)
+        mms = []
+        for _ in range(10):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gb.attn_decode_multitoken(mq, mkc, mvc, mkl, num_splits=wm.num_splits, scale=wm.scale,
+                                      out=mo, lse=mlse, workspace=mws)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            mms.append(e0.elapsed_time(e1))
+        mm = max_over_ranks([sum(mms) / len(mms)], dev)[0]
+        mbytes = float(mkl_c.sum()) * wm.Hkv * wm.d * 2 * 2 + 2.0 * wm.B * wm.Hq * wm.Sq * wm.d * 2
+        mtok = {"workload": wm.name, "ms": mm, "value": mbytes / (mm * 1e-3) / 1e9, "unit": "GB/s"}
+        del mq, mkc, mvc, mkl, mo, mlse, mws
+
     st, word = gb.attn_last_device_error()
     if st != 0:
         raise RuntimeError(f"device error word {word} during the timed steps")
@@ -382,6 +410,8 @@ def run_gpu(args, rank, world, local_rank):
     per_gpu_bw = dbytes / (dec_avg * 1e-3) / 1e9
     if chunk is not None:
         chunk["frac"] = chunk["value"] / peak_tf      # per GPU
+    if mtok is not None:
+        mtok["frac"] = mtok["value"] / peak_bw         # per GPU
     line = {
         "metric": "prefill attn TFLOP/s & decode KV GB/s at 1 GB300, % of roofline",
         "value": pre_tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -405,6 +435,7 @@ def run_gpu(args, rank, world, local_rank):
                 "ms_per_step": e2e_pre + e2e_dec},
         "gpu_launches": 3 * args.steps,
         "chunked_prefill": chunk,
+        "multitoken_decode": mtok,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:

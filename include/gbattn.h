@@ -131,7 +131,7 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int n
  * C = ceil(len / n) rounded up to 64 ("ADR-0060" section 2.1: contiguous blocks); each
  * split streams its chunk once for all G = Hq / Hkv query heads of a KV head (the heads
  * are stacked into one MMA operand, "ADR-0060" section 5.2), and a combine kernel merges
- * the partial (lse_s, O_s) of the splits.  kv_lens values are read on the device; values
+ * the partial (lse_s, O_s) of the splits (a sequence with one split is written directly).  kv_lens values are read on the device; values
  * outside [0, Lmax] are clamped into it.
  * Requirements: d = 128 or 64, G <= 8 per launch group (larger G runs several groups),
  * all pointers 16-byte aligned.  Returns GBATTN_OK or a negative status.
@@ -140,6 +140,32 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
                         const int* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
                         int Lmax, int d, float scale, int num_splits, void* workspace,
                         size_t ws_bytes, void* stream);
+
+/*
+ * attn_decode_multitoken -- decode of Tq >= 1 new tokens per sequence at once (for
+ * example speculative decoding), split-KV with the same log-sum-exp merge.  The G * Tq
+ * query rows of a KV head are stacked into the MMA operand ("ADR-0060" section 0.5:
+ * the group's Q [G, T_q, d] folds to [G * T_q, d]), 8 rows per pass over a K/V tile.
+ *
+ *   q       [B, Hq, Tq, d]      device, bf16    the new tokens' post-RoPE queries
+ *   kcache  [B, Hkv, Lmax, d]   device, bf16    key cache; the new tokens' keys are
+ *                                               already its rows [len - Tq, len)
+ *   vcache  [B, Hkv, Lmax, d]   device, bf16    value cache, same rows
+ *   kv_lens [B]                 device, int32   len: cached keys per sequence, new ones included
+ *   o       [B, Hq, Tq, d]      device, bf16    output (written)
+ *   lse     [B, Hq, Tq]         device, fp32    log-sum-exp (written); may be NULL
+ *   workspace, ws_bytes                         >= attn_decode_multitoken_workspace_size(...)
+ *
+ * New token t (0-based) sees keys j <= len - Tq + t (causal among the new tokens; every
+ * older key).  A row that sees no key (len < Tq) gets O = 0, LSE = -inf.  Requirements
+ * as attn_decode_splitkv, plus 1 <= Tq <= 64.  Tq = 1 is exactly attn_decode_splitkv.
+ */
+size_t attn_decode_multitoken_workspace_size(int B, int Hq, int Hkv, int Tq, int Lmax, int d,
+                                             int num_splits);
+int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache,
+                           const int* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
+                           int Tq, int Lmax, int d, float scale, int num_splits,
+                           void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * attn_decode_splitkv_noalloc -- attn_decode_splitkv for callers that cannot allocate

@@ -42,6 +42,8 @@ EXPORTS = {
     "attn_prefill_kvcache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "attn_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "attn_decode_multitoken_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "attn_decode_multitoken": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "attn_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_last_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_int)]),
     "attn_selftest_bounded_wait": (_I, [_P]),
@@ -203,6 +205,38 @@ def attn_decode_splitkv(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Ten
                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                  _stream_ptr(stream))
     _check("attn_decode_splitkv", st)
+    return out, lse
+
+
+def attn_decode_multitoken(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
+                           kv_lens: torch.Tensor, num_splits: int = 0, scale: float | None = None,
+                           out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                           workspace: torch.Tensor | None = None, stream=None):
+    """Decode of Tq new tokens per sequence: q [B,Hq,Tq,d], caches [B,Hkv,Lmax,d] bf16,
+    kv_lens int32 [B] (new tokens included).  Returns (out [B,Hq,Tq,d], lse [B,Hq,Tq])."""
+    lib = load_library()
+    for n, t in (("q", q), ("kcache", kcache), ("vcache", vcache)):
+        _dev_tensor(n, t, (torch.bfloat16,))
+    _dev_tensor("kv_lens", kv_lens, (torch.int32,))
+    B, Hq, Tq, d = q.shape
+    _, Hkv, Lmax, _ = kcache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
+    need = int(lib.attn_decode_multitoken_workspace_size(B, Hq, Hkv, Tq, Lmax, d, num_splits))
+    if need == 0:
+        _check("attn_decode_multitoken_workspace_size", -1)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = lib.attn_decode_multitoken(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
+                                    kv_lens.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                    B, Hq, Hkv, Tq, Lmax, d, float(scale), int(num_splits),
+                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                    _stream_ptr(stream))
+    _check("attn_decode_multitoken", st)
     return out, lse
 
 

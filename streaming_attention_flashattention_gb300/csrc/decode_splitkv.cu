@@ -48,7 +48,10 @@ constexpr int kHeads = 8;                  // query heads per work item (MMA N)
 struct StageInfo {
     int b, kvh, hc, s;
     int tile, ntok, last, done;
-    int n_ne, pad0, pad1, pad2;   // non-empty splits of the sequence
+    int n_ne;                     // non-empty splits of the sequence
+    int key0;                     // first key of this tile
+    int len;                      // keys of the sequence
+    int pad;
 };
 
 template <int D>
@@ -210,16 +213,18 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 const int nb = splits_for(len, p.fixed_splits);
                 if (s >= nb) continue;
                 const int n_ne = nonempty_splits(len, nb);
-                const int h0 = kvh * p.G + hc * kHeads;
-                const int gcnt = min(kHeads, p.G - hc * kHeads);
+                // rows of this item: the KV head's G * Tq query rows (head-major, token
+                // minor), 8 per head chunk
+                const long long row0 = ((long long)b * p.Hkv + kvh) * p.R + hc * kHeads;
+                const int gcnt = min(kHeads, p.R - hc * kHeads);
                 if (s >= n_ne) {
                     // empty split: no partial.  A sequence with no keys at all gets
                     // O = 0, LSE = -inf from its split 0.
                     if (s == 0) {
                         for (int g = 0; g < gcnt; ++g) {
-                            uint4* dst = reinterpret_cast<uint4*>(p.o + ((long long)b * p.Hq + h0 + g) * D);
+                            uint4* dst = reinterpret_cast<uint4*>(p.o + (row0 + g) * D);
                             for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
-                            if (p.lse != nullptr) p.lse[(long long)b * p.Hq + h0 + g] = -INFINITY;
+                            if (p.lse != nullptr) p.lse[row0 + g] = -INFINITY;
                         }
                     }
                     continue;
@@ -241,6 +246,8 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                     si.last = (tile == ntiles - 1);
                     si.done = 0;
                     si.n_ne = n_ne;
+                    si.key0 = y;
+                    si.len = len;
                     uint8_t* st = smem + stage * L::kStageBytes;
                     const uint32_t bytes = L::kKBytes + L::kVBytes + (tile == 0 ? L::kQBytes : 0);
                     mbar_arrive_expect_tx(&full[stage], bytes);
@@ -252,7 +259,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                                     bx * 64, y, zkv, &full[stage]);
                     }
                     if (tile == 0) {
-                        const int yq = b * p.Hq + h0;
+                        const int yq = (int)row0;
                         #pragma unroll
                         for (int bx = 0; bx < L::kBoxes; ++bx)
                             tma_load_3d(st + L::kKBytes + L::kVBytes + bx * (kHeads * 128),
@@ -288,6 +295,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
         uint4 qf[D / 32];
         float acc[D / 16][4];
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        int lim0 = 0, lim1 = 0;
         int stage = 0;
         uint32_t phase = 0, sync_phase = 0;
         const int R0 = warp * 16;   // this warp's 16 keys within a stage
@@ -298,7 +306,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
             const uint32_t kbox = ring + stage * L::kStageBytes;
             const uint32_t vbox = kbox + L::kKBytes;
             const uint32_t qbox = vbox + L::kVBytes;
-            const int gcnt = min(kHeads, p.G - si.hc * kHeads);
+            const int gcnt = min(kHeads, p.R - si.hc * kHeads);
             if (si.tile == 0) {
                 #pragma unroll
                 for (int s = 0; s < D / 32; ++s) {
@@ -308,6 +316,10 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 }
                 m0 = m1 = -INFINITY;
                 l0 = l1 = 0.f;
+                // causal limit of my two columns (rows hc*8 + 2c, +1): token t of the
+                // Tq new ones sees keys < len - Tq + t + 1 (all keys when Tq = 1)
+                lim0 = si.len - p.Tq + ((si.hc * kHeads + 2 * c) % p.Tq) + 1;
+                lim1 = si.len - p.Tq + ((si.hc * kHeads + 2 * c + 1) % p.Tq) + 1;
                 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt)
                     acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
@@ -327,10 +339,11 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 }
                 // ---- online softmax over the keys (columns = heads 2c, 2c+1) ----
                 const bool v_lo = g < nvalid, v_hi = g + 8 < nvalid;
-                sc[0] = v_lo ? sc[0] * scale_log2 : -INFINITY;
-                sc[1] = v_lo ? sc[1] * scale_log2 : -INFINITY;
-                sc[2] = v_hi ? sc[2] * scale_log2 : -INFINITY;
-                sc[3] = v_hi ? sc[3] * scale_log2 : -INFINITY;
+                const int key_lo = si.key0 + R0 + g, key_hi = key_lo + 8;
+                sc[0] = (v_lo && key_lo < lim0) ? sc[0] * scale_log2 : -INFINITY;
+                sc[1] = (v_lo && key_lo < lim1) ? sc[1] * scale_log2 : -INFINITY;
+                sc[2] = (v_hi && key_hi < lim0) ? sc[2] * scale_log2 : -INFINITY;
+                sc[3] = (v_hi && key_hi < lim1) ? sc[3] * scale_log2 : -INFINITY;
                 float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
                 #pragma unroll
                 for (int w = 4; w < 32; w <<= 1) {
@@ -423,8 +436,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 const int head = t >> 4;
                 constexpr int per = D / 16;
                 const int d0 = (t & 15) * per;
-                const int hq = si.kvh * p.G + si.hc * kHeads + head;
-                const long long row = (long long)si.b * p.Hq + hq;
+                const long long row = ((long long)si.b * p.Hkv + si.kvh) * p.R + si.hc * kHeads + head;
                 if (head < gcnt) {
                     float M = -INFINITY;
                     #pragma unroll
@@ -436,7 +448,10 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                         wt[w] = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
                         Ltot += wt[w] * red_l[w * kHeads + head];
                     }
-                    const float inv = 1.f / Ltot;
+                    // a row that saw no key in this split (a masked new token) contributes
+                    // nothing: O = 0, lse = -inf
+                    const float inv = Ltot > 0.f ? 1.f / Ltot : 0.f;
+                    const float lse2 = Ltot > 0.f ? M + __log2f(Ltot) : -INFINITY;
                     float ov[per];
                     #pragma unroll
                     for (int u = 0; u < per; ++u) {
@@ -447,14 +462,14 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                         ov[u] = sum * inv;
                     }
                     if (si.n_ne == 1) {
-                        store_final<per>(p, row, d0, ov, (t & 15) == 0, M + __log2f(Ltot));
+                        store_final<per>(p, row, d0, ov, (t & 15) == 0, lse2);
                     } else {
                         const long long slot = row * p.n_slots + si.s;
                         float* dst = p.ws_o + slot * D + d0;
                         #pragma unroll
                         for (int e = 0; e < per; e += 4)
                             *reinterpret_cast<float4*>(dst + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
-                        if ((t & 15) == 0) p.ws_lse[slot] = M + __log2f(Ltot);
+                        if ((t & 15) == 0) p.ws_lse[slot] = lse2;
                     }
                 }
                 __syncwarp();
@@ -479,8 +494,8 @@ decode_combine_kernel(const __grid_constant__ DecodeParams p) {
     const int cg = (int)(idx % kGroups);
     // the partials come from the split kernel launched just before this one
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (row >= (long long)p.B * p.Hq) return;
-    const int b = (int)(row / p.Hq);
+    if (row >= (long long)p.B * p.Hq * p.Tq) return;
+    const int b = (int)(row / ((long long)p.Hq * p.Tq));
     int len = __ldg(&p.kv_lens[b]);
     len = max(0, min(len, p.Lmax));
     const int n_ne = nonempty_splits(len, splits_for(len, p.fixed_splits));
@@ -508,18 +523,20 @@ decode_combine_kernel(const __grid_constant__ DecodeParams p) {
         acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
         #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
-            const float w = (ls[i] == -INFINITY) ? 0.f : ex2_approx(ls[i] - Mc);
+            if (ls[i] == -INFINITY) continue;     // a split this row saw no key of
+            const float w = ex2_approx(ls[i] - Mc);
             Ltot += w;
             acc.x += w * ox[i].x; acc.y += w * ox[i].y; acc.z += w * ox[i].z; acc.w += w * ox[i].w;
         }
         M = Mc;
     }
-    const float inv = 1.f / Ltot;
+    const float inv = Ltot > 0.f ? 1.f / Ltot : 0.f;
     uint2 packed;
     packed.x = pack_bf16(acc.x * inv, acc.y * inv);
     packed.y = pack_bf16(acc.z * inv, acc.w * inv);
     *reinterpret_cast<uint2*>(p.o + row * D + cg * 4) = packed;
-    if (cg == 0 && p.lse != nullptr) p.lse[row] = (M + __log2f(Ltot)) * 0.69314718055994531f;
+    if (cg == 0 && p.lse != nullptr)
+        p.lse[row] = Ltot > 0.f ? (M + __log2f(Ltot)) * 0.69314718055994531f : -INFINITY;
 }
 
 }  // namespace
@@ -552,7 +569,7 @@ cudaError_t launch_pair(const DecodeParams& p, int grid, cudaStream_t stream) {
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     // combine: programmatic dependent launch on the same stream
-    const long long threads = (long long)p.B * p.Hq * (D / 4);
+    const long long threads = (long long)p.B * p.Hq * p.Tq * (D / 4);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((threads + 255) / 256));
     cfg.blockDim = dim3(256);

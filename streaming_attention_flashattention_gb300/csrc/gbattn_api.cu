@@ -194,45 +194,53 @@ int attn_prefill_kvcache(const void* q, const void* kcache, const void* vcache, 
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int num_splits) {
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lmax <= 0 || (d != 64 && d != 128)) return 0;
-    if (num_splits < 0 || num_splits > kMaxSplits) return 0;
-    if (Hq % Hkv != 0) return 0;
-    return decode_workspace_bytes(B, Hq, d, decode_slots(Lmax, num_splits));
+    return attn_decode_multitoken_workspace_size(B, Hq, Hkv, 1, Lmax, d, num_splits);
 }
 
-int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
-                        const int* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
-                        int Lmax, int d, float scale, int num_splits, void* workspace,
-                        size_t ws_bytes, void* stream) {
+size_t attn_decode_multitoken_workspace_size(int B, int Hq, int Hkv, int Tq, int Lmax, int d,
+                                             int num_splits) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Tq <= 0 || Lmax <= 0 || (d != 64 && d != 128)) return 0;
+    if (num_splits < 0 || num_splits > kMaxSplits) return 0;
+    if (Hq % Hkv != 0) return 0;
+    if ((long long)B * Hq * Tq > kIntMax) return 0;
+    return decode_workspace_bytes(B * Tq, Hq, d, decode_slots(Lmax, num_splits));
+}
+
+int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache,
+                           const int* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
+                           int Tq, int Lmax, int d, float scale, int num_splits,
+                           void* workspace, size_t ws_bytes, void* stream) {
     if (!q || !kcache || !vcache || !kv_lens || !o) return GBATTN_ERR_INVALID_ARG;
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lmax <= 0 || d <= 0) return GBATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Tq <= 0 || Lmax <= 0 || d <= 0)
+        return GBATTN_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return GBATTN_ERR_INVALID_ARG;
     if (!(scale > 0.f) || scale != scale) return GBATTN_ERR_INVALID_ARG;
     if (num_splits < 0 || num_splits > kMaxSplits) return GBATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return GBATTN_ERR_UNSUPPORTED;
+    if (Tq > 64) return GBATTN_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
         (lse && !aligned16(lse)) || (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
         return GBATTN_ERR_MISALIGNED;
+    if ((long long)B * Hq * Tq > kIntMax / 8) return GBATTN_ERR_TOO_LARGE;
     const int n_slots = decode_slots(Lmax, num_splits);
-    const size_t need = decode_workspace_bytes(B, Hq, d, n_slots);
+    const size_t need = decode_workspace_bytes(B * Tq, Hq, d, n_slots);
     if (!workspace || ws_bytes < need) return GBATTN_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GBATTN_ERR_MISALIGNED;
     const int G = Hq / Hkv;
-    const int n_hc = (G + 7) / 8;
+    const int R = G * Tq;
+    const int n_hc = (R + 7) / 8;
     const long long n_items = (long long)n_slots * B * Hkv * n_hc;
-    if (n_items > kIntMax || (long long)B * Hkv * Lmax > kIntMax ||
-        (long long)B * Hq > kIntMax / 8)
-        return GBATTN_ERR_TOO_LARGE;
+    if (n_items > kIntMax || (long long)B * Hkv * Lmax > kIntMax) return GBATTN_ERR_TOO_LARGE;
     const int nsm = sm_count();
     if (nsm <= 0) return GBATTN_ERR_CUDA;
 
     DecodeParams p{};
     if (!make_map_bf16_3d(&p.tmap_k, kcache, d, Lmax, (uint64_t)B * Hkv, 64) ||
         !make_map_bf16_3d(&p.tmap_v, vcache, d, Lmax, (uint64_t)B * Hkv, 64) ||
-        !make_map_bf16_3d(&p.tmap_q, q, d, (uint64_t)B * Hq, 1, 8))
+        !make_map_bf16_3d(&p.tmap_q, q, d, (uint64_t)B * Hq * Tq, 1, 8))
         return GBATTN_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const size_t rows = (size_t)B * Hq * n_slots;
+    const size_t rows = (size_t)B * Hq * Tq * n_slots;
     const size_t cnt_bytes = decode_counter_bytes();
     p.counter = reinterpret_cast<int*>(ws);
     p.ws_lse = reinterpret_cast<float*>(ws + cnt_bytes);
@@ -241,6 +249,8 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
     p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Lmax = Lmax; p.G = G;
+    p.Tq = Tq;
+    p.R = R;
     p.n_hc = n_hc;
     p.n_slots = n_slots;
     p.fixed_splits = num_splits;
@@ -250,6 +260,14 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
     if (!p.err) return GBATTN_ERR_CUDA;
     cudaError_t e = launch_decode_splitkv(p, d, nsm, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
+                        const int* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Lmax, int d, float scale, int num_splits, void* workspace,
+                        size_t ws_bytes, void* stream) {
+    return attn_decode_multitoken(q, kcache, vcache, kv_lens, o, lse, B, Hq, Hkv, 1, Lmax, d,
+                                  scale, num_splits, workspace, ws_bytes, stream);
 }
 
 int attn_selftest_bounded_wait(void* stream) {

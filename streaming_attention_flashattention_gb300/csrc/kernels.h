@@ -43,10 +43,12 @@ struct DecodeParams {
     __nv_bfloat16* o;     // [B, Hq, d]
     float* lse;           // [B, Hq] or null
     int* counter;         // work queue counter (zeroed before the split kernel)
-    float* ws_lse;        // [B, Hq, n_slots] log2-domain partial lse
-    float* ws_o;          // [B, Hq, n_slots, d] normalised partial outputs
+    float* ws_lse;        // [B, Hq, Tq, n_slots] log2-domain partial lse
+    float* ws_o;          // [B, Hq, Tq, n_slots, d] normalised partial outputs
     int B, Hq, Hkv, Lmax, G;
-    int n_hc;             // head chunks of <= 8 heads per KV head: ceil(G / 8)
+    int Tq;               // new query tokens per sequence (1: single-token decode)
+    int R;                // query rows per KV head: G * Tq (head-major, token-minor)
+    int n_hc;             // row chunks of <= 8 rows per KV head: ceil(R / 8)
     int n_slots;          // split slots per sequence
     int fixed_splits;     // > 0 fixed count, 0 automatic
     int n_items;          // n_slots * B * Hkv * n_hc
