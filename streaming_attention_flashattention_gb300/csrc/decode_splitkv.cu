@@ -201,11 +201,12 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
             int item = dynamic ? atomicAdd(p.counter, 1) : (int)blockIdx.x;
             for (; ok && item < p.n_items;
                  item = dynamic ? atomicAdd(p.counter, 1) : item + (int)gridDim.x) {
-                // group-major order (split innermost): a group's splits run side by side on
-                // different CTAs
+                // order: row chunk innermost, then split, then KV head, then sequence.  The
+                // row chunks of one split (several when G * Tq > 8) read the same K/V tiles
+                // and run side by side, so all but the first pass hit L2.
                 int rem = item;
-                const int s = rem % p.n_slots; rem /= p.n_slots;
                 const int hc = rem % p.n_hc; rem /= p.n_hc;
+                const int s = rem % p.n_slots; rem /= p.n_slots;
                 const int kvh = rem % p.Hkv; rem /= p.Hkv;
                 const int b = rem;
                 int len = __ldg(&p.kv_lens[b]);
