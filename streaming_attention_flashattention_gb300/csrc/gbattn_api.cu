@@ -108,8 +108,15 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, fl
     p.n_qblk = (Sq + 127) / 128;
     const long long per_group = ((long long)p.n_qblk * p.G + 1) / 2;
     const long long n_pairs = per_group * B * Hkv;
-    if (n_pairs > kIntMax) return GBATTN_ERR_TOO_LARGE;
-    p.n_pairs = (int)n_pairs;
+    const long long n_tiles = (long long)p.n_qblk * B * Hq;
+    if (n_pairs > kIntMax || n_tiles > kIntMax) return GBATTN_ERR_TOO_LARGE;
+    // Pairs of Q tiles keep both ping-pong slots busy with independent work; when they
+    // would not fill the SMs twice over, splitting each tile's KV range over the two slots
+    // halves the longest item instead.
+    const int nsm = sm_count();
+    if (nsm <= 0) return GBATTN_ERR_CUDA;
+    p.kv_split = n_pairs < 2LL * nsm ? 1 : 0;
+    p.n_pairs = (int)(p.kv_split ? n_tiles : n_pairs);
     p.causal = causal;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = device_error_word();

@@ -27,7 +27,8 @@ struct PrefillParams {
     int B, Hq, Hkv, Sq, Skv;
     int G;                // Hq / Hkv
     int n_qblk;           // ceil(Sq / 128)
-    int n_pairs;          // work units (pairs of Q tiles)
+    int n_pairs;          // work items: pairs of Q tiles, or single Q tiles with kv_split
+    int kv_split;         // 1: each CTA splits one Q tile's KV range over its two slots
     int causal;
     float scale_log2;     // scale * log2(e)
     int* err;             // device error word of bounded waits

@@ -25,6 +25,14 @@
 // GQA head packing: the two Q tiles of a CTA are consecutive entries of the list
 // (b, kv head, q block, head in group), so for G >= 2 they are two query heads of one KV
 // head at the same query block and share every K/V tile and the same causal extent.
+//
+// KV-split mode (small problems, where pairs would leave SMs idle): a CTA takes ONE Q tile
+// and gives its two ping-pong slots the two halves of that tile's KV range, [0, n0) and
+// [n0, n).  Each slot keeps its own (m, l, O); at the end the two states are merged
+// inside the CTA with the log-sum-exp rule of "ADR-0060" section 4 (slot 1's O goes
+// through shared memory).  The heaviest causal tiles then take half as long.  The K ring
+// gets a third slot (the unused second Q buffer) because each K/V tile now feeds one
+// S/PV pair instead of two.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -48,8 +56,10 @@ struct PLayout {
     static constexpr int kK0 = 2 * kTileBytes;               // 2 K slots
     static constexpr int kV0 = 4 * kTileBytes;               // 2 V slots
     static constexpr int kBar = 6 * kTileBytes;
-    static constexpr int kNumBars = 16;
-    static constexpr int kTmemSlot = kBar + kNumBars * 8;
+    static constexpr int kNumBars = 18;
+    static constexpr int kXm = kBar + kNumBars * 8;          // split merge: m, l [2 slot][128]
+    static constexpr int kTmemSlot = kXm + 4 * 128 * 4;
+    static constexpr int kOStride = 129;                     // split merge: slot 1's O in the rings
     static constexpr int kBytes = kTmemSlot + 16;
     static constexpr int kAlloc = kBytes + 1024;
     static constexpr uint32_t kColS0 = 0, kColS1 = 128;
@@ -62,7 +72,32 @@ struct TileDesc {
     int h;        // query head
     int q0;       // first query row
     int n_kv;     // KV tiles to visit
+    int kv0;      // first KV tile (KV-split mode: the second half starts at n0)
 };
+
+__device__ __forceinline__ int kv_tiles_of(const PrefillParams& p, int q0) {
+    if (!p.causal) return (p.Skv + kBlockN - 1) / kBlockN;
+    const int last_row = min(q0 + kBlockM, p.Sq) - 1;
+    const int keys = min(p.Skv, last_row + (p.Skv - p.Sq) + 1);
+    return (keys + kBlockN - 1) / kBlockN;
+}
+
+// KV-split mode: item `rank` is one Q tile (heaviest first); slot 0 takes KV tiles
+// [0, n0), slot 1 takes [n0, n), n0 = ceil(n / 2).
+__device__ __forceinline__ void split_tiles(const PrefillParams& p, int rank, int& b, int& kvh,
+                                            TileDesc (&t)[2]) {
+    const int bh_count = p.B * p.Hq;
+    const int qb = p.n_qblk - 1 - rank / bh_count;
+    const int bh = rank % bh_count;
+    b = bh / p.Hq;
+    const int h = bh % p.Hq;
+    kvh = h / p.G;
+    const int q0 = qb * kBlockM;
+    const int n = kv_tiles_of(p, q0);
+    const int n0 = (n + 1) / 2;
+    t[0].present = 1; t[0].h = h; t[0].q0 = q0; t[0].n_kv = n0; t[0].kv0 = 0;
+    t[1].present = n - n0 > 0; t[1].h = h; t[1].q0 = q0; t[1].n_kv = n - n0; t[1].kv0 = n0;
+}
 
 __device__ __forceinline__ void pair_tiles(const PrefillParams& p, int rank, int& b, int& kvh,
                                            TileDesc (&t)[2]) {
@@ -74,8 +109,6 @@ __device__ __forceinline__ void pair_tiles(const PrefillParams& p, int rank, int
     const int grp = rank % n_groups;
     b = grp / p.Hkv;
     kvh = grp % p.Hkv;
-    const int off = p.Skv - p.Sq;
-    const int n_all = (p.Skv + kBlockN - 1) / kBlockN;
     #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int u = 2 * jj + i;
@@ -83,46 +116,55 @@ __device__ __forceinline__ void pair_tiles(const PrefillParams& p, int rank, int
         const int qb = u / p.G, gi = u % p.G;
         t[i].h = kvh * p.G + gi;
         t[i].q0 = qb * kBlockM;
-        int n = n_all;
-        if (p.causal) {
-            const int last_row = min(t[i].q0 + kBlockM, p.Sq) - 1;
-            const int keys = min(p.Skv, last_row + off + 1);
-            n = (keys + kBlockN - 1) / kBlockN;
-        }
-        t[i].n_kv = t[i].present ? n : 0;
+        t[i].n_kv = t[i].present ? kv_tiles_of(p, t[i].q0) : 0;
+        t[i].kv0 = 0;
     }
 }
 
-template <int D>
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
+    constexpr int KS = kSplit ? 3 : 2;   // K ring slots
     using L = PLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
     uint64_t* q_full = bars + 0;
-    uint64_t* k_full = bars + 1;     // [2]
-    uint64_t* k_empty = bars + 3;    // [2]
-    uint64_t* v_full = bars + 5;     // [2]
-    uint64_t* v_empty = bars + 7;    // [2]
-    uint64_t* s_full = bars + 9;     // [2] per Q tile
-    uint64_t* p_ready = bars + 11;   // [2] per Q tile
-    uint64_t* o_done = bars + 13;    // [2] per Q tile
+    uint64_t* k_full = bars + 1;     // [KS]
+    uint64_t* k_empty = bars + 4;    // [KS]
+    uint64_t* v_full = bars + 7;     // [2]
+    uint64_t* v_empty = bars + 9;    // [2]
+    uint64_t* s_full = bars + 11;    // [2] per slot
+    uint64_t* p_ready = bars + 13;   // [2] per slot
+    uint64_t* o_done = bars + 15;    // [2] per slot
+    uint64_t* merge_bar = bars + 17; // KV-split mode: the two softmax warpgroups meet
+    float* xm = reinterpret_cast<float*>(smem + L::kXm);   // [2][128] m, then [2][128] l
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     int b, kvh;
     TileDesc td[2];
-    pair_tiles(p, blockIdx.x, b, kvh, td);
+    if constexpr (kSplit) split_tiles(p, blockIdx.x, b, kvh, td);
+    else pair_tiles(p, blockIdx.x, b, kvh, td);
     const int n_kv_max = max(td[0].n_kv, td[1].n_kv);
+    // K ring slot of fill f: with KV split, slot 0 is the unused second Q buffer
+    auto k_slot = [&](uint32_t f) -> uint8_t* {
+        const uint32_t ks = f % KS;
+        if constexpr (kSplit) return ks == 0 ? smem + L::kQ0 + L::kTileBytes
+                                             : smem + L::kK0 + (ks - 1) * L::kTileBytes;
+        else return smem + L::kK0 + ks * L::kTileBytes;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < KS; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
+        }
+        mbar_init(merge_bar, 8);
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
@@ -143,43 +185,52 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
             prefetch_tensormap(&p.tmap_q);
             prefetch_tensormap(&p.tmap_k);
             prefetch_tensormap(&p.tmap_v);
-            const uint32_t qbytes = (td[1].present ? 2 : 1) * L::kTileBytes;
-            mbar_arrive_expect_tx(q_full, qbytes);
+            // one Q tile per slot (pairs), or one Q tile for both slots (KV split)
+            const int nq = kSplit ? 1 : (td[1].present ? 2 : 1);
+            mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
             #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                if (!td[t].present) continue;
+                if (t >= nq) continue;
                 #pragma unroll
                 for (int bx = 0; bx < L::kBoxes; ++bx)
                     tma_load_3d(smem + L::kQ0 + t * L::kTileBytes + bx * L::kBoxBytes, &p.tmap_q,
                                 bx * 64, td[t].q0, b * p.Hq + td[t].h, q_full);
             }
+            // K/V fills in the order the MMA issuer consumes them: one per KV step for
+            // pairs (shared by both slots), slot 0 then slot 1 per step with KV split
             const int zkv = b * p.Hkv + kvh;
-            int filled_k = 0, filled_v = 0;
+            uint32_t nf = 0, nfv = 0;
             bool ok = true;
             for (int j = 0; j < n_kv_max && ok; ++j) {
-                const int slot = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
-                if (!mbar_wait(&k_empty[slot], ph ^ 1u, kErrWaitProducer, p.err)) { ok = false; break; }
-                mbar_arrive_expect_tx(&k_full[slot], L::kTileBytes);
                 #pragma unroll
-                for (int bx = 0; bx < L::kBoxes; ++bx)
-                    tma_load_3d(smem + L::kK0 + slot * L::kTileBytes + bx * L::kBoxBytes,
-                                &p.tmap_k, bx * 64, j * kBlockN, zkv, &k_full[slot]);
-                filled_k = j + 1;
-                if (!mbar_wait(&v_empty[slot], ph ^ 1u, kErrWaitProducer, p.err)) { ok = false; break; }
-                mbar_arrive_expect_tx(&v_full[slot], L::kTileBytes);
-                #pragma unroll
-                for (int bx = 0; bx < L::kBoxes; ++bx)
-                    tma_load_3d(smem + L::kV0 + slot * L::kTileBytes + bx * L::kBoxBytes,
-                                &p.tmap_v, bx * 64, j * kBlockN, zkv, &v_full[slot]);
-                filled_v = j + 1;
+                for (int t = 0; t < 2; ++t) {
+                    if (!kSplit && t == 1) break;
+                    if (kSplit && j >= td[t].n_kv) continue;
+                    const int tile = kSplit ? td[t].kv0 + j : j;
+                    const uint32_t ks = nf % KS, kph = (nf / KS) & 1;
+                    if (!mbar_wait(&k_empty[ks], kph ^ 1u, kErrWaitProducer, p.err)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&k_full[ks], L::kTileBytes);
+                    #pragma unroll
+                    for (int bx = 0; bx < L::kBoxes; ++bx)
+                        tma_load_3d(k_slot(nf) + bx * L::kBoxBytes, &p.tmap_k, bx * 64,
+                                    tile * kBlockN, zkv, &k_full[ks]);
+                    ++nf;
+                    const uint32_t vs = nfv & 1, vph = (nfv >> 1) & 1;
+                    if (!mbar_wait(&v_empty[vs], vph ^ 1u, kErrWaitProducer, p.err)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&v_full[vs], L::kTileBytes);
+                    #pragma unroll
+                    for (int bx = 0; bx < L::kBoxes; ++bx)
+                        tma_load_3d(smem + L::kV0 + vs * L::kTileBytes + bx * L::kBoxBytes,
+                                    &p.tmap_v, bx * 64, tile * kBlockN, zkv, &v_full[vs]);
+                    ++nfv;
+                }
             }
             // drain: the last fills of each slot must land before the CTA can exit
             mbar_wait(q_full, 0, kErrWaitDrain, p.err);
-            for (int j = max(0, filled_k - 2); j < filled_k; ++j)
-                mbar_wait(&k_full[j & 1], (j >> 1) & 1, kErrWaitDrain, p.err);
-            for (int j = max(0, filled_v - 2); j < filled_v; ++j)
-                mbar_wait(&v_full[j & 1], (j >> 1) & 1, kErrWaitDrain, p.err);
+            for (uint32_t f = nf >= (uint32_t)KS ? nf - KS : 0; f < nf; ++f)
+                mbar_wait(&k_full[f % KS], (f / KS) & 1, kErrWaitDrain, p.err);
+            for (uint32_t f = nfv >= 2 ? nfv - 2 : 0; f < nfv; ++f)
+                mbar_wait(&v_full[f & 1], (f >> 1) & 1, kErrWaitDrain, p.err);
         }
     } else if (warp == 1) {
         // ================================= MMA issuer =================================
@@ -192,13 +243,13 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
             constexpr uint32_t idesc_s = make_idesc_bf16(kBlockM, kBlockN, 0, 0);
             constexpr uint32_t idesc_pv = make_idesc_bf16(kBlockM, D, 0, 1);
             const uint32_t q_base = smem_u32(smem + L::kQ0);
-            const uint32_t k_base = smem_u32(smem + L::kK0);
             const uint32_t v_base = smem_u32(smem + L::kV0);
             const int n0 = td[0].n_kv, n1 = td[1].n_kv;
 
-            auto issue_s = [&](int t, int j) {
-                const uint32_t qa = q_base + t * L::kTileBytes;
-                const uint32_t kb = k_base + (j & 1) * L::kTileBytes;
+            // S_t = Q K^T with the K tile of fill f (Q buffer t for pairs, 0 with KV split)
+            auto issue_s = [&](int t, uint32_t f) {
+                const uint32_t qa = q_base + (kSplit ? 0 : t) * L::kTileBytes;
+                const uint32_t kb = smem_u32(k_slot(f));
                 const uint32_t dst = tmem + (t == 0 ? L::kColS0 : L::kColS1);
                 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -208,10 +259,11 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
                 }
                 mma_commit(&s_full[t]);
             };
-            auto issue_pv = [&](int t, int j) -> bool {
+            // O_t (+)= P_t V with the V tile of fill f; j = the slot's step (0: overwrite O)
+            auto issue_pv = [&](int t, int j, uint32_t f) -> bool {
                 if (!mbar_wait(&p_ready[t], j & 1, kErrWaitMma, p.err)) return false;
                 tc_fence_after();
-                const uint32_t vb = v_base + (j & 1) * L::kTileBytes;
+                const uint32_t vb = v_base + (f & 1) * L::kTileBytes;
                 const uint32_t col_s = t == 0 ? L::kColS0 : L::kColS1;
                 const uint32_t dst = tmem + (t == 0 ? L::kColO0 : L::kColO1);
                 #pragma unroll
@@ -222,33 +274,71 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
                 mma_commit(&o_done[t]);
                 return true;
             };
+            auto wait_k = [&](uint32_t f) -> bool {
+                const bool okw = mbar_wait(&k_full[f % KS], (f / KS) & 1, kErrWaitMma, p.err);
+                tc_fence_after();
+                return okw;
+            };
+            auto wait_v = [&](uint32_t f) -> bool {
+                const bool okw = mbar_wait(&v_full[f & 1], (f >> 1) & 1, kErrWaitMma, p.err);
+                tc_fence_after();
+                return okw;
+            };
 
             bool ok = mbar_wait(q_full, 0, kErrWaitMma, p.err);
             tc_fence_after();
-            if (ok && n_kv_max > 0) {
-                ok = mbar_wait(&k_full[0], 0, kErrWaitMma, p.err);
-                tc_fence_after();
-                if (ok) {
+            if constexpr (!kSplit) {
+                // pairs: KV step j is fill j, shared by both slots
+                if (ok && n_kv_max > 0 && (ok = wait_k(0))) {
                     if (n0 > 0) issue_s(0, 0);
                     if (n1 > 0) issue_s(1, 0);
                     mma_commit(&k_empty[0]);
                 }
-            }
-            for (int j = 0; j < n_kv_max && ok; ++j) {
-                const bool next = j + 1 < n_kv_max;
-                if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, kErrWaitMma, p.err)) break;
-                tc_fence_after();
-                if (j < n0 && !issue_pv(0, j)) break;
-                if (next) {
-                    if (!mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, kErrWaitMma, p.err)) break;
-                    tc_fence_after();
-                    if (j + 1 < n0) issue_s(0, j + 1);
+                for (int j = 0; j < n_kv_max && ok; ++j) {
+                    const bool next = j + 1 < n_kv_max;
+                    if (!wait_v(j)) break;
+                    if (j < n0 && !issue_pv(0, j, j)) break;
+                    if (next) {
+                        if (!wait_k(j + 1)) break;
+                        if (j + 1 < n0) issue_s(0, j + 1);
+                    }
+                    if (j < n1 && !issue_pv(1, j, j)) break;
+                    mma_commit(&v_empty[j & 1]);
+                    if (next) {
+                        if (j + 1 < n1) issue_s(1, j + 1);
+                        mma_commit(&k_empty[(j + 1) % KS]);
+                    }
                 }
-                if (j < n1 && !issue_pv(1, j)) break;
-                mma_commit(&v_empty[j & 1]);
-                if (next) {
-                    if (j + 1 < n1) issue_s(1, j + 1);
-                    mma_commit(&k_empty[(j + 1) & 1]);
+            } else {
+                // KV split: slot 0's step j is fill j + min(j, n1), slot 1's is 2j + 1;
+                // every fill feeds one S and one PV, and is released after each
+                auto f0 = [&](int j) -> uint32_t { return (uint32_t)(j + min(j, n1)); };
+                auto f1 = [&](int j) -> uint32_t { return (uint32_t)(2 * j + 1); };
+                if (ok && (ok = wait_k(f0(0)))) {
+                    issue_s(0, f0(0));
+                    mma_commit(&k_empty[f0(0) % KS]);
+                    if (n1 > 0 && (ok = wait_k(f1(0)))) {
+                        issue_s(1, f1(0));
+                        mma_commit(&k_empty[f1(0) % KS]);
+                    }
+                }
+                for (int j = 0; j < n0 && ok; ++j) {
+                    if (!wait_v(f0(j)) || !issue_pv(0, j, f0(j))) break;
+                    mma_commit(&v_empty[f0(j) & 1]);
+                    if (j + 1 < n0) {
+                        if (!wait_k(f0(j + 1))) break;
+                        issue_s(0, f0(j + 1));
+                        mma_commit(&k_empty[f0(j + 1) % KS]);
+                    }
+                    if (j < n1) {
+                        if (!wait_v(f1(j)) || !issue_pv(1, j, f1(j))) break;
+                        mma_commit(&v_empty[f1(j) & 1]);
+                    }
+                    if (j + 1 < n1) {
+                        if (!wait_k(f1(j + 1))) break;
+                        issue_s(1, f1(j + 1));
+                        mma_commit(&k_empty[f1(j + 1) % KS]);
+                    }
                 }
             }
         }
@@ -271,7 +361,7 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
             for (int j = 0; j < me.n_kv; ++j) {
                 if (!mbar_wait(&s_full[t], j & 1, kErrWaitSoftmax, p.err)) { ok = false; break; }
                 tc_fence_after();
-                const int kbase = j * kBlockN;
+                const int kbase = (me.kv0 + j) * kBlockN;
                 const bool masked = kbase + kBlockN > lim;
                 uint32_t sr[kBlockN];
                 tmem_ld128(t_s, sr);
@@ -341,30 +431,88 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
             // epilogue: O / l -> bf16 -> HBM, LSE
             if (ok && me.n_kv > 0 && mbar_wait(&o_done[t], (me.n_kv - 1) & 1, kErrWaitSoftmax, p.err)) {
                 tc_fence_after();
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                const bool live = row < p.Sq;
                 __nv_bfloat16* orow = p.o + (((long long)b * p.Hq + me.h) * p.Sq + row) * D;
-                #pragma unroll 1
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t rr[32];
-                    tmem_ld32(t_o + ch * 32, rr);
-                    tmem_wait_ld();
-                    if (live) {
-                        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
-                        #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint4 w;
-                            w.x = pack_bf16(__uint_as_float(rr[8 * q4 + 0]) * inv, __uint_as_float(rr[8 * q4 + 1]) * inv);
-                            w.y = pack_bf16(__uint_as_float(rr[8 * q4 + 2]) * inv, __uint_as_float(rr[8 * q4 + 3]) * inv);
-                            w.z = pack_bf16(__uint_as_float(rr[8 * q4 + 4]) * inv, __uint_as_float(rr[8 * q4 + 5]) * inv);
-                            w.w = pack_bf16(__uint_as_float(rr[8 * q4 + 6]) * inv, __uint_as_float(rr[8 * q4 + 7]) * inv);
-                            dst[q4] = w;
+                const bool live = row < p.Sq;
+                if (kSplit && td[1].present) {
+                    // KV split: merge the two halves' states of this row (log-sum-exp):
+                    // O = (a0 O0 + a1 O1) / (a0 l0 + a1 l1), a_t = 2^(m_t - max(m0, m1))
+                    float* ms = xm;              // [2][128] running max per slot
+                    float* ls = xm + 256;        // [2][128] row sum per slot
+                    float* ob = reinterpret_cast<float*>(smem + L::kK0);   // [128][kOStride]
+                    ms[t * 128 + r] = m;
+                    ls[t * 128 + r] = l;
+                    auto meet = [&](uint32_t ph) -> bool {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(merge_bar);
+                        return mbar_wait(merge_bar, ph, kErrWaitSoftmax, p.err);
+                    };
+                    if (meet(0)) {
+                        const float m0 = ms[r], m1 = ms[128 + r];
+                        const float M = fmaxf(m0, m1);
+                        const float a0 = (m0 == -INFINITY) ? 0.f : ex2_approx(m0 - M);
+                        const float a1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - M);
+                        const float lt = a0 * ls[r] + a1 * ls[128 + r];
+                        if (t == 1) {                // slot 1: a1 O1 -> shared memory
+                            #pragma unroll 1
+                            for (int ch = 0; ch < D / 32; ++ch) {
+                                uint32_t rr[32];
+                                tmem_ld32(t_o + ch * 32, rr);
+                                #pragma unroll
+                                for (int e = 0; e < 32; ++e)
+                                    ob[r * L::kOStride + ch * 32 + e] = a1 * __uint_as_float(rr[e]);
+                            }
+                        }
+                        if (meet(1) && t == 0) {     // slot 0: a0 O0 + a1 O1, normalise, store
+                            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                            #pragma unroll 1
+                            for (int ch = 0; ch < D / 32; ++ch) {
+                                uint32_t rr[32];
+                                tmem_ld32(t_o + ch * 32, rr);
+                                if (live) {
+                                    float o32[32];
+                                    #pragma unroll
+                                    for (int e = 0; e < 32; ++e)
+                                        o32[e] = (a0 * __uint_as_float(rr[e]) + ob[r * L::kOStride + ch * 32 + e]) * inv;
+                                    uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+                                    #pragma unroll
+                                    for (int q4 = 0; q4 < 4; ++q4) {
+                                        uint4 w;
+                                        w.x = pack_bf16(o32[8 * q4 + 0], o32[8 * q4 + 1]);
+                                        w.y = pack_bf16(o32[8 * q4 + 2], o32[8 * q4 + 3]);
+                                        w.z = pack_bf16(o32[8 * q4 + 4], o32[8 * q4 + 5]);
+                                        w.w = pack_bf16(o32[8 * q4 + 6], o32[8 * q4 + 7]);
+                                        dst[q4] = w;
+                                    }
+                                }
+                            }
+                            if (live && p.lse != nullptr)
+                                p.lse[((long long)b * p.Hq + me.h) * p.Sq + row] =
+                                    lt > 0.f ? (M + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
                         }
                     }
+                } else {
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    #pragma unroll 1
+                    for (int ch = 0; ch < D / 32; ++ch) {
+                        uint32_t rr[32];
+                        tmem_ld32(t_o + ch * 32, rr);
+                        if (live) {
+                            uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+                            #pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                uint4 w;
+                                w.x = pack_bf16(__uint_as_float(rr[8 * q4 + 0]) * inv, __uint_as_float(rr[8 * q4 + 1]) * inv);
+                                w.y = pack_bf16(__uint_as_float(rr[8 * q4 + 2]) * inv, __uint_as_float(rr[8 * q4 + 3]) * inv);
+                                w.z = pack_bf16(__uint_as_float(rr[8 * q4 + 4]) * inv, __uint_as_float(rr[8 * q4 + 5]) * inv);
+                                w.w = pack_bf16(__uint_as_float(rr[8 * q4 + 6]) * inv, __uint_as_float(rr[8 * q4 + 7]) * inv);
+                                dst[q4] = w;
+                            }
+                        }
+                    }
+                    if (live && p.lse != nullptr)
+                        p.lse[((long long)b * p.Hq + me.h) * p.Sq + row] =
+                            l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
                 }
-                if (live && p.lse != nullptr)
-                    p.lse[((long long)b * p.Hq + me.h) * p.Sq + row] =
-                        l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             }
         }
     }
@@ -377,25 +525,23 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
     }
 }
 
+template <int D, bool kSplit>
+cudaError_t launch_variant(const PrefillParams& p, cudaStream_t stream) {
+    constexpr int smem = PLayout<D>::kAlloc;
+    cudaError_t err = cudaFuncSetAttribute(prefill_fwd_kernel<D, kSplit>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    prefill_fwd_kernel<D, kSplit><<<p.n_pairs, kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_attn_fwd_bf16(const PrefillParams& p, int d, cudaStream_t stream) {
     if (p.n_pairs <= 0) return cudaSuccess;
-    cudaError_t err;
-    if (d == 128) {
-        constexpr int smem = PLayout<128>::kAlloc;
-        err = cudaFuncSetAttribute(prefill_fwd_kernel<128>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (err != cudaSuccess) return err;
-        prefill_fwd_kernel<128><<<p.n_pairs, kThreads, smem, stream>>>(p);
-    } else {
-        constexpr int smem = PLayout<64>::kAlloc;
-        err = cudaFuncSetAttribute(prefill_fwd_kernel<64>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (err != cudaSuccess) return err;
-        prefill_fwd_kernel<64><<<p.n_pairs, kThreads, smem, stream>>>(p);
-    }
-    return cudaGetLastError();
+    if (d == 128)
+        return p.kv_split ? launch_variant<128, true>(p, stream) : launch_variant<128, false>(p, stream);
+    return p.kv_split ? launch_variant<64, true>(p, stream) : launch_variant<64, false>(p, stream);
 }
 
 }  // namespace gbattn

@@ -157,3 +157,14 @@ def test_bounded_wait_expiry_is_reported_and_context_survives():
     st, word = gb.attn_last_device_error()          # read-and-clear
     assert st == 0 and word == 0
     check(small(1, 4, 2, 200, 200, 128, True, seed=13))
+
+
+def test_bf16_pair_mode_full_compare():
+    # 320 pairs of Q tiles (>= 2 per SM): the kernel runs in pair mode (two heads of one
+    # KV head per CTA); the small shapes above run in KV-split mode.
+    check(small(1, 32, 8, 2560, 2560, 128, True, seed=17))
+
+
+def test_bf16_split_mode_ragged_noncausal_long_kv():
+    # few Q tiles and a long KV range: one tile's two KV halves merged in the CTA
+    check(small(1, 2, 1, 100, 3000, 128, False, seed=19))
