@@ -246,16 +246,28 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
             const uint32_t v_base = smem_u32(smem + L::kV0);
             const int n0 = td[0].n_kv, n1 = td[1].n_kv;
 
+            // Operand descriptors are built once; the start-address field (bits 0-13, in
+            // 16-byte units) then advances by a constant per K=16 step, so issuing an MMA
+            // costs one add.  Shared addresses stay below 2^18, so the field cannot carry.
+            // (kept in registers: selected with ternaries, never indexed at run time)
+            const uint64_t dq0 = make_sdesc_sw128(q_base, 16, 1024);
+            const uint64_t dq1 = make_sdesc_sw128(q_base + L::kTileBytes, 16, 1024);
+            const uint64_t dv0 = make_sdesc_sw128(v_base, L::kBoxBytes, 1024);
+            const uint64_t dv1 = make_sdesc_sw128(v_base + L::kTileBytes, L::kBoxBytes, 1024);
+            const uint64_t dk0 = make_sdesc_sw128(smem_u32(k_slot(0)), 16, 1024);
+            const uint64_t dk1 = make_sdesc_sw128(smem_u32(k_slot(1)), 16, 1024);
+            const uint64_t dk2 = make_sdesc_sw128(smem_u32(k_slot(KS - 1)), 16, 1024);
+
             // S_t = Q K^T with the K tile of fill f (Q buffer t for pairs, 0 with KV split)
             auto issue_s = [&](int t, uint32_t f) {
-                const uint32_t qa = q_base + (kSplit ? 0 : t) * L::kTileBytes;
-                const uint32_t kb = smem_u32(k_slot(f));
+                const uint64_t a0 = (kSplit || t == 0) ? dq0 : dq1;
+                const uint32_t ks = f % KS;
+                const uint64_t b0 = ks == 0 ? dk0 : (ks == 1 ? dk1 : dk2);
                 const uint32_t dst = tmem + (t == 0 ? L::kColS0 : L::kColS1);
                 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    mma_bf16_ss(dst, make_sdesc_sw128(qa + off, 16, 1024),
-                                make_sdesc_sw128(kb + off, 16, 1024), idesc_s, kk > 0);
+                    const uint64_t off = (uint64_t)(((kk >> 2) * L::kBoxBytes + (kk & 3) * 32) >> 4);
+                    mma_bf16_ss(dst, a0 + off, b0 + off, idesc_s, kk > 0);
                 }
                 mma_commit(&s_full[t]);
             };
@@ -263,13 +275,12 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
             auto issue_pv = [&](int t, int j, uint32_t f) -> bool {
                 if (!mbar_wait(&p_ready[t], j & 1, kErrWaitMma, p.err)) return false;
                 tc_fence_after();
-                const uint32_t vb = v_base + (f & 1) * L::kTileBytes;
+                const uint64_t b0 = (f & 1) ? dv1 : dv0;
                 const uint32_t col_s = t == 0 ? L::kColS0 : L::kColS1;
                 const uint32_t dst = tmem + (t == 0 ? L::kColO0 : L::kColO1);
                 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    mma_bf16_ts(dst, tmem + col_s + kk * 8,
-                                make_sdesc_sw128(vb + kk * 16 * 128, L::kBoxBytes, 1024),
+                    mma_bf16_ts(dst, tmem + col_s + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4),
                                 idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&o_done[t]);
                 return true;
