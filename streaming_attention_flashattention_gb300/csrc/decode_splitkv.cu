@@ -12,9 +12,8 @@
 //   section 2.1 -- each range is one contiguous block of the cache.
 //
 // GB300 mapping.
-//   split kernel: persistent CTAs (one per SM) take work items (sequence b, KV head,
-//   head chunk, split s): round-robin for a fixed split count, from a device counter for
-//   automatic (length-dependent) splits.  One producer warp streams the split's
+//   split kernel: persistent CTAs (one per SM) pull work items (sequence b, KV head,
+//   row chunk, split s) from a device counter.  One producer warp streams the split's
 //   K and V through a 5-stage shared-memory ring with 3-D TMA copies (64 keys x d,
 //   128-byte swizzle) and mbarrier handoff.  Four consumer warps take 16 keys each per
 //   stage and run S^T = K Q^T and O^T += V^T P^T on mma.sync m16n8k16 with the G <= 8
@@ -193,14 +192,10 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;   // per-stage bits for the exit drain
             bool ok = true;
-            // Work distribution: with a fixed split count every item is the same size and a
-            // static round-robin is already balanced (no counter, no reset before the
-            // launch); with automatic splits the sizes follow the ragged lengths and items
-            // are pulled from a device counter instead.
-            const bool dynamic = p.fixed_splits == 0;
-            int item = dynamic ? atomicAdd(p.counter, 1) : (int)blockIdx.x;
-            for (; ok && item < p.n_items;
-                 item = dynamic ? atomicAdd(p.counter, 1) : item + (int)gridDim.x) {
+            // Items are pulled from a device counter, so a CTA that finishes early takes
+            // more (a static round-robin measured slower even for equal-size splits).
+            for (int item = atomicAdd(p.counter, 1); ok && item < p.n_items;
+                 item = atomicAdd(p.counter, 1)) {
                 // order: row chunk innermost, then split, then KV head, then sequence.  The
                 // row chunks of one split (several when G * Tq > 8) read the same K/V tiles
                 // and run side by side, so all but the first pass hit L2.
@@ -340,11 +335,18 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 }
                 // ---- online softmax over the keys (columns = heads 2c, 2c+1) ----
                 const bool v_lo = g < nvalid, v_hi = g + 8 < nvalid;
-                const int key_lo = si.key0 + R0 + g, key_hi = key_lo + 8;
-                sc[0] = (v_lo && key_lo < lim0) ? sc[0] * scale_log2 : -INFINITY;
-                sc[1] = (v_lo && key_lo < lim1) ? sc[1] * scale_log2 : -INFINITY;
-                sc[2] = (v_hi && key_hi < lim0) ? sc[2] * scale_log2 : -INFINITY;
-                sc[3] = (v_hi && key_hi < lim1) ? sc[3] * scale_log2 : -INFINITY;
+                if (p.Tq == 1) {
+                    sc[0] = v_lo ? sc[0] * scale_log2 : -INFINITY;
+                    sc[1] = v_lo ? sc[1] * scale_log2 : -INFINITY;
+                    sc[2] = v_hi ? sc[2] * scale_log2 : -INFINITY;
+                    sc[3] = v_hi ? sc[3] * scale_log2 : -INFINITY;
+                } else {
+                    const int key_lo = si.key0 + R0 + g, key_hi = key_lo + 8;
+                    sc[0] = (v_lo && key_lo < lim0) ? sc[0] * scale_log2 : -INFINITY;
+                    sc[1] = (v_lo && key_lo < lim1) ? sc[1] * scale_log2 : -INFINITY;
+                    sc[2] = (v_hi && key_hi < lim0) ? sc[2] * scale_log2 : -INFINITY;
+                    sc[3] = (v_hi && key_hi < lim1) ? sc[3] * scale_log2 : -INFINITY;
+                }
                 float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
                 #pragma unroll
                 for (int w = 4; w < 32; w <<= 1) {
@@ -588,10 +590,8 @@ cudaError_t launch_pair(const DecodeParams& p, int grid, cudaStream_t stream) {
 
 cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
                                   cudaStream_t stream) {
-    if (p.fixed_splits == 0) {   // the work counter of the automatic mode starts at zero
-        cudaError_t err = cudaMemsetAsync(p.counter, 0, decode_counter_bytes(), stream);
-        if (err != cudaSuccess) return err;
-    }
+    cudaError_t err = cudaMemsetAsync(p.counter, 0, decode_counter_bytes(), stream);
+    if (err != cudaSuccess) return err;
     const int grid = p.n_items < num_sms ? p.n_items : num_sms;
     if (grid <= 0) return cudaSuccess;
     return d == 128 ? launch_pair<128>(p, grid, stream) : launch_pair<64>(p, grid, stream);
