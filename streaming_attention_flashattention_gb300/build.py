@@ -40,9 +40,19 @@ def _headers():
     return hs
 
 
+STAMP = os.path.join(BUILD, "sources.txt")
+
+
+def _source_list() -> str:
+    return "\n".join(os.path.basename(f) for f in _sources())
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
         return False
+    with open(STAMP) as f:
+        if f.read() != _source_list():       # a source was added or removed
+            return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(f) <= t for f in _sources() + _headers() + [__file__])
 
@@ -76,6 +86,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(_source_list())
     return LIB
 
 

@@ -165,6 +165,24 @@ def test_bf16_pair_mode_full_compare():
     check(small(1, 32, 8, 2560, 2560, 128, True, seed=17))
 
 
+def test_bf16_pair_mode_g1_causal_ragged_odd_tiles():
+    # pair mode with G = 1: a CTA's two Q tiles are consecutive q blocks of one head with
+    # different causal extents; 9 q blocks per head leave a last CTA with one tile, and
+    # Sq = 1100 ends in a ragged tile.
+    check(small(1, 64, 64, 1100, 1100, 128, True, seed=23))
+
+
+def test_bf16_pair_mode_g3_noncausal_ragged():
+    # pair mode with G = 3 and 5 q blocks: 15 tiles per KV head, so pairs straddle q blocks
+    # and the last pair has one tile; ragged Sq and Skv
+    check(small(1, 120, 40, 600, 700, 128, False, seed=29))
+
+
+def test_bf16_single_sm_pair_mode_d64():
+    # d = 64 with >= 2 pairs per SM: the one-SM kernel in pair mode
+    check(small(1, 32, 8, 2560, 2560, 64, True, seed=31))
+
+
 def test_bf16_split_mode_ragged_noncausal_long_kv():
     # few Q tiles and a long KV range: one tile's two KV halves merged in the CTA
     check(small(1, 2, 1, 100, 3000, 128, False, seed=19))
