@@ -13,7 +13,7 @@
 //
 // GB300 mapping.
 //   split kernel: persistent CTAs (one per SM) pull work items (sequence b, KV head,
-//   row chunk, split s) from a device counter.  One producer warp streams the split's
+//   group of row chunks, split s) from a device counter.  One producer warp streams the split's
 //   K and V through a 5-stage shared-memory ring with 3-D TMA copies (64 keys x d,
 //   128-byte swizzle) and mbarrier handoff.  Four consumer warps take 16 keys each per
 //   stage and run S^T = K Q^T and O^T += V^T P^T on mma.sync m16n8k16 with the G <= 8
@@ -23,6 +23,11 @@
 //   (m, l, O); at the end of a split the four states merge through shared memory and the
 //   normalised partial (lse_s, O_s / l_s) goes to the workspace; a group with a single
 //   split writes its final O and LSE directly.
+//   Multi-token decode (T_q > 1) has G * T_q query rows per KV head, in chunks of 8.  An
+//   item then takes NCI = 2 or 4 chunks at once: warp w serves chunk w / (4 / NCI) over
+//   its 64 * NCI / 4 keys of every stage, so each split's K and V are read from HBM once
+//   for all rows instead of once per chunk, and the end-of-split merge runs over the warps
+//   of one chunk.  NCI = 1 is the single-token case above.
 //   combine kernel: one thread per (b, query head, 4 output columns) folds the partials of
 //   the splits.  It is launched with programmatic dependent launch: its CTAs are
 //   scheduled while the split kernel drains and wait on the device (griddepcontrol.wait)
@@ -53,12 +58,12 @@ struct StageInfo {
     int pad;
 };
 
-template <int D>
+template <int D, int NCI>
 struct Layout {
     static constexpr int kBoxes = D / 64;                       // 64-element swizzle boxes
     static constexpr int kKBytes = kKeysPerStage * D * 2;       // K tile
     static constexpr int kVBytes = kKeysPerStage * D * 2;
-    static constexpr int kQBytes = kHeads * D * 2;              // 8 query rows
+    static constexpr int kQBytes = kHeads * NCI * D * 2;        // 8 query rows per chunk
     static constexpr int kStageBytes = kKBytes + kVBytes + kQBytes;   // multiple of 1024
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kInfoOff = kRingBytes;
@@ -134,17 +139,20 @@ __device__ __forceinline__ int splits_for(int len, int fixed_splits) {
     return max(1, min(kMaxSplits, n));
 }
 
-// Final output of one (b, query head): `per` consecutive columns of O (bf16) starting at
+// Final output of one query row: `per` consecutive columns of O (bf16) starting at
 // d0, plus the LSE (natural log) from its log2 value when `with_lse`.
-template <int per>
+template <int D, int per>
 __device__ __forceinline__ void store_final(const DecodeParams& p, long long row, int d0,
                                             const float* ov, bool with_lse, float lse2) {
-    __nv_bfloat16* dst = p.o + row * (per * 16) + d0;
-    if constexpr (per == 8) {
-        uint4 w;
-        w.x = pack_bf16(ov[0], ov[1]); w.y = pack_bf16(ov[2], ov[3]);
-        w.z = pack_bf16(ov[4], ov[5]); w.w = pack_bf16(ov[6], ov[7]);
-        *reinterpret_cast<uint4*>(dst) = w;
+    __nv_bfloat16* dst = p.o + row * D + d0;
+    if constexpr (per % 8 == 0) {
+        #pragma unroll
+        for (int i = 0; i < per; i += 8) {
+            uint4 w;
+            w.x = pack_bf16(ov[i + 0], ov[i + 1]); w.y = pack_bf16(ov[i + 2], ov[i + 3]);
+            w.z = pack_bf16(ov[i + 4], ov[i + 5]); w.w = pack_bf16(ov[i + 6], ov[i + 7]);
+            *reinterpret_cast<uint4*>(dst + i) = w;
+        }
     } else {
         uint2 w;
         w.x = pack_bf16(ov[0], ov[1]); w.y = pack_bf16(ov[2], ov[3]);
@@ -153,10 +161,12 @@ __device__ __forceinline__ void store_final(const DecodeParams& p, long long row
     if (with_lse && p.lse != nullptr) p.lse[row] = lse2 * 0.69314718055994531f;
 }
 
-template <int D>
+template <int D, int NCI>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_split_kernel(const __grid_constant__ DecodeParams p) {
-    using L = Layout<D>;
+    using L = Layout<D, NCI>;
+    constexpr int W = kConsumerWarps / NCI;       // consumer warps per row chunk
+    constexpr int kKeysPerWarp = kKeysPerStage / W;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -200,7 +210,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 // row chunks of one split (several when G * Tq > 8) read the same K/V tiles
                 // and run side by side, so all but the first pass hit L2.
                 int rem = item;
-                const int hc = rem % p.n_hc; rem /= p.n_hc;
+                const int hc = rem % p.n_hg; rem /= p.n_hg;         // chunk group
                 const int s = rem % p.n_slots; rem /= p.n_slots;
                 const int kvh = rem % p.Hkv; rem /= p.Hkv;
                 const int b = rem;
@@ -210,9 +220,9 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 if (s >= nb) continue;
                 const int n_ne = nonempty_splits(len, nb);
                 // rows of this item: the KV head's G * Tq query rows (head-major, token
-                // minor), 8 per head chunk
-                const long long row0 = ((long long)b * p.Hkv + kvh) * p.R + hc * kHeads;
-                const int gcnt = min(kHeads, p.R - hc * kHeads);
+                // minor), 8 per chunk, NCI chunks per group
+                const long long row0 = ((long long)b * p.Hkv + kvh) * p.R + hc * (kHeads * NCI);
+                const int gcnt = min(kHeads * NCI, p.R - hc * (kHeads * NCI));
                 if (s >= n_ne) {
                     // empty split: no partial.  A sequence with no keys at all gets
                     // O = 0, LSE = -inf from its split 0.
@@ -255,11 +265,13 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                                     bx * 64, y, zkv, &full[stage]);
                     }
                     if (tile == 0) {
-                        const int yq = (int)row0;
                         #pragma unroll
-                        for (int bx = 0; bx < L::kBoxes; ++bx)
-                            tma_load_3d(st + L::kKBytes + L::kVBytes + bx * (kHeads * 128),
-                                        &p.tmap_q, bx * 64, yq, 0, &full[stage]);
+                        for (int cq = 0; cq < NCI; ++cq)
+                            #pragma unroll
+                            for (int bx = 0; bx < L::kBoxes; ++bx)
+                                tma_load_3d(st + L::kKBytes + L::kVBytes + bx * (kHeads * NCI * 128) +
+                                                cq * (kHeads * 128),
+                                            &p.tmap_q, bx * 64, (int)row0 + cq * kHeads, 0, &full[stage]);
                     }
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
@@ -294,7 +306,9 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
         int lim0 = 0, lim1 = 0;
         int stage = 0;
         uint32_t phase = 0, sync_phase = 0;
-        const int R0 = warp * 16;   // this warp's 16 keys within a stage
+        const int cw = warp / W;                 // row chunk of this warp within the group
+        const int kp0 = (warp % W) * kKeysPerWarp;   // this warp's first key within a stage
+        int gcnt = 0;                            // rows of this warp's chunk (<= 0: none)
         while (true) {
             if (!mbar_wait(&full[stage], phase, kErrWaitConsumer, p.err)) break;
             const StageInfo si = info[stage];
@@ -302,107 +316,222 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
             const uint32_t kbox = ring + stage * L::kStageBytes;
             const uint32_t vbox = kbox + L::kKBytes;
             const uint32_t qbox = vbox + L::kVBytes;
-            const int gcnt = min(kHeads, p.R - si.hc * kHeads);
+            const int hc = si.hc * NCI + cw;         // this warp's row chunk in the KV head
             if (si.tile == 0) {
+                gcnt = min(kHeads, p.R - hc * kHeads);
                 #pragma unroll
                 for (int s = 0; s < D / 32; ++s) {
                     uint4 z = make_uint4(0, 0, 0, 0);
-                    if (g < gcnt) z = lds128(sw128(qbox + (s >> 1) * (kHeads * 128), g, 2 * c + (s & 1)));
+                    if (g < gcnt)
+                        z = lds128(sw128(qbox + (s >> 1) * (kHeads * NCI * 128), cw * kHeads + g,
+                                         2 * c + (s & 1)));
                     qf[s] = z;
                 }
                 m0 = m1 = -INFINITY;
                 l0 = l1 = 0.f;
                 // causal limit of my two columns (rows hc*8 + 2c, +1): token t of the
                 // Tq new ones sees keys < len - Tq + t + 1 (all keys when Tq = 1)
-                lim0 = si.len - p.Tq + ((si.hc * kHeads + 2 * c) % p.Tq) + 1;
-                lim1 = si.len - p.Tq + ((si.hc * kHeads + 2 * c + 1) % p.Tq) + 1;
+                lim0 = si.len - p.Tq + ((hc * kHeads + 2 * c) % p.Tq) + 1;
+                lim1 = si.len - p.Tq + ((hc * kHeads + 2 * c + 1) % p.Tq) + 1;
                 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt)
                     acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
             }
-            const int nvalid = min(16, si.ntok - R0);
-            if (nvalid > 0) {
-                // ---- S^T[16 keys x 8 heads] = K Q^T ----
-                float sc[4] = {0.f, 0.f, 0.f, 0.f};
-                #pragma unroll
-                for (int s = 0; s < D / 32; ++s) {
-                    const uint32_t kb = kbox + (s >> 1) * (kKeysPerStage * 128);
-                    const int ch = 2 * c + (s & 1);
-                    const uint4 k0 = lds128(sw128(kb, R0 + g, ch));
-                    const uint4 k1 = lds128(sw128(kb, R0 + g + 8, ch));
-                    mma16816(sc, k0.x, k1.x, k0.y, k1.y, qf[s].x, qf[s].y);
-                    mma16816(sc, k0.z, k1.z, k0.w, k1.w, qf[s].z, qf[s].w);
-                }
-                // ---- online softmax over the keys (columns = heads 2c, 2c+1) ----
-                const bool v_lo = g < nvalid, v_hi = g + 8 < nvalid;
-                if (p.Tq == 1) {
-                    sc[0] = v_lo ? sc[0] * scale_log2 : -INFINITY;
-                    sc[1] = v_lo ? sc[1] * scale_log2 : -INFINITY;
-                    sc[2] = v_hi ? sc[2] * scale_log2 : -INFINITY;
-                    sc[3] = v_hi ? sc[3] * scale_log2 : -INFINITY;
-                } else {
-                    const int key_lo = si.key0 + R0 + g, key_hi = key_lo + 8;
-                    sc[0] = (v_lo && key_lo < lim0) ? sc[0] * scale_log2 : -INFINITY;
-                    sc[1] = (v_lo && key_lo < lim1) ? sc[1] * scale_log2 : -INFINITY;
-                    sc[2] = (v_hi && key_hi < lim0) ? sc[2] * scale_log2 : -INFINITY;
-                    sc[3] = (v_hi && key_hi < lim1) ? sc[3] * scale_log2 : -INFINITY;
-                }
-                float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
-                #pragma unroll
-                for (int w = 4; w < 32; w <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, w));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, w));
-                }
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-                const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-                const float corr0 = ex2_approx(m0 - base0), corr1 = ex2_approx(m1 - base1);
-                const float p00 = ex2_approx(sc[0] - base0), p01 = ex2_approx(sc[1] - base1);
-                const float p10 = ex2_approx(sc[2] - base0), p11 = ex2_approx(sc[3] - base1);
-                l0 = l0 * corr0 + p00 + p10;
-                l1 = l1 * corr1 + p01 + p11;
-                m0 = mn0;
-                m1 = mn1;
-                #pragma unroll
-                for (int mt = 0; mt < D / 16; ++mt) {
-                    acc[mt][0] *= corr0; acc[mt][1] *= corr1;
-                    acc[mt][2] *= corr0; acc[mt][3] *= corr1;
-                }
-                // ---- P^T operand: transpose the (key x head) 8x8 blocks in registers ----
-                const uint32_t b0 = movmatrix_trans(pack_bf16(p00, p01));
-                const uint32_t b1 = movmatrix_trans(pack_bf16(p10, p11));
-                // ---- O^T[d x 8 heads] += V^T P^T ----
-                const int tk[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
-                if constexpr (D == 128) {
-                    uint4 vv[4][2];
+            if constexpr (NCI == 1) {
+                const int R0 = kp0;                      // this warp's 16 keys within the stage
+                const int nvalid = min(16, si.ntok - R0);
+                if (nvalid > 0) {
+                    // ---- S^T[16 keys x 8 heads] = K Q^T ----
+                    float sc[4] = {0.f, 0.f, 0.f, 0.f};
                     #pragma unroll
-                    for (int i = 0; i < 4; ++i)
+                    for (int s = 0; s < D / 32; ++s) {
+                        const uint32_t kb = kbox + (s >> 1) * (kKeysPerStage * 128);
+                        const int ch = 2 * c + (s & 1);
+                        const uint4 k0 = lds128(sw128(kb, R0 + g, ch));
+                        const uint4 k1 = lds128(sw128(kb, R0 + g + 8, ch));
+                        mma16816(sc, k0.x, k1.x, k0.y, k1.y, qf[s].x, qf[s].y);
+                        mma16816(sc, k0.z, k1.z, k0.w, k1.w, qf[s].z, qf[s].w);
+                    }
+                    // ---- online softmax over the keys (columns = heads 2c, 2c+1) ----
+                    const bool v_lo = g < nvalid, v_hi = g + 8 < nvalid;
+                    if (p.Tq == 1) {
+                        sc[0] = v_lo ? sc[0] * scale_log2 : -INFINITY;
+                        sc[1] = v_lo ? sc[1] * scale_log2 : -INFINITY;
+                        sc[2] = v_hi ? sc[2] * scale_log2 : -INFINITY;
+                        sc[3] = v_hi ? sc[3] * scale_log2 : -INFINITY;
+                    } else {
+                        const int key_lo = si.key0 + R0 + g, key_hi = key_lo + 8;
+                        sc[0] = (v_lo && key_lo < lim0) ? sc[0] * scale_log2 : -INFINITY;
+                        sc[1] = (v_lo && key_lo < lim1) ? sc[1] * scale_log2 : -INFINITY;
+                        sc[2] = (v_hi && key_hi < lim0) ? sc[2] * scale_log2 : -INFINITY;
+                        sc[3] = (v_hi && key_hi < lim1) ? sc[3] * scale_log2 : -INFINITY;
+                    }
+                    float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+                    #pragma unroll
+                    for (int w = 4; w < 32; w <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, w));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, w));
+                    }
+                    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+                    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+                    const float corr0 = ex2_approx(m0 - base0), corr1 = ex2_approx(m1 - base1);
+                    const float p00 = ex2_approx(sc[0] - base0), p01 = ex2_approx(sc[1] - base1);
+                    const float p10 = ex2_approx(sc[2] - base0), p11 = ex2_approx(sc[3] - base1);
+                    l0 = l0 * corr0 + p00 + p10;
+                    l1 = l1 * corr1 + p01 + p11;
+                    m0 = mn0;
+                    m1 = mn1;
+                    #pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        acc[mt][0] *= corr0; acc[mt][1] *= corr1;
+                        acc[mt][2] *= corr0; acc[mt][3] *= corr1;
+                    }
+                    // ---- P^T operand: transpose the (key x head) 8x8 blocks in registers ----
+                    const uint32_t b0 = movmatrix_trans(pack_bf16(p00, p01));
+                    const uint32_t b1 = movmatrix_trans(pack_bf16(p10, p11));
+                    // ---- O^T[d x 8 heads] += V^T P^T ----
+                    const int tk[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+                    if constexpr (D == 128) {
+                        uint4 vv[4][2];
                         #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
+                        for (int i = 0; i < 4; ++i)
+                            #pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                uint4 z = make_uint4(0, 0, 0, 0);
+                                if (tk[i] < nvalid) z = lds128(sw128(vbox + h * (kKeysPerStage * 128), R0 + tk[i], g));
+                                vv[i][h] = z;
+                            }
+                        #pragma unroll
+                        for (int mt = 0; mt < 8; ++mt)
+                            mma16816(acc[mt], pair_elem(vv[0][0], vv[1][0], mt),
+                                     pair_elem(vv[0][1], vv[1][1], mt),
+                                     pair_elem(vv[2][0], vv[3][0], mt),
+                                     pair_elem(vv[2][1], vv[3][1], mt), b0, b1);
+                    } else {
+                        uint4 vv[4];
+                        #pragma unroll
+                        for (int i = 0; i < 4; ++i) {
                             uint4 z = make_uint4(0, 0, 0, 0);
-                            if (tk[i] < nvalid) z = lds128(sw128(vbox + h * (kKeysPerStage * 128), R0 + tk[i], g));
-                            vv[i][h] = z;
+                            if (tk[i] < nvalid) z = lds128(sw128(vbox, R0 + tk[i], g));
+                            vv[i] = z;
                         }
+                        #pragma unroll
+                        for (int mt = 0; mt < 4; ++mt)
+                            mma16816(acc[mt], pair_elem(vv[0], vv[1], mt),
+                                     pair_elem(vv[0], vv[1], mt + 4),
+                                     pair_elem(vv[2], vv[3], mt),
+                                     pair_elem(vv[2], vv[3], mt + 4), b0, b1);
+                    }
+                }
+            
+            } else {
+                // Several 16-key sub-tiles per warp (multi-token items): all their scores
+                // first, then one max, one correction and the P.V products, so that the
+                // sub-tiles do not form a serial chain of softmax steps.
+                constexpr int NT = kKeysPerWarp / 16;
+                float sc[NT][4];
+                int nvt[NT];
+                bool any = false;
+                #pragma unroll
+                for (int kt = 0; kt < NT; ++kt) {
+                    const int R0 = kp0 + kt * 16;
+                    nvt[kt] = gcnt > 0 ? min(16, si.ntok - R0) : 0;
+                    sc[kt][0] = sc[kt][1] = sc[kt][2] = sc[kt][3] = 0.f;
+                    if (nvt[kt] > 0) {
+                        any = true;
+                        #pragma unroll
+                        for (int s = 0; s < D / 32; ++s) {
+                            const uint32_t kb = kbox + (s >> 1) * (kKeysPerStage * 128);
+                            const int ch = 2 * c + (s & 1);
+                            const uint4 k0 = lds128(sw128(kb, R0 + g, ch));
+                            const uint4 k1 = lds128(sw128(kb, R0 + g + 8, ch));
+                            mma16816(sc[kt], k0.x, k1.x, k0.y, k1.y, qf[s].x, qf[s].y);
+                            mma16816(sc[kt], k0.z, k1.z, k0.w, k1.w, qf[s].z, qf[s].w);
+                        }
+                    }
+                    const int key_lo = si.key0 + R0 + g, key_hi = key_lo + 8;
+                    const bool v_lo = g < nvt[kt], v_hi = g + 8 < nvt[kt];
+                    sc[kt][0] = (v_lo && key_lo < lim0) ? sc[kt][0] * scale_log2 : -INFINITY;
+                    sc[kt][1] = (v_lo && key_lo < lim1) ? sc[kt][1] * scale_log2 : -INFINITY;
+                    sc[kt][2] = (v_hi && key_hi < lim0) ? sc[kt][2] * scale_log2 : -INFINITY;
+                    sc[kt][3] = (v_hi && key_hi < lim1) ? sc[kt][3] * scale_log2 : -INFINITY;
+                }
+                if (any) {
+                    float mx0 = -INFINITY, mx1 = -INFINITY;
                     #pragma unroll
-                    for (int mt = 0; mt < 8; ++mt)
-                        mma16816(acc[mt], pair_elem(vv[0][0], vv[1][0], mt),
-                                 pair_elem(vv[0][1], vv[1][1], mt),
-                                 pair_elem(vv[2][0], vv[3][0], mt),
-                                 pair_elem(vv[2][1], vv[3][1], mt), b0, b1);
-                } else {
-                    uint4 vv[4];
-                    #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint4 z = make_uint4(0, 0, 0, 0);
-                        if (tk[i] < nvalid) z = lds128(sw128(vbox, R0 + tk[i], g));
-                        vv[i] = z;
+                    for (int kt = 0; kt < NT; ++kt) {
+                        mx0 = fmax3(mx0, sc[kt][0], sc[kt][2]);
+                        mx1 = fmax3(mx1, sc[kt][1], sc[kt][3]);
                     }
                     #pragma unroll
-                    for (int mt = 0; mt < 4; ++mt)
-                        mma16816(acc[mt], pair_elem(vv[0], vv[1], mt),
-                                 pair_elem(vv[0], vv[1], mt + 4),
-                                 pair_elem(vv[2], vv[3], mt),
-                                 pair_elem(vv[2], vv[3], mt + 4), b0, b1);
+                    for (int w = 4; w < 32; w <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, w));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, w));
+                    }
+                    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+                    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+                    const float corr0 = ex2_approx(m0 - base0), corr1 = ex2_approx(m1 - base1);
+                    float ps0 = 0.f, ps1 = 0.f;
+                    #pragma unroll
+                    for (int kt = 0; kt < NT; ++kt) {
+                        sc[kt][0] = ex2_approx(sc[kt][0] - base0);
+                        sc[kt][1] = ex2_approx(sc[kt][1] - base1);
+                        sc[kt][2] = ex2_approx(sc[kt][2] - base0);
+                        sc[kt][3] = ex2_approx(sc[kt][3] - base1);
+                        ps0 += sc[kt][0] + sc[kt][2];
+                        ps1 += sc[kt][1] + sc[kt][3];
+                    }
+                    l0 = l0 * corr0 + ps0;
+                    l1 = l1 * corr1 + ps1;
+                    m0 = mn0;
+                    m1 = mn1;
+                    #pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        acc[mt][0] *= corr0; acc[mt][1] *= corr1;
+                        acc[mt][2] *= corr0; acc[mt][3] *= corr1;
+                    }
+                    #pragma unroll
+                    for (int kt = 0; kt < NT; ++kt) {
+                        const int nvalid = nvt[kt];
+                        if (nvalid <= 0) continue;
+                        const int R0 = kp0 + kt * 16;
+                        const uint32_t b0 = movmatrix_trans(pack_bf16(sc[kt][0], sc[kt][1]));
+                        const uint32_t b1 = movmatrix_trans(pack_bf16(sc[kt][2], sc[kt][3]));
+                        const int tk[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+                        if constexpr (D == 128) {
+                            uint4 vv[4][2];
+                            #pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                #pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    uint4 z = make_uint4(0, 0, 0, 0);
+                                    if (tk[i] < nvalid) z = lds128(sw128(vbox + h * (kKeysPerStage * 128), R0 + tk[i], g));
+                                    vv[i][h] = z;
+                                }
+                            #pragma unroll
+                            for (int mt = 0; mt < 8; ++mt)
+                                mma16816(acc[mt], pair_elem(vv[0][0], vv[1][0], mt),
+                                         pair_elem(vv[0][1], vv[1][1], mt),
+                                         pair_elem(vv[2][0], vv[3][0], mt),
+                                         pair_elem(vv[2][1], vv[3][1], mt), b0, b1);
+                        } else {
+                            uint4 vv[4];
+                            #pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                uint4 z = make_uint4(0, 0, 0, 0);
+                                if (tk[i] < nvalid) z = lds128(sw128(vbox, R0 + tk[i], g));
+                                vv[i] = z;
+                            }
+                            #pragma unroll
+                            for (int mt = 0; mt < 4; ++mt)
+                                mma16816(acc[mt], pair_elem(vv[0], vv[1], mt),
+                                         pair_elem(vv[0], vv[1], mt + 4),
+                                         pair_elem(vv[2], vv[3], mt),
+                                         pair_elem(vv[2], vv[3], mt + 4), b0, b1);
+                        }
+                    }
                 }
             }
             __syncwarp();
@@ -435,21 +564,28 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sync_a);
                 if (!mbar_wait(sync_a, sync_phase, kErrWaitConsumer, p.err)) break;
+                // rows of the group: NCI chunks x 8 heads, each finished by kThrPerRow
+                // threads from the states of the W warps of its chunk
+                constexpr int kRows = kHeads * NCI;
+                constexpr int kThrPerRow = (kConsumerWarps * 32) / kRows;
+                constexpr int per = D / kThrPerRow;
                 const int t = threadIdx.x;              // 0..127
-                const int head = t >> 4;
-                constexpr int per = D / 16;
-                const int d0 = (t & 15) * per;
-                const long long row = ((long long)si.b * p.Hkv + si.kvh) * p.R + si.hc * kHeads + head;
-                if (head < gcnt) {
+                const int rloc = t / kThrPerRow;
+                const int cr = rloc / kHeads, head = rloc % kHeads;
+                const int d0 = (t % kThrPerRow) * per;
+                const int hcr = si.hc * NCI + cr;
+                const long long row = ((long long)si.b * p.Hkv + si.kvh) * p.R + hcr * kHeads + head;
+                if (head < min(kHeads, p.R - hcr * kHeads)) {
                     float M = -INFINITY;
                     #pragma unroll
-                    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * kHeads + head]);
-                    float wt[kConsumerWarps], Ltot = 0.f;
+                    for (int w = cr * W; w < cr * W + W; ++w) M = fmaxf(M, red_m[w * kHeads + head]);
+                    float wt[W], Ltot = 0.f;
                     #pragma unroll
-                    for (int w = 0; w < kConsumerWarps; ++w) {
+                    for (int i = 0; i < W; ++i) {
+                        const int w = cr * W + i;
                         const float mw = red_m[w * kHeads + head];
-                        wt[w] = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
-                        Ltot += wt[w] * red_l[w * kHeads + head];
+                        wt[i] = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
+                        Ltot += wt[i] * red_l[w * kHeads + head];
                     }
                     // a row that saw no key in this split (a masked new token) contributes
                     // nothing: O = 0, lse = -inf
@@ -460,19 +596,19 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                     for (int u = 0; u < per; ++u) {
                         float sum = 0.f;
                         #pragma unroll
-                        for (int w = 0; w < kConsumerWarps; ++w)
-                            sum += wt[w] * red_o[(w * kHeads + head) * D + d0 + u];
+                        for (int i = 0; i < W; ++i)
+                            sum += wt[i] * red_o[((cr * W + i) * kHeads + head) * D + d0 + u];
                         ov[u] = sum * inv;
                     }
                     if (si.n_ne == 1) {
-                        store_final<per>(p, row, d0, ov, (t & 15) == 0, lse2);
+                        store_final<D, per>(p, row, d0, ov, (t % kThrPerRow) == 0, lse2);
                     } else {
                         const long long slot = row * p.n_slots + si.s;
                         float* dst = p.ws_o + slot * D + d0;
                         #pragma unroll
                         for (int e = 0; e < per; e += 4)
                             *reinterpret_cast<float4*>(dst + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
-                        if ((t & 15) == 0) p.ws_lse[slot] = lse2;
+                        if ((t % kThrPerRow) == 0) p.ws_lse[slot] = lse2;
                     }
                 }
                 __syncwarp();
@@ -562,13 +698,16 @@ size_t decode_workspace_bytes(int B, int Hq, int d, int n_slots) {
 
 namespace {
 
-template <int D>
-cudaError_t launch_pair(const DecodeParams& p, int grid, cudaStream_t stream) {
-    constexpr int smem = Layout<D>::kAlloc;
-    cudaError_t err = cudaFuncSetAttribute(decode_split_kernel<D>,
+template <int D, int NCI>
+cudaError_t launch_pair(const DecodeParams& p, int num_sms, cudaStream_t stream) {
+    constexpr int smem = Layout<D, NCI>::kAlloc;
+    static_assert(smem <= 227 * 1024, "shared memory budget");
+    const int grid = p.n_items < num_sms ? p.n_items : num_sms;
+    if (grid <= 0) return cudaSuccess;
+    cudaError_t err = cudaFuncSetAttribute(decode_split_kernel<D, NCI>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    decode_split_kernel<D><<<grid, kThreads, smem, stream>>>(p);
+    decode_split_kernel<D, NCI><<<grid, kThreads, smem, stream>>>(p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     // combine: programmatic dependent launch on the same stream
@@ -592,9 +731,14 @@ cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
                                   cudaStream_t stream) {
     cudaError_t err = cudaMemsetAsync(p.counter, 0, decode_counter_bytes(), stream);
     if (err != cudaSuccess) return err;
-    const int grid = p.n_items < num_sms ? p.n_items : num_sms;
-    if (grid <= 0) return cudaSuccess;
-    return d == 128 ? launch_pair<128>(p, grid, stream) : launch_pair<64>(p, grid, stream);
+    if (d == 128) {
+        if (p.nci == 4) return launch_pair<128, 4>(p, num_sms, stream);
+        if (p.nci == 2) return launch_pair<128, 2>(p, num_sms, stream);
+        return launch_pair<128, 1>(p, num_sms, stream);
+    }
+    if (p.nci == 4) return launch_pair<64, 4>(p, num_sms, stream);
+    if (p.nci == 2) return launch_pair<64, 2>(p, num_sms, stream);
+    return launch_pair<64, 1>(p, num_sms, stream);
 }
 
 }  // namespace gbattn

@@ -236,7 +236,10 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
     const int G = Hq / Hkv;
     const int R = G * Tq;
     const int n_hc = (R + 7) / 8;
-    const long long n_items = (long long)n_slots * B * Hkv * n_hc;
+    // one work item serves up to 4 row chunks, so K/V are read once for all of them
+    const int nci = n_hc >= 3 ? 4 : n_hc;
+    const int n_hg = (n_hc + nci - 1) / nci;
+    const long long n_items = (long long)n_slots * B * Hkv * n_hg;
     if (n_items > kIntMax || (long long)B * Hkv * Lmax > kIntMax) return GBATTN_ERR_TOO_LARGE;
     const int nsm = sm_count();
     if (nsm <= 0) return GBATTN_ERR_CUDA;
@@ -259,6 +262,8 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
     p.Tq = Tq;
     p.R = R;
     p.n_hc = n_hc;
+    p.nci = nci;
+    p.n_hg = n_hg;
     p.n_slots = n_slots;
     p.fixed_splits = num_splits;
     p.n_items = (int)n_items;

@@ -50,9 +50,11 @@ struct DecodeParams {
     int Tq;               // new query tokens per sequence (1: single-token decode)
     int R;                // query rows per KV head: G * Tq (head-major, token-minor)
     int n_hc;             // row chunks of <= 8 rows per KV head: ceil(R / 8)
+    int nci;              // row chunks per work item: 1, 2 or 4
+    int n_hg;             // chunk groups per KV head: ceil(n_hc / nci)
     int n_slots;          // split slots per sequence
     int fixed_splits;     // > 0 fixed count, 0 automatic
-    int n_items;          // n_slots * B * Hkv * n_hc
+    int n_items;          // n_slots * B * Hkv * n_hg
     float scale_log2;
     int* err;             // device error word of bounded waits
 };

@@ -52,6 +52,8 @@ def run(B, Hq, Hkv, Tq, Lmax, d, lens, ns, seed=5):
     (3, 8, 8, 3, 700, 128, [700, 65, 3], 16),         # G = 1, ragged, tiny sequences
     (1, 8, 1, 8, 2048, 64, [2048], 3),                # 64 rows, d = 64
     (2, 4, 2, 5, 300, 128, [2, 300], 2),              # len < Tq: rows with no visible key
+    (2, 16, 2, 3, 1500, 128, [1500, 700], 0),         # 3 row chunks: a group of 4 with one empty
+    (1, 8, 2, 10, 900, 128, [900], 2),                # 5 row chunks: a second group of one chunk
 ])
 def test_multitoken_decode_shapes(B, Hq, Hkv, Tq, Lmax, d, lens, ns):
     run(B, Hq, Hkv, Tq, Lmax, d, lens, ns)
