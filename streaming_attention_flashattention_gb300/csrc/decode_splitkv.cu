@@ -24,10 +24,11 @@
 //   normalised partial (lse_s, O_s / l_s) goes to the workspace; a group with a single
 //   split writes its final O and LSE directly.
 //   Multi-token decode (T_q > 1) has G * T_q query rows per KV head, in chunks of 8.  An
-//   item then takes NCI = 2 or 4 chunks at once: warp w serves chunk w / (4 / NCI) over
-//   its 64 * NCI / 4 keys of every stage, so each split's K and V are read from HBM once
-//   for all rows instead of once per chunk, and the end-of-split merge runs over the warps
-//   of one chunk.  NCI = 1 is the single-token case above.
+//   item then takes NCI = 2 or 4 chunks at once, so each split's K and V are read from HBM
+//   once for all rows instead of once per chunk.  Eight consumer warps split every stage
+//   into 4 key slices x 2 halves of the item's chunks; a warp's chunks sit side by side in
+//   the MMA N dimension, so each K and V^T fragment it builds feeds one MMA per chunk.
+//   NCI = 1 is the single-token case above.
 //   combine kernel: one thread per (b, query head, 4 output columns) folds the partials of
 //   the splits.  It is launched with programmatic dependent launch: its CTAs are
 //   scheduled while the split kernel drains and wait on the device (griddepcontrol.wait)
@@ -44,9 +45,18 @@ namespace gbattn {
 namespace {
 
 constexpr int kKeysPerStage = 64;
-constexpr int kConsumerWarps = 4;          // 16 keys each per stage
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 5;
+// Warps and ring depth per kind of work item.  Single-token items (NCI = 1): 4 consumer
+// warps of 16 keys each and a 5-stage ring, one CTA per SM -- HBM bound.  Multi-token
+// items carry NCI times the math per byte of K/V: 8 consumer warps (4 key slices x 2
+// halves of the item's chunks) so that each warp holds fewer chunks' state and more warps
+// hide the MMA and shuffle latencies; the ring drops to 4 stages to make room for their
+// merge buffers.
+template <int NCI>
+struct Cfg {
+    static constexpr int kCW = NCI == 1 ? 4 : 8;           // consumer warps
+    static constexpr int kThreads = (kCW + 1) * 32;
+    static constexpr int kStages = NCI == 1 ? 5 : 4;
+};
 constexpr int kHeads = 8;                  // query heads per work item (MMA N)
 
 struct StageInfo {
@@ -60,6 +70,8 @@ struct StageInfo {
 
 template <int D, int NCI>
 struct Layout {
+    static constexpr int kStages = Cfg<NCI>::kStages;
+    static constexpr int kConsumerWarps = Cfg<NCI>::kCW;
     static constexpr int kBoxes = D / 64;                       // 64-element swizzle boxes
     static constexpr int kKBytes = kKeysPerStage * D * 2;       // K tile
     static constexpr int kVBytes = kKeysPerStage * D * 2;
@@ -162,9 +174,11 @@ __device__ __forceinline__ void store_final(const DecodeParams& p, long long row
 }
 
 template <int D, int NCI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NCI>::kThreads, 1)
 decode_split_kernel(const __grid_constant__ DecodeParams p) {
     using L = Layout<D, NCI>;
+    constexpr int kConsumerWarps = Cfg<NCI>::kCW;
+    constexpr int kStages = Cfg<NCI>::kStages;
     constexpr int W = kConsumerWarps / NCI;       // consumer warps per row chunk
     constexpr int kKeysPerWarp = kKeysPerStage / W;
     extern __shared__ uint8_t smem_raw[];
@@ -173,7 +187,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
     StageInfo* info = reinterpret_cast<StageInfo*>(smem + L::kInfoOff);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
     uint64_t* full = bars;                   // [kStages] producer -> consumers (TMA bytes)
-    uint64_t* empty = bars + kStages;        // [kStages] consumers -> producer (4 arrivals)
+    uint64_t* empty = bars + kStages;        // [kStages] consumers -> producer (one per warp)
     uint64_t* sync_a = bars + 2 * kStages;   // consumer-warp rendezvous at a split's end
     uint64_t* sync_b = sync_a + 1;
     float* red_m = reinterpret_cast<float*>(smem + L::kRedMOff);
@@ -255,7 +269,11 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                     si.key0 = y;
                     si.len = len;
                     uint8_t* st = smem + stage * L::kStageBytes;
-                    const uint32_t bytes = L::kKBytes + L::kVBytes + (tile == 0 ? L::kQBytes : 0);
+                    // single-token items load Q with their first tile only; stacked
+                    // multi-token items re-read it from every stage (no registers to keep
+                    // NCI chunks of it)
+                    const bool with_q = tile == 0 || NCI > 1;
+                    const uint32_t bytes = L::kKBytes + L::kVBytes + (with_q ? L::kQBytes : 0);
                     mbar_arrive_expect_tx(&full[stage], bytes);
                     #pragma unroll
                     for (int bx = 0; bx < L::kBoxes; ++bx) {
@@ -264,7 +282,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                         tma_load_3d(st + L::kKBytes + bx * (kKeysPerStage * 128), &p.tmap_v,
                                     bx * 64, y, zkv, &full[stage]);
                     }
-                    if (tile == 0) {
+                    if (with_q) {
                         #pragma unroll
                         for (int cq = 0; cq < NCI; ++cq)
                             #pragma unroll
@@ -295,8 +313,8 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
             for (int i = 0; i < kStages; ++i)
                 if (filled & (1u << i)) mbar_wait(&full[i], (fill_parity >> i) & 1u, kErrWaitDrain, p.err);
         }
-    } else {
-        // ============================== consumer warps =============================
+    } else if constexpr (NCI == 1) {
+        // ======================= consumer warps (single token) ======================
         const int g = lane >> 2, c = lane & 3;
         const uint32_t ring = smem_u32(smem);
         const float scale_log2 = p.scale_log2;
@@ -337,203 +355,93 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 for (int mt = 0; mt < D / 16; ++mt)
                     acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
             }
-            if constexpr (NCI == 1) {
-                const int R0 = kp0;                      // this warp's 16 keys within the stage
-                const int nvalid = min(16, si.ntok - R0);
-                if (nvalid > 0) {
-                    // ---- S^T[16 keys x 8 heads] = K Q^T ----
-                    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-                    #pragma unroll
-                    for (int s = 0; s < D / 32; ++s) {
-                        const uint32_t kb = kbox + (s >> 1) * (kKeysPerStage * 128);
-                        const int ch = 2 * c + (s & 1);
-                        const uint4 k0 = lds128(sw128(kb, R0 + g, ch));
-                        const uint4 k1 = lds128(sw128(kb, R0 + g + 8, ch));
-                        mma16816(sc, k0.x, k1.x, k0.y, k1.y, qf[s].x, qf[s].y);
-                        mma16816(sc, k0.z, k1.z, k0.w, k1.w, qf[s].z, qf[s].w);
-                    }
-                    // ---- online softmax over the keys (columns = heads 2c, 2c+1) ----
-                    const bool v_lo = g < nvalid, v_hi = g + 8 < nvalid;
-                    if (p.Tq == 1) {
-                        sc[0] = v_lo ? sc[0] * scale_log2 : -INFINITY;
-                        sc[1] = v_lo ? sc[1] * scale_log2 : -INFINITY;
-                        sc[2] = v_hi ? sc[2] * scale_log2 : -INFINITY;
-                        sc[3] = v_hi ? sc[3] * scale_log2 : -INFINITY;
-                    } else {
-                        const int key_lo = si.key0 + R0 + g, key_hi = key_lo + 8;
-                        sc[0] = (v_lo && key_lo < lim0) ? sc[0] * scale_log2 : -INFINITY;
-                        sc[1] = (v_lo && key_lo < lim1) ? sc[1] * scale_log2 : -INFINITY;
-                        sc[2] = (v_hi && key_hi < lim0) ? sc[2] * scale_log2 : -INFINITY;
-                        sc[3] = (v_hi && key_hi < lim1) ? sc[3] * scale_log2 : -INFINITY;
-                    }
-                    float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
-                    #pragma unroll
-                    for (int w = 4; w < 32; w <<= 1) {
-                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, w));
-                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, w));
-                    }
-                    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-                    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-                    const float corr0 = ex2_approx(m0 - base0), corr1 = ex2_approx(m1 - base1);
-                    const float p00 = ex2_approx(sc[0] - base0), p01 = ex2_approx(sc[1] - base1);
-                    const float p10 = ex2_approx(sc[2] - base0), p11 = ex2_approx(sc[3] - base1);
-                    l0 = l0 * corr0 + p00 + p10;
-                    l1 = l1 * corr1 + p01 + p11;
-                    m0 = mn0;
-                    m1 = mn1;
-                    #pragma unroll
-                    for (int mt = 0; mt < D / 16; ++mt) {
-                        acc[mt][0] *= corr0; acc[mt][1] *= corr1;
-                        acc[mt][2] *= corr0; acc[mt][3] *= corr1;
-                    }
-                    // ---- P^T operand: transpose the (key x head) 8x8 blocks in registers ----
-                    const uint32_t b0 = movmatrix_trans(pack_bf16(p00, p01));
-                    const uint32_t b1 = movmatrix_trans(pack_bf16(p10, p11));
-                    // ---- O^T[d x 8 heads] += V^T P^T ----
-                    const int tk[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
-                    if constexpr (D == 128) {
-                        uint4 vv[4][2];
-                        #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            #pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                uint4 z = make_uint4(0, 0, 0, 0);
-                                if (tk[i] < nvalid) z = lds128(sw128(vbox + h * (kKeysPerStage * 128), R0 + tk[i], g));
-                                vv[i][h] = z;
-                            }
-                        #pragma unroll
-                        for (int mt = 0; mt < 8; ++mt)
-                            mma16816(acc[mt], pair_elem(vv[0][0], vv[1][0], mt),
-                                     pair_elem(vv[0][1], vv[1][1], mt),
-                                     pair_elem(vv[2][0], vv[3][0], mt),
-                                     pair_elem(vv[2][1], vv[3][1], mt), b0, b1);
-                    } else {
-                        uint4 vv[4];
-                        #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            uint4 z = make_uint4(0, 0, 0, 0);
-                            if (tk[i] < nvalid) z = lds128(sw128(vbox, R0 + tk[i], g));
-                            vv[i] = z;
-                        }
-                        #pragma unroll
-                        for (int mt = 0; mt < 4; ++mt)
-                            mma16816(acc[mt], pair_elem(vv[0], vv[1], mt),
-                                     pair_elem(vv[0], vv[1], mt + 4),
-                                     pair_elem(vv[2], vv[3], mt),
-                                     pair_elem(vv[2], vv[3], mt + 4), b0, b1);
-                    }
-                }
-            
-            } else {
-                // Several 16-key sub-tiles per warp (multi-token items): all their scores
-                // first, then one max, one correction and the P.V products, so that the
-                // sub-tiles do not form a serial chain of softmax steps.
-                constexpr int NT = kKeysPerWarp / 16;
-                float sc[NT][4];
-                int nvt[NT];
-                bool any = false;
+            const int R0 = kp0;                      // this warp's 16 keys within the stage
+            const int nvalid = min(16, si.ntok - R0);
+            if (nvalid > 0) {
+                // ---- S^T[16 keys x 8 heads] = K Q^T ----
+                float sc[4] = {0.f, 0.f, 0.f, 0.f};
                 #pragma unroll
-                for (int kt = 0; kt < NT; ++kt) {
-                    const int R0 = kp0 + kt * 16;
-                    nvt[kt] = gcnt > 0 ? min(16, si.ntok - R0) : 0;
-                    sc[kt][0] = sc[kt][1] = sc[kt][2] = sc[kt][3] = 0.f;
-                    if (nvt[kt] > 0) {
-                        any = true;
-                        #pragma unroll
-                        for (int s = 0; s < D / 32; ++s) {
-                            const uint32_t kb = kbox + (s >> 1) * (kKeysPerStage * 128);
-                            const int ch = 2 * c + (s & 1);
-                            const uint4 k0 = lds128(sw128(kb, R0 + g, ch));
-                            const uint4 k1 = lds128(sw128(kb, R0 + g + 8, ch));
-                            mma16816(sc[kt], k0.x, k1.x, k0.y, k1.y, qf[s].x, qf[s].y);
-                            mma16816(sc[kt], k0.z, k1.z, k0.w, k1.w, qf[s].z, qf[s].w);
-                        }
-                    }
-                    const int key_lo = si.key0 + R0 + g, key_hi = key_lo + 8;
-                    const bool v_lo = g < nvt[kt], v_hi = g + 8 < nvt[kt];
-                    sc[kt][0] = (v_lo && key_lo < lim0) ? sc[kt][0] * scale_log2 : -INFINITY;
-                    sc[kt][1] = (v_lo && key_lo < lim1) ? sc[kt][1] * scale_log2 : -INFINITY;
-                    sc[kt][2] = (v_hi && key_hi < lim0) ? sc[kt][2] * scale_log2 : -INFINITY;
-                    sc[kt][3] = (v_hi && key_hi < lim1) ? sc[kt][3] * scale_log2 : -INFINITY;
+                for (int s = 0; s < D / 32; ++s) {
+                    const uint32_t kb = kbox + (s >> 1) * (kKeysPerStage * 128);
+                    const int ch = 2 * c + (s & 1);
+                    const uint4 k0 = lds128(sw128(kb, R0 + g, ch));
+                    const uint4 k1 = lds128(sw128(kb, R0 + g + 8, ch));
+                    mma16816(sc, k0.x, k1.x, k0.y, k1.y, qf[s].x, qf[s].y);
+                    mma16816(sc, k0.z, k1.z, k0.w, k1.w, qf[s].z, qf[s].w);
                 }
-                if (any) {
-                    float mx0 = -INFINITY, mx1 = -INFINITY;
+                // ---- online softmax over the keys (columns = heads 2c, 2c+1) ----
+                const bool v_lo = g < nvalid, v_hi = g + 8 < nvalid;
+                if (p.Tq == 1) {
+                    sc[0] = v_lo ? sc[0] * scale_log2 : -INFINITY;
+                    sc[1] = v_lo ? sc[1] * scale_log2 : -INFINITY;
+                    sc[2] = v_hi ? sc[2] * scale_log2 : -INFINITY;
+                    sc[3] = v_hi ? sc[3] * scale_log2 : -INFINITY;
+                } else {
+                    const int key_lo = si.key0 + R0 + g, key_hi = key_lo + 8;
+                    sc[0] = (v_lo && key_lo < lim0) ? sc[0] * scale_log2 : -INFINITY;
+                    sc[1] = (v_lo && key_lo < lim1) ? sc[1] * scale_log2 : -INFINITY;
+                    sc[2] = (v_hi && key_hi < lim0) ? sc[2] * scale_log2 : -INFINITY;
+                    sc[3] = (v_hi && key_hi < lim1) ? sc[3] * scale_log2 : -INFINITY;
+                }
+                float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+                #pragma unroll
+                for (int w = 4; w < 32; w <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, w));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, w));
+                }
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+                const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+                const float corr0 = ex2_approx(m0 - base0), corr1 = ex2_approx(m1 - base1);
+                const float p00 = ex2_approx(sc[0] - base0), p01 = ex2_approx(sc[1] - base1);
+                const float p10 = ex2_approx(sc[2] - base0), p11 = ex2_approx(sc[3] - base1);
+                l0 = l0 * corr0 + p00 + p10;
+                l1 = l1 * corr1 + p01 + p11;
+                m0 = mn0;
+                m1 = mn1;
+                #pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    acc[mt][0] *= corr0; acc[mt][1] *= corr1;
+                    acc[mt][2] *= corr0; acc[mt][3] *= corr1;
+                }
+                // ---- P^T operand: transpose the (key x head) 8x8 blocks in registers ----
+                const uint32_t b0 = movmatrix_trans(pack_bf16(p00, p01));
+                const uint32_t b1 = movmatrix_trans(pack_bf16(p10, p11));
+                // ---- O^T[d x 8 heads] += V^T P^T ----
+                const int tk[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+                if constexpr (D == 128) {
+                    uint4 vv[4][2];
                     #pragma unroll
-                    for (int kt = 0; kt < NT; ++kt) {
-                        mx0 = fmax3(mx0, sc[kt][0], sc[kt][2]);
-                        mx1 = fmax3(mx1, sc[kt][1], sc[kt][3]);
-                    }
-                    #pragma unroll
-                    for (int w = 4; w < 32; w <<= 1) {
-                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, w));
-                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, w));
-                    }
-                    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-                    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-                    const float corr0 = ex2_approx(m0 - base0), corr1 = ex2_approx(m1 - base1);
-                    float ps0 = 0.f, ps1 = 0.f;
-                    #pragma unroll
-                    for (int kt = 0; kt < NT; ++kt) {
-                        sc[kt][0] = ex2_approx(sc[kt][0] - base0);
-                        sc[kt][1] = ex2_approx(sc[kt][1] - base1);
-                        sc[kt][2] = ex2_approx(sc[kt][2] - base0);
-                        sc[kt][3] = ex2_approx(sc[kt][3] - base1);
-                        ps0 += sc[kt][0] + sc[kt][2];
-                        ps1 += sc[kt][1] + sc[kt][3];
-                    }
-                    l0 = l0 * corr0 + ps0;
-                    l1 = l1 * corr1 + ps1;
-                    m0 = mn0;
-                    m1 = mn1;
-                    #pragma unroll
-                    for (int mt = 0; mt < D / 16; ++mt) {
-                        acc[mt][0] *= corr0; acc[mt][1] *= corr1;
-                        acc[mt][2] *= corr0; acc[mt][3] *= corr1;
-                    }
-                    #pragma unroll
-                    for (int kt = 0; kt < NT; ++kt) {
-                        const int nvalid = nvt[kt];
-                        if (nvalid <= 0) continue;
-                        const int R0 = kp0 + kt * 16;
-                        const uint32_t b0 = movmatrix_trans(pack_bf16(sc[kt][0], sc[kt][1]));
-                        const uint32_t b1 = movmatrix_trans(pack_bf16(sc[kt][2], sc[kt][3]));
-                        const int tk[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
-                        if constexpr (D == 128) {
-                            uint4 vv[4][2];
-                            #pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                #pragma unroll
-                                for (int h = 0; h < 2; ++h) {
-                                    uint4 z = make_uint4(0, 0, 0, 0);
-                                    if (tk[i] < nvalid) z = lds128(sw128(vbox + h * (kKeysPerStage * 128), R0 + tk[i], g));
-                                    vv[i][h] = z;
-                                }
-                            #pragma unroll
-                            for (int mt = 0; mt < 8; ++mt)
-                                mma16816(acc[mt], pair_elem(vv[0][0], vv[1][0], mt),
-                                         pair_elem(vv[0][1], vv[1][1], mt),
-                                         pair_elem(vv[2][0], vv[3][0], mt),
-                                         pair_elem(vv[2][1], vv[3][1], mt), b0, b1);
-                        } else {
-                            uint4 vv[4];
-                            #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                uint4 z = make_uint4(0, 0, 0, 0);
-                                if (tk[i] < nvalid) z = lds128(sw128(vbox, R0 + tk[i], g));
-                                vv[i] = z;
-                            }
-                            #pragma unroll
-                            for (int mt = 0; mt < 4; ++mt)
-                                mma16816(acc[mt], pair_elem(vv[0], vv[1], mt),
-                                         pair_elem(vv[0], vv[1], mt + 4),
-                                         pair_elem(vv[2], vv[3], mt),
-                                         pair_elem(vv[2], vv[3], mt + 4), b0, b1);
+                    for (int i = 0; i < 4; ++i)
+                        #pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint4 z = make_uint4(0, 0, 0, 0);
+                            if (tk[i] < nvalid) z = lds128(sw128(vbox + h * (kKeysPerStage * 128), R0 + tk[i], g));
+                            vv[i][h] = z;
                         }
+                    #pragma unroll
+                    for (int mt = 0; mt < 8; ++mt)
+                        mma16816(acc[mt], pair_elem(vv[0][0], vv[1][0], mt),
+                                 pair_elem(vv[0][1], vv[1][1], mt),
+                                 pair_elem(vv[2][0], vv[3][0], mt),
+                                 pair_elem(vv[2][1], vv[3][1], mt), b0, b1);
+                } else {
+                    uint4 vv[4];
+                    #pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 z = make_uint4(0, 0, 0, 0);
+                        if (tk[i] < nvalid) z = lds128(sw128(vbox, R0 + tk[i], g));
+                        vv[i] = z;
                     }
+                    #pragma unroll
+                    for (int mt = 0; mt < 4; ++mt)
+                        mma16816(acc[mt], pair_elem(vv[0], vv[1], mt),
+                                 pair_elem(vv[0], vv[1], mt + 4),
+                                 pair_elem(vv[2], vv[3], mt),
+                                 pair_elem(vv[2], vv[3], mt + 4), b0, b1);
                 }
             }
+        
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
 
@@ -615,6 +523,232 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 if (lane == 0) mbar_arrive(sync_b);
                 if (!mbar_wait(sync_b, sync_phase, kErrWaitConsumer, p.err)) break;
                 sync_phase ^= 1u;
+            }
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+    } else {
+        // ================== consumer warps (multi-token: chunks stacked) ==================
+        // Warp w takes keys [16 (w % 4), +16) of every stage for chunks
+        // (w / 4) * CPW .. + CPW - 1 of the item, side by side in the MMA N dimension: each K
+        // fragment and each V^T fragment (the byte permutes included) is built once and
+        // feeds CPW MMAs.  Q comes from every stage; per-chunk (m, l, O) stay in registers.
+        constexpr int CPW = NCI * 4 / kConsumerWarps;   // row chunks per warp
+        const int g = lane >> 2, c = lane & 3;
+        const uint32_t ring = smem_u32(smem);
+        const float scale_log2 = p.scale_log2;
+        float acc[CPW][D / 16][4];
+        float m0[CPW], m1[CPW], l0[CPW], l1[CPW];
+        int lim0[CPW], lim1[CPW], rows[CPW];
+        int stage = 0;
+        uint32_t phase = 0, sync_phase = 0;
+        const int R0 = (warp & 3) * 16;          // this warp's 16 keys within a stage
+        const int qd = warp >> 2;                // which half of the item's chunks
+        bool run = true;
+        while (run) {
+            if (!mbar_wait(&full[stage], phase, kErrWaitConsumer, p.err)) break;
+            const StageInfo si = info[stage];
+            if (si.done) break;
+            const uint32_t kbox = ring + stage * L::kStageBytes;
+            const uint32_t vbox = kbox + L::kKBytes;
+            const uint32_t qbox = vbox + L::kVBytes;
+            if (si.tile == 0) {
+                #pragma unroll
+                for (int cq = 0; cq < CPW; ++cq) {
+                    const int hc = si.hc * NCI + qd * CPW + cq;
+                    rows[cq] = min(kHeads, p.R - hc * kHeads);
+                    m0[cq] = m1[cq] = -INFINITY;
+                    l0[cq] = l1[cq] = 0.f;
+                    // causal limit of my two columns (rows hc*8 + 2c, +1)
+                    lim0[cq] = si.len - p.Tq + ((hc * kHeads + 2 * c) % p.Tq) + 1;
+                    lim1[cq] = si.len - p.Tq + ((hc * kHeads + 2 * c + 1) % p.Tq) + 1;
+                    #pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt)
+                        acc[cq][mt][0] = acc[cq][mt][1] = acc[cq][mt][2] = acc[cq][mt][3] = 0.f;
+                }
+            }
+            const int nvalid = min(16, si.ntok - R0);
+            if (nvalid > 0) {
+                // ---- S^T[16 keys x 8 rows] per chunk = K Q^T ----
+                float sc[CPW][4];
+                #pragma unroll
+                for (int cq = 0; cq < CPW; ++cq) sc[cq][0] = sc[cq][1] = sc[cq][2] = sc[cq][3] = 0.f;
+                #pragma unroll
+                for (int s = 0; s < D / 32; ++s) {
+                    const uint32_t kb = kbox + (s >> 1) * (kKeysPerStage * 128);
+                    const int ch = 2 * c + (s & 1);
+                    const uint4 k0 = lds128(sw128(kb, R0 + g, ch));
+                    const uint4 k1 = lds128(sw128(kb, R0 + g + 8, ch));
+                    #pragma unroll
+                    for (int cq = 0; cq < CPW; ++cq) {
+                        if (rows[cq] <= 0) continue;
+                        const uint4 qv = lds128(sw128(qbox + (s >> 1) * (kHeads * NCI * 128),
+                                                      (qd * CPW + cq) * kHeads + g, ch));
+                        mma16816(sc[cq], k0.x, k1.x, k0.y, k1.y, qv.x, qv.y);
+                        mma16816(sc[cq], k0.z, k1.z, k0.w, k1.w, qv.z, qv.w);
+                    }
+                }
+                // ---- online softmax per chunk (columns = rows 2c, 2c+1 of the chunk) ----
+                const bool v_lo = g < nvalid, v_hi = g + 8 < nvalid;
+                const int key_lo = si.key0 + R0 + g, key_hi = key_lo + 8;
+                uint32_t pb0[CPW], pb1[CPW];
+                #pragma unroll
+                for (int cq = 0; cq < CPW; ++cq) {
+                    pb0[cq] = pb1[cq] = 0u;
+                    if (rows[cq] <= 0) continue;
+                    const float s0 = (v_lo && key_lo < lim0[cq]) ? sc[cq][0] * scale_log2 : -INFINITY;
+                    const float s1 = (v_lo && key_lo < lim1[cq]) ? sc[cq][1] * scale_log2 : -INFINITY;
+                    const float s2 = (v_hi && key_hi < lim0[cq]) ? sc[cq][2] * scale_log2 : -INFINITY;
+                    const float s3 = (v_hi && key_hi < lim1[cq]) ? sc[cq][3] * scale_log2 : -INFINITY;
+                    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+                    #pragma unroll
+                    for (int w = 4; w < 32; w <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, w));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, w));
+                    }
+                    const float mn0 = fmaxf(m0[cq], mx0), mn1 = fmaxf(m1[cq], mx1);
+                    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+                    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+                    const float corr0 = ex2_approx(m0[cq] - base0), corr1 = ex2_approx(m1[cq] - base1);
+                    const float p00 = ex2_approx(s0 - base0), p01 = ex2_approx(s1 - base1);
+                    const float p10 = ex2_approx(s2 - base0), p11 = ex2_approx(s3 - base1);
+                    l0[cq] = l0[cq] * corr0 + p00 + p10;
+                    l1[cq] = l1[cq] * corr1 + p01 + p11;
+                    m0[cq] = mn0;
+                    m1[cq] = mn1;
+                    #pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        acc[cq][mt][0] *= corr0; acc[cq][mt][1] *= corr1;
+                        acc[cq][mt][2] *= corr0; acc[cq][mt][3] *= corr1;
+                    }
+                    pb0[cq] = movmatrix_trans(pack_bf16(p00, p01));
+                    pb1[cq] = movmatrix_trans(pack_bf16(p10, p11));
+                }
+                // ---- O^T[d x 8 rows] per chunk += V^T P^T ----
+                const int tk[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+                if constexpr (D == 128) {
+                    uint4 vv[4][2];
+                    #pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        #pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint4 z = make_uint4(0, 0, 0, 0);
+                            if (tk[i] < nvalid) z = lds128(sw128(vbox + h * (kKeysPerStage * 128), R0 + tk[i], g));
+                            vv[i][h] = z;
+                        }
+                    #pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        const uint32_t a0 = pair_elem(vv[0][0], vv[1][0], mt);
+                        const uint32_t a1 = pair_elem(vv[0][1], vv[1][1], mt);
+                        const uint32_t a2 = pair_elem(vv[2][0], vv[3][0], mt);
+                        const uint32_t a3 = pair_elem(vv[2][1], vv[3][1], mt);
+                        #pragma unroll
+                        for (int cq = 0; cq < CPW; ++cq)
+                            if (rows[cq] > 0) mma16816(acc[cq][mt], a0, a1, a2, a3, pb0[cq], pb1[cq]);
+                    }
+                } else {
+                    uint4 vv[4];
+                    #pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 z = make_uint4(0, 0, 0, 0);
+                        if (tk[i] < nvalid) z = lds128(sw128(vbox, R0 + tk[i], g));
+                        vv[i] = z;
+                    }
+                    #pragma unroll
+                    for (int mt = 0; mt < 4; ++mt) {
+                        const uint32_t a0 = pair_elem(vv[0], vv[1], mt);
+                        const uint32_t a1 = pair_elem(vv[0], vv[1], mt + 4);
+                        const uint32_t a2 = pair_elem(vv[2], vv[3], mt);
+                        const uint32_t a3 = pair_elem(vv[2], vv[3], mt + 4);
+                        #pragma unroll
+                        for (int cq = 0; cq < CPW; ++cq)
+                            if (rows[cq] > 0) mma16816(acc[cq][mt], a0, a1, a2, a3, pb0[cq], pb1[cq]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+
+            if (si.last) {
+                // ---- CPW rounds; in round r each half merges its chunk r over its four
+                // warps (red_* hold every warp's 8 rows) and writes the partial ----
+                #pragma unroll
+                for (int r = 0; r < CPW; ++r) {
+                    if (!run) continue;
+                    float lr0 = l0[r], lr1 = l1[r];
+                    #pragma unroll
+                    for (int w = 4; w < 32; w <<= 1) {
+                        lr0 += __shfl_xor_sync(0xffffffffu, lr0, w);
+                        lr1 += __shfl_xor_sync(0xffffffffu, lr1, w);
+                    }
+                    if (g == 0) {
+                        red_m[warp * kHeads + 2 * c] = m0[r];
+                        red_m[warp * kHeads + 2 * c + 1] = m1[r];
+                        red_l[warp * kHeads + 2 * c] = lr0;
+                        red_l[warp * kHeads + 2 * c + 1] = lr1;
+                    }
+                    float* ro = red_o + warp * kHeads * D;
+                    #pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        const int d_lo = 8 * g + mt;
+                        const int d_hi = (D == 128) ? 64 + 8 * g + mt : 8 * g + 4 + mt;
+                        ro[(2 * c) * D + d_lo] = acc[r][mt][0];
+                        ro[(2 * c + 1) * D + d_lo] = acc[r][mt][1];
+                        ro[(2 * c) * D + d_hi] = acc[r][mt][2];
+                        ro[(2 * c + 1) * D + d_hi] = acc[r][mt][3];
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sync_a);
+                    if (!mbar_wait(sync_a, sync_phase, kErrWaitConsumer, p.err)) { run = false; continue; }
+                    // 256 threads: half hq (threads 128 hq ..) finishes chunk hq*CPW + r,
+                    // 16 threads per row
+                    const int t = threadIdx.x;
+                    const int hq = t >> 7;
+                    const int head = (t >> 4) & 7;
+                    constexpr int per = D / 16;
+                    const int d0 = (t & 15) * per;
+                    const int hcr = si.hc * NCI + hq * CPW + r;
+                    const long long row = ((long long)si.b * p.Hkv + si.kvh) * p.R + hcr * kHeads + head;
+                    if (head < min(kHeads, p.R - hcr * kHeads)) {
+                        const int w0 = hq * 4;
+                        float M = -INFINITY;
+                        #pragma unroll
+                        for (int i = 0; i < 4; ++i) M = fmaxf(M, red_m[(w0 + i) * kHeads + head]);
+                        float wt[4], Ltot = 0.f;
+                        #pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float mw = red_m[(w0 + i) * kHeads + head];
+                            wt[i] = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
+                            Ltot += wt[i] * red_l[(w0 + i) * kHeads + head];
+                        }
+                        // a row that saw no key in this split (a masked new token)
+                        // contributes nothing: O = 0, lse = -inf
+                        const float inv = Ltot > 0.f ? 1.f / Ltot : 0.f;
+                        const float lse2 = Ltot > 0.f ? M + __log2f(Ltot) : -INFINITY;
+                        float ov[per];
+                        #pragma unroll
+                        for (int u = 0; u < per; ++u) {
+                            float sum = 0.f;
+                            #pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                sum += wt[i] * red_o[((w0 + i) * kHeads + head) * D + d0 + u];
+                            ov[u] = sum * inv;
+                        }
+                        if (si.n_ne == 1) {
+                            store_final<D, per>(p, row, d0, ov, (t & 15) == 0, lse2);
+                        } else {
+                            const long long slot = row * p.n_slots + si.s;
+                            float* dst = p.ws_o + slot * D + d0;
+                            #pragma unroll
+                            for (int e = 0; e < per; e += 4)
+                                *reinterpret_cast<float4*>(dst + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
+                            if ((t & 15) == 0) p.ws_lse[slot] = lse2;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sync_b);
+                    if (!mbar_wait(sync_b, sync_phase, kErrWaitConsumer, p.err)) { run = false; continue; }
+                    sync_phase ^= 1u;
+                }
             }
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -707,7 +841,7 @@ cudaError_t launch_pair(const DecodeParams& p, int num_sms, cudaStream_t stream)
     cudaError_t err = cudaFuncSetAttribute(decode_split_kernel<D, NCI>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    decode_split_kernel<D, NCI><<<grid, kThreads, smem, stream>>>(p);
+    decode_split_kernel<D, NCI><<<grid, Cfg<NCI>::kThreads, smem, stream>>>(p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     // combine: programmatic dependent launch on the same stream
