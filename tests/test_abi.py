@@ -113,3 +113,14 @@ def test_workspace_size(lib):
     assert ws(0, 64, 8, 10, 128, 0) == 0
     assert ws(1, 64, 8, 10, 96, 0) == 0
     assert ws(1, 64, 8, 10, 128, 300) == 0
+
+
+def test_profile_case_driver_parses_without_gpu():
+    """The profiling driver that the ncu summaries name is importable and parses its
+    arguments on a machine without a GPU."""
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "-m", "streaming_attention_flashattention_gb300.profile_case", "--help"],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert "multitoken" in r.stdout
