@@ -104,7 +104,9 @@ int attn_prefill_kvcache(const void* q, const void* kcache, const void* vcache, 
 
 /*
  * attn_decode_workspace_size -- bytes of device workspace attn_decode_splitkv needs.
- * Holds the per-split partial results (lse_s and O_s / l_s, fp32) and a work counter.
+ * Holds the per-split partial results (lse_s and O_s / l_s, fp32), a work counter and
+ * one finished-split counter per (sequence, KV head); the counters are cleared on the
+ * call's stream at the start of every call, so the caller need not initialise anything.
  * num_splits > 0: fixed split count; 0: automatic (one split per 4096 keys).
  * Returns 0 for invalid arguments.
  */
@@ -130,9 +132,12 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int n
  * Sequence b's keys [0, kv_lens[b]) are cut into contiguous splits of C keys,
  * C = ceil(len / n) rounded up to 64 ("ADR-0060" section 2.1: contiguous blocks); each
  * split streams its chunk once for all G = Hq / Hkv query heads of a KV head (the heads
- * are stacked into one MMA operand, "ADR-0060" section 5.2), and a combine kernel merges
- * the partial (lse_s, O_s) of the splits (a sequence with one split is written directly).  kv_lens values are read on the device; values
- * outside [0, Lmax] are clamped into it.
+ * are stacked into one MMA operand, "ADR-0060" section 5.2), and the partial (lse_s, O_s)
+ * of the splits are merged ("ADR-0060" section 4; a sequence with one split is written
+ * directly).  When every work item fits in one wave of the GPU the merge is done by the
+ * CTA that finishes a group's last split (one launch, "ADR-0060" section 4.3); otherwise
+ * a combine kernel, launched dependent on the split kernel, merges.  kv_lens values are
+ * read on the device; values outside [0, Lmax] are clamped into it.
  * Requirements: d = 128 or 64, G <= 8 per launch group (larger G runs several groups),
  * all pointers 16-byte aligned.  Returns GBATTN_OK or a negative status.
  */

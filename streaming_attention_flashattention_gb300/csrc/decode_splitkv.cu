@@ -29,6 +29,12 @@
 //   into 4 key slices x 2 halves of the item's chunks; a warp's chunks sit side by side in
 //   the MMA N dimension, so each K and V^T fragment it builds feeds one MMA per chunk.
 //   NCI = 1 is the single-token case above.
+//   Single-launch mode (single-token items that all fit in one wave): no combine kernel.
+//   Each finished split counts itself into a per-(b, KV head, row chunk) counter, and the
+//   CTA that completes the group folds all of its partials into the final O and LSE -- the
+//   data-driven merge of "ADR-0060" section 4.3, without a grid-wide barrier.  For small
+//   batches this saves the second launch; for large ones the fence and atomic at every
+//   split end cost more than the launch, so they use the combine kernel.
 //   combine kernel: one thread per (b, query head, 4 output columns) folds the partials of
 //   the splits.  It is launched with programmatic dependent launch: its CTAs are
 //   scheduled while the split kernel drains and wait on the device (griddepcontrol.wait)
@@ -84,7 +90,8 @@ struct Layout {
     static constexpr int kRedMOff = kBarOff + kNumBars * 8;
     static constexpr int kRedLOff = kRedMOff + kConsumerWarps * kHeads * 4;
     static constexpr int kRedOOff = kRedLOff + kConsumerWarps * kHeads * 4;
-    static constexpr int kBytes = kRedOOff + kConsumerWarps * kHeads * D * 4;
+    static constexpr int kFusedOff = kRedOOff + kConsumerWarps * kHeads * D * 4;  // sync_c, flag
+    static constexpr int kBytes = kFusedOff + 16;
     static constexpr int kAlloc = kBytes + 1024;                // slack for 1024-B alignment
     static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
 };
@@ -173,9 +180,61 @@ __device__ __forceinline__ void store_final(const DecodeParams& p, long long row
     if (with_lse && p.lse != nullptr) p.lse[row] = lse2 * 0.69314718055994531f;
 }
 
-template <int D, int NCI>
+// Final O (columns [d0, d0 + per)) and LSE of one query row from the n_ne split partials in
+// the workspace: O = sum_s w_s O_s / sum_s w_s, w_s = 2^(lse_s - max lse) ("ADR-0060"
+// section 4), 8 partials loaded per batch; partials with lse = -inf (a row that saw no key
+// of that split) weigh nothing.
+template <int D, int per>
+__device__ __forceinline__ void fold_partials(const DecodeParams& p, long long row, int d0,
+                                              int n_ne, bool with_lse) {
+    const float* lse_s = p.ws_lse + row * p.n_slots;
+    const float* o_s = p.ws_o + row * p.n_slots * D + d0;
+    constexpr int kChunk = 8;
+    float M = -INFINITY, Ltot = 0.f, acc[per];
+    #pragma unroll
+    for (int u = 0; u < per; ++u) acc[u] = 0.f;
+    for (int s0 = 0; s0 < n_ne; s0 += kChunk) {
+        float ls[kChunk];
+        float4 ox[kChunk][per / 4];
+        #pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const bool in = s0 + i < n_ne;
+            ls[i] = in ? __ldcg(lse_s + s0 + i) : -INFINITY;
+            #pragma unroll
+            for (int e = 0; e < per / 4; ++e)
+                ox[i][e] = in ? __ldcg(reinterpret_cast<const float4*>(o_s + (long long)(s0 + i) * D) + e)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float Mc = M;
+        #pragma unroll
+        for (int i = 0; i < kChunk; ++i) Mc = fmaxf(Mc, ls[i]);
+        const float sc = (M == -INFINITY) ? 0.f : ex2_approx(M - Mc);
+        Ltot *= sc;
+        #pragma unroll
+        for (int u = 0; u < per; ++u) acc[u] *= sc;
+        #pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            if (ls[i] == -INFINITY) continue;
+            const float w = ex2_approx(ls[i] - Mc);
+            Ltot += w;
+            #pragma unroll
+            for (int e = 0; e < per / 4; ++e) {
+                acc[4 * e] += w * ox[i][e].x; acc[4 * e + 1] += w * ox[i][e].y;
+                acc[4 * e + 2] += w * ox[i][e].z; acc[4 * e + 3] += w * ox[i][e].w;
+            }
+        }
+        M = Mc;
+    }
+    const float inv = Ltot > 0.f ? 1.f / Ltot : 0.f;
+    #pragma unroll
+    for (int u = 0; u < per; ++u) acc[u] *= inv;
+    store_final<D, per>(p, row, d0, acc, with_lse, Ltot > 0.f ? M + __log2f(Ltot) : -INFINITY);
+}
+
+template <int D, int NCI, bool kFused>
 __global__ void __launch_bounds__(Cfg<NCI>::kThreads, 1)
 decode_split_kernel(const __grid_constant__ DecodeParams p) {
+    static_assert(!kFused || NCI == 1, "single-launch mode is for single-token items");
     using L = Layout<D, NCI>;
     constexpr int kConsumerWarps = Cfg<NCI>::kCW;
     constexpr int kStages = Cfg<NCI>::kStages;
@@ -193,6 +252,8 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
     float* red_m = reinterpret_cast<float*>(smem + L::kRedMOff);
     float* red_l = reinterpret_cast<float*>(smem + L::kRedLOff);
     float* red_o = reinterpret_cast<float*>(smem + L::kRedOOff);
+    uint64_t* sync_c = reinterpret_cast<uint64_t*>(smem + L::kFusedOff);   // single-launch mode
+    int* last_flag = reinterpret_cast<int*>(smem + L::kFusedOff + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -202,6 +263,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
         }
         mbar_init(sync_a, kConsumerWarps);
         mbar_init(sync_b, kConsumerWarps);
+        if constexpr (kFused) mbar_init(sync_c, kConsumerWarps);
         fence_barrier_init();
     }
     __syncthreads();
@@ -323,7 +385,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
         int lim0 = 0, lim1 = 0;
         int stage = 0;
-        uint32_t phase = 0, sync_phase = 0;
+        uint32_t phase = 0, sync_phase = 0, sync_c_phase = 0;
         const int cw = warp / W;                 // row chunk of this warp within the group
         const int kp0 = (warp % W) * kKeysPerWarp;   // this warp's first key within a stage
         int gcnt = 0;                            // rows of this warp's chunk (<= 0: none)
@@ -517,12 +579,29 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                         for (int e = 0; e < per; e += 4)
                             *reinterpret_cast<float4*>(dst + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
                         if ((t % kThrPerRow) == 0) p.ws_lse[slot] = lse2;
+                        if constexpr (kFused) __threadfence();   // partial visible before the count
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sync_b);
                 if (!mbar_wait(sync_b, sync_phase, kErrWaitConsumer, p.err)) break;
                 sync_phase ^= 1u;
+                if constexpr (kFused) {
+                    if (si.n_ne > 1) {
+                        // count this split in; the CTA that completes the group folds it
+                        if (t == 0)
+                            *last_flag = atomicAdd(p.group_cnt + ((long long)si.b * p.Hkv + si.kvh) * p.n_hg + si.hc, 1)
+                                         == si.n_ne - 1;
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(sync_c);
+                        if (!mbar_wait(sync_c, sync_c_phase, kErrWaitConsumer, p.err)) break;
+                        sync_c_phase ^= 1u;
+                        if (*last_flag && head < min(kHeads, p.R - hcr * kHeads)) {
+                            __threadfence();
+                            fold_partials<D, per>(p, row, d0, si.n_ne, (t % kThrPerRow) == 0);
+                        }
+                    }
+                }
             }
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -820,11 +899,14 @@ int decode_slots(int Lmax, int num_splits) {
     return n < 1 ? 1 : (n > kMaxSplits ? kMaxSplits : n);
 }
 
-size_t decode_counter_bytes() { return 256; }
+size_t decode_counter_bytes(int B, int Hkv, int n_hg) {
+    // the work queue counter, then one split counter per (b, KV head, chunk group)
+    return (((size_t)1 + (size_t)B * Hkv * n_hg) * 4 + 255) / 256 * 256;
+}
 
-size_t decode_workspace_bytes(int B, int Hq, int d, int n_slots) {
-    const size_t rows = (size_t)B * Hq * n_slots;
-    size_t bytes = decode_counter_bytes();               // work queue counter
+size_t decode_workspace_bytes(int B_rows, int Hq, int kv_groups, int n_hg, int d, int n_slots) {
+    const size_t rows = (size_t)B_rows * Hq * n_slots;
+    size_t bytes = decode_counter_bytes(kv_groups, 1, n_hg);   // counters
     bytes += ((rows * 4 + 255) / 256) * 256;             // lse partials
     bytes += rows * (size_t)d * 4;                       // O partials
     return bytes;
@@ -832,18 +914,19 @@ size_t decode_workspace_bytes(int B, int Hq, int d, int n_slots) {
 
 namespace {
 
-template <int D, int NCI>
+template <int D, int NCI, bool kFused = false>
 cudaError_t launch_pair(const DecodeParams& p, int num_sms, cudaStream_t stream) {
     constexpr int smem = Layout<D, NCI>::kAlloc;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     const int grid = p.n_items < num_sms ? p.n_items : num_sms;
     if (grid <= 0) return cudaSuccess;
-    cudaError_t err = cudaFuncSetAttribute(decode_split_kernel<D, NCI>,
+    cudaError_t err = cudaFuncSetAttribute(decode_split_kernel<D, NCI, kFused>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    decode_split_kernel<D, NCI><<<grid, Cfg<NCI>::kThreads, smem, stream>>>(p);
+    decode_split_kernel<D, NCI, kFused><<<grid, Cfg<NCI>::kThreads, smem, stream>>>(p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    if constexpr (kFused) return cudaSuccess;      // merged in the split kernel
     // combine: programmatic dependent launch on the same stream
     const long long threads = (long long)p.B * p.Hq * p.Tq * (D / 4);
     cudaLaunchConfig_t cfg = {};
@@ -863,8 +946,12 @@ cudaError_t launch_pair(const DecodeParams& p, int num_sms, cudaStream_t stream)
 
 cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
                                   cudaStream_t stream) {
-    cudaError_t err = cudaMemsetAsync(p.counter, 0, decode_counter_bytes(), stream);
+    cudaError_t err = cudaMemsetAsync(p.counter, 0, decode_counter_bytes(p.B, p.Hkv, p.n_hg), stream);
     if (err != cudaSuccess) return err;
+    if (p.fused) {
+        return d == 128 ? launch_pair<128, 1, true>(p, num_sms, stream)
+                        : launch_pair<64, 1, true>(p, num_sms, stream);
+    }
     if (d == 128) {
         if (p.nci == 4) return launch_pair<128, 4>(p, num_sms, stream);
         if (p.nci == 2) return launch_pair<128, 2>(p, num_sms, stream);

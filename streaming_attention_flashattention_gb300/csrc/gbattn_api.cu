@@ -125,6 +125,20 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, fl
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 
+// Query rows of a decode call per KV head (G * Tq, chunks of 8) and how work items group
+// them: one item serves up to 4 row chunks, so K/V are read once for all of them.
+struct DecodeRows {
+    int R, n_hc, nci, n_hg;
+};
+DecodeRows decode_rows(int Hq, int Hkv, int Tq) {
+    DecodeRows r;
+    r.R = (Hq / Hkv) * Tq;
+    r.n_hc = (r.R + 7) / 8;
+    r.nci = r.n_hc >= 3 ? 4 : r.n_hc;
+    r.n_hg = (r.n_hc + r.nci - 1) / r.nci;
+    return r;
+}
+
 }  // namespace
 }  // namespace gbattn
 
@@ -210,7 +224,8 @@ size_t attn_decode_multitoken_workspace_size(int B, int Hq, int Hkv, int Tq, int
     if (num_splits < 0 || num_splits > kMaxSplits) return 0;
     if (Hq % Hkv != 0) return 0;
     if ((long long)B * Hq * Tq > kIntMax) return 0;
-    return decode_workspace_bytes(B * Tq, Hq, d, decode_slots(Lmax, num_splits));
+    const DecodeRows dr = decode_rows(Hq, Hkv, Tq);
+    return decode_workspace_bytes(B * Tq, Hq, B * Hkv, dr.n_hg, d, decode_slots(Lmax, num_splits));
 }
 
 int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache,
@@ -230,15 +245,12 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
         return GBATTN_ERR_MISALIGNED;
     if ((long long)B * Hq * Tq > kIntMax / 8) return GBATTN_ERR_TOO_LARGE;
     const int n_slots = decode_slots(Lmax, num_splits);
-    const size_t need = decode_workspace_bytes(B * Tq, Hq, d, n_slots);
+    const DecodeRows dr = decode_rows(Hq, Hkv, Tq);
+    const size_t need = decode_workspace_bytes(B * Tq, Hq, B * Hkv, dr.n_hg, d, n_slots);
     if (!workspace || ws_bytes < need) return GBATTN_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GBATTN_ERR_MISALIGNED;
     const int G = Hq / Hkv;
-    const int R = G * Tq;
-    const int n_hc = (R + 7) / 8;
-    // one work item serves up to 4 row chunks, so K/V are read once for all of them
-    const int nci = n_hc >= 3 ? 4 : n_hc;
-    const int n_hg = (n_hc + nci - 1) / nci;
+    const int R = dr.R, n_hc = dr.n_hc, nci = dr.nci, n_hg = dr.n_hg;
     const long long n_items = (long long)n_slots * B * Hkv * n_hg;
     if (n_items > kIntMax || (long long)B * Hkv * Lmax > kIntMax) return GBATTN_ERR_TOO_LARGE;
     const int nsm = sm_count();
@@ -251,8 +263,9 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
         return GBATTN_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const size_t rows = (size_t)B * Hq * Tq * n_slots;
-    const size_t cnt_bytes = decode_counter_bytes();
+    const size_t cnt_bytes = decode_counter_bytes(B, Hkv, n_hg);
     p.counter = reinterpret_cast<int*>(ws);
+    p.group_cnt = p.counter + 1;
     p.ws_lse = reinterpret_cast<float*>(ws + cnt_bytes);
     p.ws_o = reinterpret_cast<float*>(ws + cnt_bytes + ((rows * 4 + 255) / 256) * 256);
     p.kv_lens = kv_lens;
@@ -267,6 +280,9 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
     p.n_slots = n_slots;
     p.fixed_splits = num_splits;
     p.n_items = (int)n_items;
+    // single launch (the group's last split merges) when every item runs in the first wave:
+    // there the combine's launch is a large part of the call
+    p.fused = (nci == 1 && n_items <= nsm) ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = device_error_word();
     if (!p.err) return GBATTN_ERR_CUDA;

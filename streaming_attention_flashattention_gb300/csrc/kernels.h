@@ -44,6 +44,7 @@ struct DecodeParams {
     __nv_bfloat16* o;     // [B, Hq, d]
     float* lse;           // [B, Hq] or null
     int* counter;         // work queue counter (zeroed before the split kernel)
+    int* group_cnt;       // [B, Hkv, n_hg] finished splits per group (single-launch mode)
     float* ws_lse;        // [B, Hq, Tq, n_slots] log2-domain partial lse
     float* ws_o;          // [B, Hq, Tq, n_slots, d] normalised partial outputs
     int B, Hq, Hkv, Lmax, G;
@@ -55,6 +56,7 @@ struct DecodeParams {
     int n_slots;          // split slots per sequence
     int fixed_splits;     // > 0 fixed count, 0 automatic
     int n_items;          // n_slots * B * Hkv * n_hg
+    int fused;            // 1: single launch, the group's last split merges (single token)
     float scale_log2;
     int* err;             // device error word of bounded waits
 };
@@ -63,8 +65,9 @@ constexpr int kAutoChunk = 4096;
 constexpr int kMaxSplits = 256;
 constexpr int kSplitAlign = 64;
 
-size_t decode_counter_bytes();
-size_t decode_workspace_bytes(int B, int Hq, int d, int n_slots);
+size_t decode_counter_bytes(int B, int Hkv, int n_hg);
+// B_rows: B * Tq; kv_groups: B * Hkv
+size_t decode_workspace_bytes(int B_rows, int Hq, int kv_groups, int n_hg, int d, int n_slots);
 int decode_slots(int Lmax, int num_splits);
 cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
                                   cudaStream_t stream);

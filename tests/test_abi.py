@@ -101,14 +101,18 @@ def test_decode_argument_validation(lib):
 
 def test_workspace_size(lib):
     ws = gb.attn_decode_workspace_size
-    # fixed splits: work counter (256) + lse partials (rounded to 256) + O partials
-    rows = 4 * 64 * 16
-    assert ws(4, 64, 8, 32768, 128, 16) == 256 + ((rows * 4 + 255) // 256) * 256 + rows * 128 * 4
+
+    def expect(B, Hq, Hkv, slots, d):
+        # counters (the work queue, then one finished-split counter per (b, KV head, chunk
+        # group); G <= 8 gives one group) rounded to 256, lse partials rounded to 256, O partials
+        rows = B * Hq * slots
+        counters = ((1 + B * Hkv) * 4 + 255) // 256 * 256
+        return counters + ((rows * 4 + 255) // 256) * 256 + rows * d * 4
+
+    assert ws(4, 64, 8, 32768, 128, 16) == expect(4, 64, 8, 16, 128)
     # automatic: one slot per 4096 keys of capacity
-    rows = 16 * 64 * 32
-    assert ws(16, 64, 8, 131072, 128, 0) == 256 + ((rows * 4 + 255) // 256) * 256 + rows * 128 * 4
-    rows = 2 * 32 * 1
-    assert ws(2, 32, 2, 100, 64, 1) == 256 + ((rows * 4 + 255) // 256) * 256 + rows * 64 * 4
+    assert ws(16, 64, 8, 131072, 128, 0) == expect(16, 64, 8, 32, 128)
+    assert ws(2, 32, 2, 100, 64, 1) == expect(2, 32, 2, 1, 64)
     assert ws(1, 1, 1, 1, 128, 0) > 0
     assert ws(0, 64, 8, 10, 128, 0) == 0
     assert ws(1, 64, 8, 10, 96, 0) == 0
