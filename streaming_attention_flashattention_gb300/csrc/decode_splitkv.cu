@@ -45,6 +45,7 @@
 //   warp-level tensor path; the streaming design is what sets the speed.
 #include "common.cuh"
 #include "kernels.h"
+#include "decode_splits.cuh"
 
 namespace gbattn {
 
@@ -131,31 +132,6 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
     return y;
-}
-
-// Split bounds of the reading "contiguous blocks": n splits of C keys,
-// C = ceil(len / n) rounded up to kSplitAlign.
-__device__ __forceinline__ void split_range(int len, int n, int s, int& t0, int& t1) {
-    int c = (len + n - 1) / n;
-    c = ((c + kSplitAlign - 1) / kSplitAlign) * kSplitAlign;
-    if (c == 0) c = kSplitAlign;
-    const long long a = (long long)s * c;
-    t0 = (int)min((long long)len, a);
-    t1 = (int)min((long long)len, a + c);
-}
-
-// Number of non-empty splits: the first ceil(len / C) of them.
-__device__ __forceinline__ int nonempty_splits(int len, int n) {
-    if (len <= 0) return 0;
-    int c = (len + n - 1) / n;
-    c = ((c + kSplitAlign - 1) / kSplitAlign) * kSplitAlign;
-    return (len + c - 1) / c;
-}
-
-__device__ __forceinline__ int splits_for(int len, int fixed_splits) {
-    if (fixed_splits > 0) return fixed_splits;
-    int n = (len + kAutoChunk - 1) / kAutoChunk;
-    return max(1, min(kMaxSplits, n));
 }
 
 // Final output of one query row: `per` consecutive columns of O (bf16) starting at
@@ -942,7 +918,27 @@ cudaError_t launch_pair(const DecodeParams& p, int num_sms, cudaStream_t stream)
     return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, p);
 }
 
+template <int D>
+cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
+    const long long threads = (long long)p.B * p.Hq * p.Tq * (D / 4);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((threads + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, p);
+}
+
 }  // namespace
+
+cudaError_t launch_decode_combine(const DecodeParams& p, int d, cudaStream_t stream) {
+    return d == 128 ? launch_combine<128>(p, stream) : launch_combine<64>(p, stream);
+}
 
 cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
                                   cudaStream_t stream) {

@@ -286,7 +286,35 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = device_error_word();
     if (!p.err) return GBATTN_ERR_CUDA;
-    cudaError_t e = launch_decode_splitkv(p, d, nsm, static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (Tq > 1 && R >= 16) {
+        // tcgen05 path: a KV head's G * Tq rows as the M = 128 operand, each K/V tile read
+        // once per 128 rows; the combine folds the partials as for the split kernel
+        DecodeTcParams tp{};
+        if (!make_map_bf16_3d(&tp.tmap_q, q, d, (uint64_t)B * Hq * Tq, 1, 128) ||
+            !make_map_bf16_3d(&tp.tmap_k, kcache, d, Lmax, (uint64_t)B * Hkv, 128) ||
+            !make_map_bf16_3d(&tp.tmap_v, vcache, d, Lmax, (uint64_t)B * Hkv, 128))
+            return GBATTN_ERR_CUDA;
+        tp.kv_lens = kv_lens;
+        tp.o = p.o;
+        tp.lse = lse;
+        tp.ws_lse = p.ws_lse;
+        tp.ws_o = p.ws_o;
+        tp.B = B; tp.Hq = Hq; tp.Hkv = Hkv; tp.Lmax = Lmax; tp.Tq = Tq;
+        tp.R = R;
+        tp.n_rt = (R + 127) / 128;
+        tp.n_slots = n_slots;
+        tp.fixed_splits = num_splits;
+        const long long tc_items = (long long)n_slots * B * Hkv * tp.n_rt;
+        if (tc_items > kIntMax) return GBATTN_ERR_TOO_LARGE;
+        tp.n_items = (int)tc_items;
+        tp.scale_log2 = p.scale_log2;
+        tp.err = p.err;
+        cudaError_t e = launch_decode_multitoken_tc(tp, d, st);
+        if (e == cudaSuccess) e = launch_decode_combine(p, d, st);
+        return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+    }
+    cudaError_t e = launch_decode_splitkv(p, d, nsm, st);
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 

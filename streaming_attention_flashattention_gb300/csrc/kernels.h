@@ -71,5 +71,30 @@ size_t decode_workspace_bytes(int B_rows, int Hq, int kv_groups, int n_hg, int d
 int decode_slots(int Lmax, int num_splits);
 cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
                                   cudaStream_t stream);
+// The log-sum-exp combine of the partials in the workspace, launched dependent on the
+// kernel before it on `stream`.
+cudaError_t launch_decode_combine(const DecodeParams& p, int d, cudaStream_t stream);
+
+// ---- bf16 tcgen05 multi-token decode (decode_tcgen05.cu) ----------------------------------
+// Work items (b, KV head, split, 128-row tile of the R = G * Tq rows); partials go to the
+// same workspace layout as the split kernel's and are folded by launch_decode_combine.
+struct DecodeTcParams {
+    CUtensorMap tmap_q;   // 3-D (d, B*Hq*Tq, 1), box (64, 128, 1), 128B swizzle
+    CUtensorMap tmap_k;   // 3-D (d, Lmax, B*Hkv), box (64, 128, 1), 128B swizzle
+    CUtensorMap tmap_v;
+    const int* kv_lens;
+    __nv_bfloat16* o;     // [B, Hq, Tq, d]
+    float* lse;           // [B, Hq, Tq] or null
+    float* ws_lse;        // [B, Hq, Tq, n_slots] log2-domain partial lse
+    float* ws_o;          // [B, Hq, Tq, n_slots, d]
+    int B, Hq, Hkv, Lmax, Tq;
+    int R;                // query rows per KV head: G * Tq
+    int n_rt;             // 128-row tiles per KV head: ceil(R / 128)
+    int n_slots, fixed_splits;
+    int n_items;          // n_slots * B * Hkv * n_rt
+    float scale_log2;
+    int* err;
+};
+cudaError_t launch_decode_multitoken_tc(const DecodeTcParams& p, int d, cudaStream_t stream);
 
 }  // namespace gbattn

@@ -54,6 +54,8 @@ def run(B, Hq, Hkv, Tq, Lmax, d, lens, ns, seed=5):
     (2, 4, 2, 5, 300, 128, [2, 300], 2),              # len < Tq: rows with no visible key
     (2, 16, 2, 3, 1500, 128, [1500, 700], 0),         # 3 row chunks: a group of 4 with one empty
     (1, 8, 2, 10, 900, 128, [900], 2),                # 5 row chunks: a second group of one chunk
+    (2, 16, 2, 20, 1300, 128, [1300, 555], 3),        # 160 rows per KV head: two 128-row tiles
+    (1, 32, 4, 6, 700, 64, [700], 0),                 # 48 rows, d = 64, automatic splits
 ])
 def test_multitoken_decode_shapes(B, Hq, Hkv, Tq, Lmax, d, lens, ns):
     run(B, Hq, Hkv, Tq, Lmax, d, lens, ns)
