@@ -136,7 +136,9 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int n
  * of the splits are merged ("ADR-0060" section 4; a sequence with one split is written
  * directly).  When every work item fits in one wave of the GPU the merge is done by the
  * CTA that finishes a group's last split (one launch, "ADR-0060" section 4.3); otherwise
- * a combine kernel, launched dependent on the split kernel, merges.  kv_lens values are
+ * a combine kernel, launched dependent on the split kernel, merges.  With G >= 16 query
+ * heads per KV head the heads form the M = 128 operand of a tcgen05 kernel instead of
+ * the N dimension of warp-level MMAs.  kv_lens values are
  * read on the device; values outside [0, Lmax] are clamped into it.
  * Requirements: d = 128 or 64, G <= 8 per launch group (larger G runs several groups),
  * all pointers 16-byte aligned.  Returns GBATTN_OK or a negative status.
@@ -150,7 +152,9 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
  * attn_decode_multitoken -- decode of Tq >= 1 new tokens per sequence at once (for
  * example speculative decoding), split-KV with the same log-sum-exp merge.  The G * Tq
  * query rows of a KV head are stacked into the MMA operand ("ADR-0060" section 0.5:
- * the group's Q [G, T_q, d] folds to [G * T_q, d]), 8 rows per pass over a K/V tile.
+ * the group's Q [G, T_q, d] folds to [G * T_q, d]).  Up to 15 rows run 8 at a time on
+ * warp-level MMAs; 16 or more run as the M = 128 operand of tcgen05 MMAs, each K/V tile
+ * read once per 128 rows.
  *
  *   q       [B, Hq, Tq, d]      device, bf16    the new tokens' post-RoPE queries
  *   kcache  [B, Hkv, Lmax, d]   device, bf16    key cache; the new tokens' keys are

@@ -948,14 +948,11 @@ cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
         return d == 128 ? launch_pair<128, 1, true>(p, num_sms, stream)
                         : launch_pair<64, 1, true>(p, num_sms, stream);
     }
-    if (d == 128) {
-        if (p.nci == 4) return launch_pair<128, 4>(p, num_sms, stream);
-        if (p.nci == 2) return launch_pair<128, 2>(p, num_sms, stream);
-        return launch_pair<128, 1>(p, num_sms, stream);
-    }
-    if (p.nci == 4) return launch_pair<64, 4>(p, num_sms, stream);
-    if (p.nci == 2) return launch_pair<64, 2>(p, num_sms, stream);
-    return launch_pair<64, 1>(p, num_sms, stream);
+    // (16 or more rows per KV head run on the tcgen05 kernel, so NCI <= 2 here)
+    if (p.nci > 2) return cudaErrorInvalidValue;
+    if (d == 128)
+        return p.nci == 2 ? launch_pair<128, 2>(p, num_sms, stream) : launch_pair<128, 1>(p, num_sms, stream);
+    return p.nci == 2 ? launch_pair<64, 2>(p, num_sms, stream) : launch_pair<64, 1>(p, num_sms, stream);
 }
 
 }  // namespace gbattn

@@ -287,9 +287,10 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
     p.err = device_error_word();
     if (!p.err) return GBATTN_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (Tq > 1 && R >= 16) {
-        // tcgen05 path: a KV head's G * Tq rows as the M = 128 operand, each K/V tile read
-        // once per 128 rows; the combine folds the partials as for the split kernel
+    if (R >= 16) {
+        // tcgen05 path (16 or more query rows per KV head: several new tokens, or G >= 16):
+        // the KV head's rows as the M = 128 operand, each K/V tile read once per 128 rows;
+        // the combine folds the partials as for the split kernel
         DecodeTcParams tp{};
         if (!make_map_bf16_3d(&tp.tmap_q, q, d, (uint64_t)B * Hq * Tq, 1, 128) ||
             !make_map_bf16_3d(&tp.tmap_k, kcache, d, Lmax, (uint64_t)B * Hkv, 128) ||
