@@ -56,6 +56,8 @@ def run(B, Hq, Hkv, Tq, Lmax, d, lens, ns, seed=5):
     (1, 8, 2, 10, 900, 128, [900], 2),                # 5 row chunks: a second group of one chunk
     (2, 16, 2, 20, 1300, 128, [1300, 555], 3),        # 160 rows per KV head: two 128-row tiles
     (1, 32, 4, 6, 700, 64, [700], 0),                 # 48 rows, d = 64, automatic splits
+    (2, 16, 2, 4, 300, 128, [2, 300], 2),             # tcgen05 path with len < Tq: rows see no key
+    (3, 16, 2, 2, 500, 128, [0, 500, 17], 4),         # tcgen05 path: an empty sequence, short ones
 ])
 def test_multitoken_decode_shapes(B, Hq, Hkv, Tq, Lmax, d, lens, ns):
     run(B, Hq, Hkv, Tq, Lmax, d, lens, ns)
