@@ -82,6 +82,37 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              void* stream);
 
 /*
+ * attn_fwd_host_workspace_size -- device bytes attn_fwd_host needs for these sizes on the
+ * current device (two staging buffer sets); 0 for invalid sizes.
+ */
+size_t attn_fwd_host_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int d, int dtype);
+
+/*
+ * attn_fwd_host -- attn_fwd on HOST buffers: the same operation and kernel, with the inputs
+ * copied to the device and the outputs back as part of the call.  Not in the pages (their
+ * accelerator has no host link); a library-level addition for callers whose tensors live
+ * in host memory.
+ *
+ *   q, k, v, o, lse      HOST pointers, layouts as for attn_fwd (lse may be NULL); page-locked
+ *                        memory gives asynchronous copies, pageable memory works but the
+ *                        copies then wait on the host
+ *   workspace, ws_bytes  DEVICE scratch of at least attn_fwd_host_workspace_size(...) bytes,
+ *                        owned by the caller
+ *   stream               the call is ordered after the earlier work on `stream`, and work
+ *                        queued on `stream` afterwards runs after its last copy has landed
+ *                        in host memory (synchronise on it before reading o / lse)
+ *
+ * The (batch, KV head) groups are cut into up to 4 chunks, each large enough for the
+ * kernel's pair mode, and staged through two device buffer sets on internal copy streams:
+ * chunk i+1 is copied in and chunk i-1 copied out while chunk i computes.  Calls on one
+ * device are serialised on the host; calls sharing a workspace must be ordered on one
+ * stream.  Requirements and status codes as attn_fwd, plus GBATTN_ERR_WORKSPACE.
+ */
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                  int Hq, int Hkv, int Sq, int Skv, int d, float scale, int causal, int dtype,
+                  void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * attn_prefill_kvcache -- chunked prefill against a KV cache: a chunk of Sq new queries
  * attends to the first Skv rows of a cache of capacity Lmax (the chunk's own keys are the
  * last Sq of those rows; "ADR-0060" section 0.5.2: T_q = the chunk width for a

@@ -39,6 +39,8 @@ _F = ctypes.c_float
 _SZ = ctypes.c_size_t
 EXPORTS = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "attn_fwd_host_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "attn_prefill_kvcache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "attn_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
@@ -139,6 +141,72 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool,
                       B, Hq, Hkv, Sq, Skv, d, float(scale), 1 if causal else 0, dtype,
                       _stream_ptr(stream))
     _check("attn_fwd", st)
+    return out, lse
+
+
+def _host_tensor(name: str, t: torch.Tensor, dtypes):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+_host_ws = {}
+
+
+def attn_fwd_host_workspace_size(B: int, Hq: int, Hkv: int, Sq: int, Skv: int, d: int,
+                                 dtype: int = GBATTN_BF16) -> int:
+    return int(load_library().attn_fwd_host_workspace_size(B, Hq, Hkv, Sq, Skv, d, dtype))
+
+
+def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool,
+                  scale: float | None = None, out: torch.Tensor | None = None,
+                  lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                  stream=None):
+    """attn_fwd on host (CPU) tensors: inputs copied in and outputs copied back by the call,
+    overlapped with the kernel chunk by chunk.  Pinned (page-locked) tensors make the copies
+    asynchronous; out / lse are allocated pinned when not given.  Returns (out, lse) on the
+    host; they are complete once `stream` (default: the current stream) has been
+    synchronised.  The device workspace is allocated and cached per size when not given.
+    """
+    lib = load_library()
+    dts = (torch.bfloat16, torch.float32)
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _host_tensor(n, t, dts)
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share a dtype")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("expected q [B,Hq,Sq,d] and k, v [B,Hkv,Skv,d]")
+    B, Hq, Sq, d = q.shape
+    _, Hkv, Skv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    else:
+        _host_tensor("out", out, (q.dtype,))
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32).pin_memory()
+    else:
+        _host_tensor("lse", lse, (torch.float32,))
+    dtype = GBATTN_BF16 if q.dtype == torch.bfloat16 else GBATTN_FP32
+    need = attn_fwd_host_workspace_size(B, Hq, Hkv, Sq, Skv, d, dtype)
+    if need == 0:
+        raise GbAttnError("attn_fwd_host", GBATTN_ERR_INVALID_ARG)
+    if workspace is None:
+        key = (torch.cuda.current_device(), need)
+        workspace = _host_ws.get(key)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+            _host_ws[key] = workspace
+    st = lib.attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                           B, Hq, Hkv, Sq, Skv, d, float(scale), 1 if causal else 0, dtype,
+                           workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
+    _check("attn_fwd_host", st)
     return out, lse
 
 

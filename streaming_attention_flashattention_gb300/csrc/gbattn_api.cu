@@ -6,7 +6,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -125,6 +127,75 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, fl
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 
+// ---- host-buffer prefill: chunked copies in and out overlapped with the kernel ----------
+// The work is cut into chunks of consecutive (batch, KV head) groups -- each a contiguous
+// slab of Q/O ([G, Sq, d]), K and V ([Skv, d]) and LSE ([G, Sq]) -- staged through two
+// device buffer sets.  Chunk i's copy in waits for chunk i-2's copy out (the same buffers),
+// its kernel for its copy in, its copy out for its kernel, so chunk i+1 comes in and chunk
+// i-1 goes out while chunk i computes.
+struct HostPlan {
+    int cg;                  // groups per chunk
+    int n_chunks;
+    int n_bufs;              // buffer sets (2 when there are several chunks)
+    size_t q_off, k_off, v_off, o_off, l_off, set_bytes;   // one buffer set
+};
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+HostPlan host_plan(int B, int Hq, int Hkv, int Sq, int Skv, int d, size_t esize, int nsm) {
+    HostPlan h{};
+    const int G = Hq / Hkv;
+    const long long ng = (long long)B * Hkv;
+    const long long pairs_per_group = ((long long)((Sq + 127) / 128) * G + 1) / 2;
+    // the smallest chunk that keeps the kernel's pair mode (>= 2 Q-tile pairs per SM), and
+    // no more than 4 chunks
+    long long cg = (2LL * nsm + pairs_per_group - 1) / pairs_per_group;
+    cg = std::max(cg, (ng + 3) / 4);
+    cg = std::min(std::max(cg, 1LL), ng);
+    h.cg = (int)cg;
+    h.n_chunks = (int)((ng + cg - 1) / cg);
+    h.n_bufs = h.n_chunks > 1 ? 2 : 1;
+    const size_t qb = (size_t)cg * G * Sq * d * esize;
+    const size_t kb = (size_t)cg * Skv * d * esize;
+    const size_t lb = (size_t)cg * G * Sq * 4;
+    h.q_off = 0;
+    h.k_off = align256(qb);
+    h.v_off = h.k_off + align256(kb);
+    h.o_off = h.v_off + align256(kb);
+    h.l_off = h.o_off + align256(qb);
+    h.set_bytes = h.l_off + align256(lb);
+    return h;
+}
+
+// Copy streams and events of the current device, created on first use.
+struct HostPipe {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t entry = nullptr, done = nullptr;
+    cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_comp[2] = {nullptr, nullptr}, ev_out[2] = {nullptr, nullptr};
+    std::mutex mu;           // one host-buffer call at a time per device
+};
+
+HostPipe* host_pipe() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    static HostPipe pipes[64];
+    static std::once_flag once[64];
+    bool ok = true;
+    std::call_once(once[dev], [&] {
+        HostPipe& h = pipes[dev];
+        ok = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) == cudaSuccess &&
+             cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) == cudaSuccess &&
+             cudaEventCreateWithFlags(&h.entry, cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&h.done, cudaEventDisableTiming) == cudaSuccess;
+        for (int i = 0; i < 2 && ok; ++i)
+            ok = cudaEventCreateWithFlags(&h.ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&h.ev_comp[i], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&h.ev_out[i], cudaEventDisableTiming) == cudaSuccess;
+    });
+    HostPipe& h = pipes[dev];
+    return (h.in && h.out && h.done && h.ev_out[1]) ? &h : nullptr;
+}
+
 // Query rows of a decode call per KV head (G * Tq, chunks of 8) and how work items group
 // them: one item serves up to 4 row chunks, so K/V are read once for all of them.
 struct DecodeRows {
@@ -192,6 +263,87 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     }
 
     return launch_prefill_bf16(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, Skv, d, scale, causal, st);
+}
+
+size_t attn_fwd_host_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int d, int dtype) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || Hq % Hkv != 0) return 0;
+    if ((d != 64 && d != 128) || (dtype != GBATTN_BF16 && dtype != GBATTN_FP32)) return 0;
+    const int nsm = sm_count();
+    if (nsm <= 0) return 0;
+    const HostPlan h = host_plan(B, Hq, Hkv, Sq, Skv, d, dtype == GBATTN_BF16 ? 2 : 4, nsm);
+    return h.set_bytes * h.n_bufs;
+}
+
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                  int Hq, int Hkv, int Sq, int Skv, int d, float scale, int causal, int dtype,
+                  void* workspace, size_t ws_bytes, void* stream) {
+    if (!q || !k || !v || !o) return GBATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || d <= 0)
+        return GBATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return GBATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || scale != scale) return GBATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return GBATTN_ERR_INVALID_ARG;
+    if (dtype != GBATTN_BF16 && dtype != GBATTN_FP32) return GBATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return GBATTN_ERR_UNSUPPORTED;
+    if (causal && Sq > Skv) return GBATTN_ERR_UNSUPPORTED;
+    if ((long long)B * Hq > 65535LL * 65535LL || (long long)B * Hq * Sq > kIntMax ||
+        (long long)B * Hkv * Skv > kIntMax)
+        return GBATTN_ERR_TOO_LARGE;
+    const size_t need = attn_fwd_host_workspace_size(B, Hq, Hkv, Sq, Skv, d, dtype);
+    if (need == 0) return GBATTN_ERR_CUDA;
+    if (!workspace || ws_bytes < need) return GBATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return GBATTN_ERR_MISALIGNED;
+    HostPipe* hp = host_pipe();
+    if (!hp) return GBATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(hp->mu);
+
+    const size_t es = dtype == GBATTN_BF16 ? 2 : 4;
+    const HostPlan h = host_plan(B, Hq, Hkv, Sq, Skv, d, es, sm_count());
+    const int G = Hq / Hkv;
+    const int ng = B * Hkv;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const char* qh = static_cast<const char*>(q);
+    const char* kh = static_cast<const char*>(k);
+    const char* vh = static_cast<const char*>(v);
+    char* oh = static_cast<char*>(o);
+    char* lh = reinterpret_cast<char*>(lse);
+    char* ws = static_cast<char*>(workspace);
+    const size_t qg = (size_t)G * Sq * d * es, kg = (size_t)Skv * d * es, lg = (size_t)G * Sq * 4;
+    auto chk = [](cudaError_t e) { return e == cudaSuccess; };
+    bool ok = chk(cudaEventRecord(hp->entry, st));   // the caller's earlier work comes first
+    for (int i = 0; ok && i < h.n_chunks; ++i) {
+        const int bset = i % h.n_bufs;
+        const int g0 = i * h.cg, gn = std::min(h.cg, ng - g0);
+        char* base = ws + (size_t)bset * h.set_bytes;
+        ok = chk(cudaStreamWaitEvent(hp->in, i >= h.n_bufs ? hp->ev_out[bset] : hp->entry, 0)) &&
+             chk(cudaMemcpyAsync(base + h.q_off, qh + g0 * qg, gn * qg, cudaMemcpyHostToDevice, hp->in)) &&
+             chk(cudaMemcpyAsync(base + h.k_off, kh + g0 * kg, gn * kg, cudaMemcpyHostToDevice, hp->in)) &&
+             chk(cudaMemcpyAsync(base + h.v_off, vh + g0 * kg, gn * kg, cudaMemcpyHostToDevice, hp->in)) &&
+             chk(cudaEventRecord(hp->ev_in[bset], hp->in)) &&
+             chk(cudaStreamWaitEvent(st, hp->ev_in[bset], 0));
+        if (!ok) break;
+        float* lse_d = lh ? reinterpret_cast<float*>(base + h.l_off) : nullptr;
+        int rc;
+        if (dtype == GBATTN_FP32) {
+            rc = launch_attn_fwd_f32(reinterpret_cast<const float*>(base + h.q_off),
+                                     reinterpret_cast<const float*>(base + h.k_off),
+                                     reinterpret_cast<const float*>(base + h.v_off),
+                                     reinterpret_cast<float*>(base + h.o_off), lse_d, 1, gn * G, gn,
+                                     Sq, Skv, d, scale, causal, st) == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+        } else {
+            rc = launch_prefill_bf16(base + h.q_off, base + h.k_off, base + h.v_off, base + h.o_off,
+                                     lse_d, 1, gn * G, gn, Sq, Skv, Skv, d, scale, causal, st);
+        }
+        if (rc != GBATTN_OK) return rc;
+        ok = chk(cudaEventRecord(hp->ev_comp[bset], st)) &&
+             chk(cudaStreamWaitEvent(hp->out, hp->ev_comp[bset], 0)) &&
+             chk(cudaMemcpyAsync(oh + g0 * qg, base + h.o_off, gn * qg, cudaMemcpyDeviceToHost, hp->out)) &&
+             (!lh || chk(cudaMemcpyAsync(lh + g0 * lg, base + h.l_off, gn * lg, cudaMemcpyDeviceToHost, hp->out))) &&
+             chk(cudaEventRecord(hp->ev_out[bset], hp->out));
+    }
+    // the caller's stream completes after the last copy out
+    ok = ok && chk(cudaEventRecord(hp->done, hp->out)) && chk(cudaStreamWaitEvent(st, hp->done, 0));
+    return ok ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 
 int attn_prefill_kvcache(const void* q, const void* kcache, const void* vcache, void* o,

@@ -128,3 +128,11 @@ def test_profile_case_driver_parses_without_gpu():
                        capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     assert "multitoken" in r.stdout
+
+
+def test_host_workspace_size_rejects_invalid_sizes(lib):
+    f = gb.attn_fwd_host_workspace_size
+    assert f(0, 8, 2, 128, 128, 128) == 0
+    assert f(1, 8, 3, 128, 128, 128) == 0          # Hq % Hkv != 0
+    assert f(1, 8, 2, 128, 128, 96) == 0           # d not 64 / 128
+    assert f(1, 8, 2, 128, 128, 128, 7) == 0       # dtype
