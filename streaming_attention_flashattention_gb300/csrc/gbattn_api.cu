@@ -461,9 +461,10 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
         const long long tc_items = (long long)n_slots * B * Hkv * tp.n_rt;
         if (tc_items > kIntMax) return GBATTN_ERR_TOO_LARGE;
         tp.n_items = (int)tc_items;
+        tp.counter = p.counter;
         tp.scale_log2 = p.scale_log2;
         tp.err = p.err;
-        cudaError_t e = launch_decode_multitoken_tc(tp, d, st);
+        cudaError_t e = launch_decode_multitoken_tc(tp, d, nsm, st);
         if (e == cudaSuccess) e = launch_decode_combine(p, d, st);
         return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
     }

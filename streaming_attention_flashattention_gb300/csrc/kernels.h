@@ -92,9 +92,11 @@ struct DecodeTcParams {
     int n_rt;             // 128-row tiles per KV head: ceil(R / 128)
     int n_slots, fixed_splits;
     int n_items;          // n_slots * B * Hkv * n_rt
+    int* counter;         // work queue counter (zeroed before the kernel)
     float scale_log2;
     int* err;
 };
-cudaError_t launch_decode_multitoken_tc(const DecodeTcParams& p, int d, cudaStream_t stream);
+cudaError_t launch_decode_multitoken_tc(const DecodeTcParams& p, int d, int nsm,
+                                        cudaStream_t stream);
 
 }  // namespace gbattn

@@ -84,3 +84,40 @@ def test_each_token_equals_its_own_single_token_decode():
         torch.cuda.synchronize()
         assert (o[:, :, t:t + 1].float() - o_t.float()).abs().max().item() <= 2e-2
         assert (lse[:, :, t] - l_t).abs().max().item() <= 1e-3
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Tq,Lmax,d,lens,ns", [
+    # hundreds of work items over the persistent CTAs: each takes several, of 1 to 4 key
+    # tiles, with a ragged last tile (NaN past len) in most of them
+    (4, 16, 8, 8, 8192, 128, [8192, 5000, 1500, 777], 16),
+    (4, 32, 8, 4, 6000, 64, [6000, 2500, 128, 4000], 32),
+    (6, 16, 2, 16, 3000, 128, [3000, 0, 1, 2999, 130, 1024], 24),
+])
+def test_multitoken_decode_many_items_per_cta(B, Hq, Hkv, Tq, Lmax, d, lens, ns):
+    run(B, Hq, Hkv, Tq, Lmax, d, lens, ns, seed=17)
+
+
+def test_multitoken_workload7_llama70b_sampled():
+    # the 4-token Llama3-70B decode at full size (512 work items), sampled rows
+    w = wl.EXTRA_WORKLOADS[7]
+    q, kc, vc, kl = wl.multitoken_inputs(w)
+    o, lse = gb.attn_decode_multitoken(q.cuda(), kc.cuda(), vc.cuda(), kl.cuda(),
+                                       num_splits=w.num_splits, scale=w.scale)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(7)
+    n = w.B * w.Hq * w.Sq
+    rows = np.unique(np.concatenate([rng.integers(0, n, 96), [0, n - 1]]))
+    o_ref, lse_ref = oracle.attention(wl.to_oracle(q), wl.to_oracle(kc), wl.to_oracle(vc),
+                                      w.scale, True, kv_len=kl.numpy(), rows=rows)
+    compare(o.float().cpu().numpy().reshape(-1, w.d)[rows], lse.cpu().numpy().reshape(-1)[rows],
+            o_ref, lse_ref, "bf16", w.name)
+
+
+def test_multitoken_deterministic_repeat():
+    # which CTA takes which item varies from call to call; the result may not
+    q, kc, vc, kl = make(4, 64, 8, 4, 7000, 128, [7000, 6500, 3000, 7000], seed=23)
+    args = (q.cuda(), kc.cuda(), vc.cuda(), kl.cuda())
+    o1, l1 = gb.attn_decode_multitoken(*args, num_splits=16)
+    o2, l2 = gb.attn_decode_multitoken(*args, num_splits=16)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
