@@ -138,7 +138,9 @@ int attn_prefill_kvcache(const void* q, const void* kcache, const void* vcache, 
  * Holds the per-split partial results (lse_s and O_s / l_s, fp32), a work counter and
  * one finished-split counter per (sequence, KV head); the counters are cleared on the
  * call's stream at the start of every call, so the caller need not initialise anything.
- * num_splits > 0: fixed split count; 0: automatic (one split per 4096 keys).
+ * num_splits > 0: fixed split count; 0: automatic: one split per 4096 keys of a sequence,
+ * raised for calls with few (sequence, KV head) groups to the most splits that still fit
+ * one wave of 152 work items (the SM count of a GB300), but never below 256 keys per split.
  * Returns 0 for invalid arguments.
  */
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int num_splits);
@@ -154,7 +156,8 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int n
  *   o       [B, Hq, 1, d]       device, bf16    output (written)
  *   lse     [B, Hq]             device, fp32    log-sum-exp (written); may be NULL
  *   num_splits                                  > 0 fixed splits per sequence (<= 256),
- *                                               0 = automatic per sequence length
+ *                                               0 = automatic per sequence length and
+ *                                               call size (attn_decode_workspace_size)
  *   workspace, ws_bytes                         device scratch of at least
  *                                               attn_decode_workspace_size(...) bytes,
  *                                               owned by the caller; calls that share a

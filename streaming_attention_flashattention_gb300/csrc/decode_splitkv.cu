@@ -268,7 +268,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 const int b = rem;
                 int len = __ldg(&p.kv_lens[b]);
                 len = max(0, min(len, p.Lmax));
-                const int nb = splits_for(len, p.fixed_splits);
+                const int nb = splits_for(len, p.fixed_splits, p.auto_floor);
                 if (s >= nb) continue;
                 const int n_ne = nonempty_splits(len, nb);
                 // rows of this item: the KV head's G * Tq query rows (head-major, token
@@ -826,7 +826,7 @@ decode_combine_kernel(const __grid_constant__ DecodeParams p) {
     const int b = (int)(row / ((long long)p.Hq * p.Tq));
     int len = __ldg(&p.kv_lens[b]);
     len = max(0, min(len, p.Lmax));
-    const int n_ne = nonempty_splits(len, splits_for(len, p.fixed_splits));
+    const int n_ne = nonempty_splits(len, splits_for(len, p.fixed_splits, p.auto_floor));
     if (n_ne <= 1) return;      // written directly by the split kernel
     const float* lse_s = p.ws_lse + row * p.n_slots;
     const float* o_s = p.ws_o + row * p.n_slots * D + cg * 4;
@@ -869,10 +869,8 @@ decode_combine_kernel(const __grid_constant__ DecodeParams p) {
 
 }  // namespace
 
-int decode_slots(int Lmax, int num_splits) {
-    if (num_splits > 0) return num_splits;
-    int n = (Lmax + kAutoChunk - 1) / kAutoChunk;
-    return n < 1 ? 1 : (n > kMaxSplits ? kMaxSplits : n);
+int decode_slots(int Lmax, int num_splits, int auto_floor) {
+    return splits_for(Lmax, num_splits, auto_floor);
 }
 
 size_t decode_counter_bytes(int B, int Hkv, int n_hg) {

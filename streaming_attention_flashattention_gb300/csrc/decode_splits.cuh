@@ -2,7 +2,8 @@
 //
 // "ADR-0060: AHBM GQA Fused Attention Kernel (Llama3-70B)", section 2.1: each split is one
 // contiguous block of the cache.  n splits of C keys, C = ceil(len / n) rounded up to
-// kSplitAlign; automatic mode takes one split per kAutoChunk keys.
+// kSplitAlign.  The automatic mode takes one split per kAutoChunk keys, or more when the
+// call has few (sequence, KV head) groups (splits_for).
 #pragma once
 #include "kernels.h"
 
@@ -27,10 +28,17 @@ __device__ __forceinline__ int nonempty_splits(int len, int n) {
     return (len + c - 1) / c;
 }
 
-__device__ __forceinline__ int splits_for(int len, int fixed_splits) {
+// Splits of a sequence of len keys.  Automatic mode: one per kAutoChunk keys, raised to
+// auto_floor (the count that gives the call about kAutoItems work items, chosen on the host)
+// as long as each split keeps kAutoMinKeys keys.  Non-decreasing in len, so the host sizes
+// the workspace with len = Lmax.
+__host__ __device__ __forceinline__ int splits_for(int len, int fixed_splits, int auto_floor) {
     if (fixed_splits > 0) return fixed_splits;
-    int n = (len + kAutoChunk - 1) / kAutoChunk;
-    return max(1, min(kMaxSplits, n));
+    const int by_len = (len + kAutoChunk - 1) / kAutoChunk;
+    const int by_keys = (len + kAutoMinKeys - 1) / kAutoMinKeys;
+    const int by_fill = auto_floor < by_keys ? auto_floor : by_keys;
+    const int n = by_len > by_fill ? by_len : by_fill;
+    return n < 1 ? 1 : (n > kMaxSplits ? kMaxSplits : n);
 }
 
 

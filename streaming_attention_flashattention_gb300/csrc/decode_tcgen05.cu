@@ -160,7 +160,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
             const int b = rem / p.Hkv;
             int len = __ldg(&p.kv_lens[b]);
             len = max(0, min(len, p.Lmax));
-            const int nb = splits_for(len, p.fixed_splits);
+            const int nb = splits_for(len, p.fixed_splits, p.auto_floor);
             const int n_ne = nonempty_splits(len, nb);
             const long long row0 = ((long long)b * p.Hkv + kvh) * p.R + (long long)rt * kRowsT;
             if (s >= n_ne) {

@@ -210,6 +210,16 @@ DecodeRows decode_rows(int Hq, int Hkv, int Tq) {
     return r;
 }
 
+// Automatic split mode: the most splits per sequence that keep the call within one wave of
+// kAutoItems work items.  A work item is one split of one (sequence, KV head) and one row
+// group: a 128-row tile on the tensor-core path (R >= 16), a chunk group on the warp-level
+// path.  Never below one.
+int auto_floor(int B, int Hkv, const DecodeRows& dr) {
+    const long long per_split = (long long)B * Hkv * (dr.R >= 16 ? (dr.R + 127) / 128 : dr.n_hg);
+    const long long f = kAutoItems / per_split;
+    return (int)(f < 1 ? 1 : (f > kMaxSplits ? kMaxSplits : f));
+}
+
 }  // namespace
 }  // namespace gbattn
 
@@ -377,7 +387,8 @@ size_t attn_decode_multitoken_workspace_size(int B, int Hq, int Hkv, int Tq, int
     if (Hq % Hkv != 0) return 0;
     if ((long long)B * Hq * Tq > kIntMax) return 0;
     const DecodeRows dr = decode_rows(Hq, Hkv, Tq);
-    return decode_workspace_bytes(B * Tq, Hq, B * Hkv, dr.n_hg, d, decode_slots(Lmax, num_splits));
+    return decode_workspace_bytes(B * Tq, Hq, B * Hkv, dr.n_hg, d,
+                                  decode_slots(Lmax, num_splits, auto_floor(B, Hkv, dr)));
 }
 
 int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache,
@@ -396,8 +407,9 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
         (lse && !aligned16(lse)) || (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
         return GBATTN_ERR_MISALIGNED;
     if ((long long)B * Hq * Tq > kIntMax / 8) return GBATTN_ERR_TOO_LARGE;
-    const int n_slots = decode_slots(Lmax, num_splits);
     const DecodeRows dr = decode_rows(Hq, Hkv, Tq);
+    const int floor_splits = auto_floor(B, Hkv, dr);
+    const int n_slots = decode_slots(Lmax, num_splits, floor_splits);
     const size_t need = decode_workspace_bytes(B * Tq, Hq, B * Hkv, dr.n_hg, d, n_slots);
     if (!workspace || ws_bytes < need) return GBATTN_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GBATTN_ERR_MISALIGNED;
@@ -431,6 +443,7 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
     p.n_hg = n_hg;
     p.n_slots = n_slots;
     p.fixed_splits = num_splits;
+    p.auto_floor = floor_splits;
     p.n_items = (int)n_items;
     // single launch (the group's last split merges) when every item runs in the first wave:
     // there the combine's launch is a large part of the call
@@ -458,6 +471,7 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
         tp.n_rt = (R + 127) / 128;
         tp.n_slots = n_slots;
         tp.fixed_splits = num_splits;
+        tp.auto_floor = floor_splits;
         const long long tc_items = (long long)n_slots * B * Hkv * tp.n_rt;
         if (tc_items > kIntMax) return GBATTN_ERR_TOO_LARGE;
         tp.n_items = (int)tc_items;

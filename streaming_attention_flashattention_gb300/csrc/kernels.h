@@ -55,20 +55,25 @@ struct DecodeParams {
     int n_hg;             // chunk groups per KV head: ceil(n_hc / nci)
     int n_slots;          // split slots per sequence
     int fixed_splits;     // > 0 fixed count, 0 automatic
+    int auto_floor;       // automatic mode: split count that fills the GPU (see splits_for)
     int n_items;          // n_slots * B * Hkv * n_hg
     int fused;            // 1: single launch, the group's last split merges (single token)
     float scale_log2;
     int* err;             // device error word of bounded waits
 };
-// Split-count rule of the automatic mode: one split per kAutoChunk keys.
+// Split-count rule of the automatic mode: one split per kAutoChunk keys, raised for calls
+// with few (sequence, KV head) groups to as many splits as still fit one wave of kAutoItems
+// work items (the SM count of a GB300), but never to fewer than kAutoMinKeys keys per split.
 constexpr int kAutoChunk = 4096;
+constexpr int kAutoItems = 152;
+constexpr int kAutoMinKeys = 256;
 constexpr int kMaxSplits = 256;
 constexpr int kSplitAlign = 64;
 
 size_t decode_counter_bytes(int B, int Hkv, int n_hg);
 // B_rows: B * Tq; kv_groups: B * Hkv
 size_t decode_workspace_bytes(int B_rows, int Hq, int kv_groups, int n_hg, int d, int n_slots);
-int decode_slots(int Lmax, int num_splits);
+int decode_slots(int Lmax, int num_splits, int auto_floor);
 cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
                                   cudaStream_t stream);
 // The log-sum-exp combine of the partials in the workspace, launched dependent on the
@@ -91,6 +96,7 @@ struct DecodeTcParams {
     int R;                // query rows per KV head: G * Tq
     int n_rt;             // 128-row tiles per KV head: ceil(R / 128)
     int n_slots, fixed_splits;
+    int auto_floor;       // automatic mode: split count that fills the GPU (see splits_for)
     int n_items;          // n_slots * B * Hkv * n_rt
     int* counter;         // work queue counter (zeroed before the kernel)
     float scale_log2;

@@ -110,8 +110,16 @@ def test_workspace_size(lib):
         return counters + ((rows * 4 + 255) // 256) * 256 + rows * d * 4
 
     assert ws(4, 64, 8, 32768, 128, 16) == expect(4, 64, 8, 16, 128)
-    # automatic: one slot per 4096 keys of capacity
+    # automatic: one slot per 4096 keys of capacity ...
     assert ws(16, 64, 8, 131072, 128, 0) == expect(16, 64, 8, 32, 128)
+    # ... raised for few (sequence, KV head) groups to the most splits that keep one wave of
+    # 152 work items: 8 groups take 152 // 8 = 19, capped by 256 keys per split (4096 / 256)
+    assert ws(1, 64, 8, 4096, 128, 0) == expect(1, 64, 8, 16, 128)
+    assert ws(1, 64, 8, 65536, 128, 0) == expect(1, 64, 8, 19, 128)
+    # 16 groups: 152 // 16 = 9 splits beat one per 4096 keys (8)
+    assert ws(2, 64, 8, 32768, 128, 0) == expect(2, 64, 8, 9, 128)
+    # 64 groups: 152 // 64 = 2, the same as one per 4096 keys
+    assert ws(8, 64, 8, 8192, 128, 0) == expect(8, 64, 8, 2, 128)
     assert ws(2, 32, 2, 100, 64, 1) == expect(2, 32, 2, 1, 64)
     assert ws(1, 1, 1, 1, 128, 0) > 0
     assert ws(0, 64, 8, 10, 128, 0) == 0
