@@ -168,9 +168,10 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int n
  * split streams its chunk once for all G = Hq / Hkv query heads of a KV head (the heads
  * are stacked into one MMA operand, "ADR-0060" section 5.2), and the partial (lse_s, O_s)
  * of the splits are merged ("ADR-0060" section 4; a sequence with one split is written
- * directly).  When every work item fits in one wave of the GPU the merge is done by the
- * CTA that finishes a group's last split (one launch, "ADR-0060" section 4.3); otherwise
- * a combine kernel, launched dependent on the split kernel, merges.  With G >= 16 query
+ * directly).  When every work item fits in one wave of the GPU, or the call has at most
+ * 16 (sequence, KV head) groups with splits of at least 1024 keys (Lmax / splits), the
+ * merge is done by the CTA that finishes a group's last split (one launch, "ADR-0060"
+ * section 4.3); otherwise a combine kernel, launched dependent on the split kernel, merges.  With G >= 16 query
  * heads per KV head the heads form the M = 128 operand of a tcgen05 kernel instead of
  * the N dimension of warp-level MMAs.  kv_lens values are
  * read on the device; values outside [0, Lmax] are clamped into it.

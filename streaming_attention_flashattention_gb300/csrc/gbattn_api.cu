@@ -93,6 +93,8 @@ __global__ void selftest_wait_kernel(int* err_word, long long limit) {
 }
 
 constexpr long long kIntMax = 2147483647LL;
+constexpr long long kFusedMaxGroups = 16;   // single-launch decode: up to this many groups,
+constexpr long long kFusedMinKeys = 1024;   // with splits of at least this many keys
 
 // bf16 tcgen05 prefill; K/V rows of one head are `kv_stride` rows apart (>= Skv).
 int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -445,9 +447,14 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
     p.fixed_splits = num_splits;
     p.auto_floor = floor_splits;
     p.n_items = (int)n_items;
-    // single launch (the group's last split merges) when every item runs in the first wave:
-    // there the combine's launch is a large part of the call
-    p.fused = (nci == 1 && n_items <= nsm) ? 1 : 0;
+    // single launch (the group's last split merges) when every item runs in the first wave,
+    // where the combine's launch is a large part of the call, or when there are few groups
+    // with long splits, where the combine's few threads wait on long partial lists; with
+    // many groups or short splits the per-split count and rendezvous cost more than the
+    // combine
+    const long long groups = (long long)B * Hkv * n_hg;
+    const bool few_long = groups <= kFusedMaxGroups && (long long)Lmax >= kFusedMinKeys * n_slots;
+    p.fused = (nci == 1 && (n_items <= nsm || few_long)) ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = device_error_word();
     if (!p.err) return GBATTN_ERR_CUDA;

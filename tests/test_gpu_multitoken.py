@@ -58,6 +58,9 @@ def run(B, Hq, Hkv, Tq, Lmax, d, lens, ns, seed=5):
     (1, 32, 4, 6, 700, 64, [700], 0),                 # 48 rows, d = 64, automatic splits
     (2, 16, 2, 4, 300, 128, [2, 300], 2),             # tcgen05 path with len < Tq: rows see no key
     (3, 16, 2, 2, 500, 128, [0, 500, 17], 4),         # tcgen05 path: an empty sequence, short ones
+    (2, 16, 2, 4, 600, 128, [0, 0], 3),               # tcgen05 path: no keys anywhere, no work item
+    (1, 16, 2, 64, 900, 128, [900], 3),               # 512 rows per KV head: four 128-row tiles
+    (2, 8, 1, 40, 700, 64, [700, 45], 0),             # 320 rows, d = 64, len < T_q, automatic
 ])
 def test_multitoken_decode_shapes(B, Hq, Hkv, Tq, Lmax, d, lens, ns):
     run(B, Hq, Hkv, Tq, Lmax, d, lens, ns)
