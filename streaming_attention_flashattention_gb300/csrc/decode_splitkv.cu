@@ -811,29 +811,41 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
     __syncthreads();
 }
 
-// One thread per (b, query head, 4 output columns): O = sum_s w_s O_s / sum_s w_s with
-// w_s = 2^(lse_s - max lse) over the non-empty splits, in one pass of 8 splits at a time.
+// The merge of the split partials ("ADR-0060" section 4): O = sum_s w_s O_s / sum_s w_s with
+// w_s = 2^(lse_s - max lse) over the non-empty splits.  Each (b, query head, 4 output
+// columns) piece is shared by p.combine_lanes adjacent lanes (a power of two, at most 32):
+// lane j merges splits [8 j, 8 j + 8) with all its loads in flight at once, and the lanes'
+// (max, sum, O) states are then merged with shuffles -- one round of partial loads instead
+// of one per 8 splits.
 template <int D>
 __global__ void __launch_bounds__(256)
 decode_combine_kernel(const __grid_constant__ DecodeParams p) {
     constexpr int kGroups = D / 4;
+    constexpr int kChunk = 8;
+    const int c = p.combine_lanes;
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long row = idx / kGroups;
-    const int cg = (int)(idx % kGroups);
+    const int j = (int)(idx % c);
+    const long long piece = idx / c;
+    const long long row = piece / kGroups;
+    const int cg = (int)(piece % kGroups);
     // the partials come from the split kernel launched just before this one
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (row >= (long long)p.B * p.Hq * p.Tq) return;
-    const int b = (int)(row / ((long long)p.Hq * p.Tq));
-    int len = __ldg(&p.kv_lens[b]);
-    len = max(0, min(len, p.Lmax));
-    const int n_ne = nonempty_splits(len, splits_for(len, p.fixed_splits, p.auto_floor));
-    if (n_ne <= 1) return;      // written directly by the split kernel
-    const float* lse_s = p.ws_lse + row * p.n_slots;
-    const float* o_s = p.ws_o + row * p.n_slots * D + cg * 4;
-    constexpr int kChunk = 8;
-    float M = -INFINITY, Ltot = 0.f;
+    // every lane takes part in the shuffles below; rows past the end or written directly by
+    // the split kernel just contribute nothing and store nothing
+    int n_ne = 0;
+    if (row < (long long)p.B * p.Hq * p.Tq) {
+        const int b = (int)(row / ((long long)p.Hq * p.Tq));
+        int len = __ldg(&p.kv_lens[b]);
+        len = max(0, min(len, p.Lmax));
+        n_ne = nonempty_splits(len, splits_for(len, p.fixed_splits, p.auto_floor));
+    }
+    const bool merge = n_ne > 1;
+    float M = -INFINITY, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < n_ne; s0 += kChunk) {
+    if (merge) {
+        const float* lse_s = p.ws_lse + row * p.n_slots;
+        const float* o_s = p.ws_o + row * p.n_slots * D + cg * 4;
+        const int s0 = j * kChunk;
         float ls[kChunk];
         float4 ox[kChunk];
         #pragma unroll
@@ -843,28 +855,41 @@ decode_combine_kernel(const __grid_constant__ DecodeParams p) {
             ox[i] = in ? __ldcg(reinterpret_cast<const float4*>(o_s + (long long)(s0 + i) * D))
                        : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        float Mc = M;
         #pragma unroll
-        for (int i = 0; i < kChunk; ++i) Mc = fmaxf(Mc, ls[i]);
-        const float sc = (M == -INFINITY) ? 0.f : ex2_approx(M - Mc);
-        Ltot *= sc;
-        acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+        for (int i = 0; i < kChunk; ++i) M = fmaxf(M, ls[i]);
         #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
             if (ls[i] == -INFINITY) continue;     // a split this row saw no key of
-            const float w = ex2_approx(ls[i] - Mc);
-            Ltot += w;
+            const float w = ex2_approx(ls[i] - M);
+            L += w;
             acc.x += w * ox[i].x; acc.y += w * ox[i].y; acc.z += w * ox[i].z; acc.w += w * ox[i].w;
         }
-        M = Mc;
     }
-    const float inv = Ltot > 0.f ? 1.f / Ltot : 0.f;
+    // merge the c lanes' states: (M, L, acc) with L and acc relative to 2^M
+    for (int off = 1; off < c; off <<= 1) {
+        const float Mo = __shfl_xor_sync(0xffffffffu, M, off);
+        const float Lo = __shfl_xor_sync(0xffffffffu, L, off);
+        float4 ao;
+        ao.x = __shfl_xor_sync(0xffffffffu, acc.x, off);
+        ao.y = __shfl_xor_sync(0xffffffffu, acc.y, off);
+        ao.z = __shfl_xor_sync(0xffffffffu, acc.z, off);
+        ao.w = __shfl_xor_sync(0xffffffffu, acc.w, off);
+        const float Mn = fmaxf(M, Mo);
+        const float a = (M == -INFINITY) ? 0.f : ex2_approx(M - Mn);
+        const float bo = (Mo == -INFINITY) ? 0.f : ex2_approx(Mo - Mn);
+        L = L * a + Lo * bo;
+        acc.x = acc.x * a + ao.x * bo; acc.y = acc.y * a + ao.y * bo;
+        acc.z = acc.z * a + ao.z * bo; acc.w = acc.w * a + ao.w * bo;
+        M = Mn;
+    }
+    if (!merge || j != 0) return;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
     uint2 packed;
     packed.x = pack_bf16(acc.x * inv, acc.y * inv);
     packed.y = pack_bf16(acc.z * inv, acc.w * inv);
     *reinterpret_cast<uint2*>(p.o + row * D + cg * 4) = packed;
     if (cg == 0 && p.lse != nullptr)
-        p.lse[row] = Ltot > 0.f ? (M + __log2f(Ltot)) * 0.69314718055994531f : -INFINITY;
+        p.lse[row] = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
 }  // namespace
@@ -902,7 +927,7 @@ cudaError_t launch_pair(const DecodeParams& p, int num_sms, cudaStream_t stream)
     if (err != cudaSuccess) return err;
     if constexpr (kFused) return cudaSuccess;      // merged in the split kernel
     // combine: programmatic dependent launch on the same stream
-    const long long threads = (long long)p.B * p.Hq * p.Tq * (D / 4);
+    const long long threads = (long long)p.B * p.Hq * p.Tq * (D / 4) * p.combine_lanes;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((threads + 255) / 256));
     cfg.blockDim = dim3(256);
@@ -918,7 +943,7 @@ cudaError_t launch_pair(const DecodeParams& p, int num_sms, cudaStream_t stream)
 
 template <int D>
 cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
-    const long long threads = (long long)p.B * p.Hq * p.Tq * (D / 4);
+    const long long threads = (long long)p.B * p.Hq * p.Tq * (D / 4) * p.combine_lanes;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((threads + 255) / 256));
     cfg.blockDim = dim3(256);

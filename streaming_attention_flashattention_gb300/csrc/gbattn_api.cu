@@ -446,6 +446,8 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
     p.n_slots = n_slots;
     p.fixed_splits = num_splits;
     p.auto_floor = floor_splits;
+    p.combine_lanes = 1;
+    while (p.combine_lanes * 8 < n_slots) p.combine_lanes *= 2;   // n_slots <= 256: at most 32
     p.n_items = (int)n_items;
     // single launch (the group's last split merges) when every item runs in the first wave,
     // where the combine's launch is a large part of the call, or when there are few groups

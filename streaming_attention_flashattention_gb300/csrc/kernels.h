@@ -56,6 +56,7 @@ struct DecodeParams {
     int n_slots;          // split slots per sequence
     int fixed_splits;     // > 0 fixed count, 0 automatic
     int auto_floor;       // automatic mode: split count that fills the GPU (see splits_for)
+    int combine_lanes;    // combine: lanes per (row, 4 columns), a power of two >= n_slots / 8
     int n_items;          // n_slots * B * Hkv * n_hg
     int fused;            // 1: single launch, the group's last split merges (single token)
     float scale_log2;
