@@ -187,9 +187,10 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
  * attn_decode_multitoken -- decode of Tq >= 1 new tokens per sequence at once (for
  * example speculative decoding), split-KV with the same log-sum-exp merge.  The G * Tq
  * query rows of a KV head are stacked into the MMA operand ("ADR-0060" section 0.5:
- * the group's Q [G, T_q, d] folds to [G * T_q, d]).  Up to 15 rows run 8 at a time on
- * warp-level MMAs; 16 or more run as the M = 128 operand of tcgen05 MMAs, each K/V tile
- * read once per 128 rows.
+ * the group's Q [G, T_q, d] folds to [G * T_q, d]).  Up to 8 rows run on warp-level MMAs;
+ * 16 or more, or 9 to 15 with splits of at least 1024 keys (Lmax / splits), run as the
+ * M = 128 operand of tcgen05 MMAs, each K/V tile read once per 128 rows; other 9 to 15 row
+ * calls run 8 rows at a time on warp-level MMAs.
  *
  *   q       [B, Hq, Tq, d]      device, bf16    the new tokens' post-RoPE queries
  *   kcache  [B, Hkv, Lmax, d]   device, bf16    key cache; the new tokens' keys are

@@ -15,10 +15,11 @@
 // The CTAs are persistent, one per SM, and pull items from a device counter:
 //   warp 0      work queue and Q/K producer: claims the next item, hands it to the other
 //               warps through a two-entry ring in shared memory, then loads the item's rows
-//               of Q (one 128-row tile; rows past R belong to the next KV head or lie
-//               outside the tensor and are never stored) and the split's K in 128-key tiles
-//               into a 2-slot ring.  It moves on to the next item's tiles as soon as ring
-//               slots free up, so the loads run on through the item boundaries;
+//               of Q (its R rows rounded up to 8, at most one 128-row tile: the other rows
+//               of the M = 128 operand keep stale data and only yield output rows that are
+//               never stored) and the split's K in 128-key tiles into a 2-slot ring.  It
+//               moves on to the next item's tiles as soon as ring slots free up, so the loads
+//               run on through the item boundaries;
 //   warp 2      V producer: the same tiles of V into a 3-slot ring.  A V slot is held until
 //               its P.V product completes, long after the K tile's S product, so V gets the
 //               deeper ring and its own thread: K loads never wait behind a V slot;
@@ -32,8 +33,8 @@
 // to the workspace (a sequence with a single split writes its final O and LSE); the decode
 // combine kernel, launched dependent on this one, folds the partials.  Meanwhile the next
 // item's S products are already running.
-// Decode reads each K/V byte once for R rows: with R >= 16 the MMA work per byte is small
-// enough on tcgen05 that the kernel runs at the memory rate.
+// Decode reads each K/V byte once for R rows: the MMA work per byte is small enough on
+// tcgen05 that the kernel runs at the memory rate even with 9 rows of 128 in use.
 #include "common.cuh"
 #include "decode_splits.cuh"
 #include "kernels.h"
@@ -192,7 +193,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                 }
                 if (ok && k > 0) ok = mbar_wait(q_empty, (k - 1) & 1, kErrWaitProducer, p.err);
                 if (ok) {
-                    mbar_arrive_expect_tx(q_full, L::kTileBytes);
+                    mbar_arrive_expect_tx(q_full, (uint32_t)(L::kBoxes * p.q_rows * 128));
                     #pragma unroll
                     for (int bx = 0; bx < L::kBoxes; ++bx)
                         tma_load_3d(smem + L::kQ0 + bx * L::kBoxBytes, &p.tmap_q, bx * 64, (int)row0, 0, q_full);

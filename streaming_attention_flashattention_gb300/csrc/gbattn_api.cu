@@ -95,6 +95,8 @@ __global__ void selftest_wait_kernel(int* err_word, long long limit) {
 constexpr long long kIntMax = 2147483647LL;
 constexpr long long kFusedMaxGroups = 16;   // single-launch decode: up to this many groups,
 constexpr long long kFusedMinKeys = 1024;   // with splits of at least this many keys
+constexpr long long kTcMinKeys = 1024;      // 9-15 rows per KV head: tcgen05 path from this
+                                            // many keys per split
 
 // bf16 tcgen05 prefill; K/V rows of one head are `kv_stride` rows apart (>= Skv).
 int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -461,12 +463,19 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
     p.err = device_error_word();
     if (!p.err) return GBATTN_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (R >= 16) {
-        // tcgen05 path (16 or more query rows per KV head: several new tokens, or G >= 16):
+    // tcgen05 path: 16 or more query rows per KV head (several new tokens, or G >= 16), or 9
+    // to 15 with long splits; 8 rows and fewer, and short splits of 9 to 15 rows, run best on
+    // the warp-level kernel, whose work items carry less fixed cost
+    if (R >= 16 || (R >= 9 && (long long)Lmax >= kTcMinKeys * n_slots)) {
+        // tcgen05 path:
         // the KV head's rows as the M = 128 operand, each K/V tile read once per 128 rows;
         // the combine folds the partials as for the split kernel
         DecodeTcParams tp{};
-        if (!make_map_bf16_3d(&tp.tmap_q, q, d, (uint64_t)B * Hq * Tq, 1, 128) ||
+        // only the item's own rows of Q are loaded (R rounded up to 8); the MMA's other rows
+        // of the M = 128 operand hold whatever the buffer held and only produce rows that are
+        // never stored (each output row depends on its own query row alone)
+        const int q_rows = R >= 128 ? 128 : (R + 7) / 8 * 8;
+        if (!make_map_bf16_3d(&tp.tmap_q, q, d, (uint64_t)B * Hq * Tq, 1, (uint32_t)q_rows) ||
             !make_map_bf16_3d(&tp.tmap_k, kcache, d, Lmax, (uint64_t)B * Hkv, 128) ||
             !make_map_bf16_3d(&tp.tmap_v, vcache, d, Lmax, (uint64_t)B * Hkv, 128))
             return GBATTN_ERR_CUDA;
@@ -477,6 +486,7 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
         tp.ws_o = p.ws_o;
         tp.B = B; tp.Hq = Hq; tp.Hkv = Hkv; tp.Lmax = Lmax; tp.Tq = Tq;
         tp.R = R;
+        tp.q_rows = q_rows;
         tp.n_rt = (R + 127) / 128;
         tp.n_slots = n_slots;
         tp.fixed_splits = num_splits;

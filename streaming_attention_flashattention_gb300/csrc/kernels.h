@@ -85,7 +85,7 @@ cudaError_t launch_decode_combine(const DecodeParams& p, int d, cudaStream_t str
 // Work items (b, KV head, split, 128-row tile of the R = G * Tq rows); partials go to the
 // same workspace layout as the split kernel's and are folded by launch_decode_combine.
 struct DecodeTcParams {
-    CUtensorMap tmap_q;   // 3-D (d, B*Hq*Tq, 1), box (64, 128, 1), 128B swizzle
+    CUtensorMap tmap_q;   // 3-D (d, B*Hq*Tq, 1), box (64, q_rows, 1), 128B swizzle
     CUtensorMap tmap_k;   // 3-D (d, Lmax, B*Hkv), box (64, 128, 1), 128B swizzle
     CUtensorMap tmap_v;
     const int* kv_lens;
@@ -95,6 +95,7 @@ struct DecodeTcParams {
     float* ws_o;          // [B, Hq, Tq, n_slots, d]
     int B, Hq, Hkv, Lmax, Tq;
     int R;                // query rows per KV head: G * Tq
+    int q_rows;           // Q rows loaded per item: R rounded up to 8, at most 128
     int n_rt;             // 128-row tiles per KV head: ceil(R / 128)
     int n_slots, fixed_splits;
     int auto_floor;       // automatic mode: split count that fills the GPU (see splits_for)

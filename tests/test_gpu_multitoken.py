@@ -61,6 +61,8 @@ def run(B, Hq, Hkv, Tq, Lmax, d, lens, ns, seed=5):
     (2, 16, 2, 4, 600, 128, [0, 0], 3),               # tcgen05 path: no keys anywhere, no work item
     (1, 16, 2, 64, 900, 128, [900], 3),               # 512 rows per KV head: four 128-row tiles
     (2, 8, 1, 40, 700, 64, [700, 45], 0),             # 320 rows, d = 64, len < T_q, automatic
+    (2, 8, 2, 3, 9000, 128, [9000, 4100], 4),         # 12 rows, long splits: tcgen05 path
+    (1, 8, 8, 9, 5000, 64, [5000], 2),                # 9 rows, long splits, d = 64: tcgen05 path
 ])
 def test_multitoken_decode_shapes(B, Hq, Hkv, Tq, Lmax, d, lens, ns):
     run(B, Hq, Hkv, Tq, Lmax, d, lens, ns)
