@@ -123,11 +123,38 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, fl
     if (nsm <= 0) return GBATTN_ERR_CUDA;
     p.kv_split = n_pairs < 2LL * nsm ? 1 : 0;
     p.n_pairs = (int)(p.kv_split ? n_tiles : n_pairs);
+    p.tail0 = -1;
     p.causal = causal;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = device_error_word();
     if (!p.err) return GBATTN_ERR_CUDA;
+    // Pairs of nearly equal weight (non-causal, or a chunk at the end of a long context)
+    // whose last wave is at most half full: those last pairs run as single Q tiles in
+    // KV-split mode, launched behind the pair grid as a programmatic dependent so that they
+    // fill SMs as the pair grid drains -- half a pair's time instead of a whole one.
+    // (Causal prefill over its whole context has pairs of all weights, heaviest first, and
+    // keeps one launch.)
+    long long tail = 0;
+    if (!p.kv_split) {
+        auto kv_tiles = [&](long long q0) {
+            if (!causal) return ((long long)Skv + 127) / 128;
+            const long long last = std::min<long long>(q0 + 128, Sq) - 1;
+            const long long keys = std::min<long long>(Skv, last + (Skv - Sq) + 1);
+            return (keys + 127) / 128;
+        };
+        const long long lo = kv_tiles(0), hi = kv_tiles((long long)(p.n_qblk - 1) * 128);
+        const long long rem = n_pairs % nsm;
+        if (lo > 0 && 4 * hi <= 5 * lo && rem > 0 && rem <= nsm / 2) tail = rem;
+    }
+    p.n_pairs = (int)(p.n_pairs - tail);
     cudaError_t e = launch_attn_fwd_bf16(p, d, st);
+    if (e == cudaSuccess && tail > 0) {
+        PrefillParams t = p;
+        t.kv_split = 1;
+        t.tail0 = (int)(n_pairs - tail);
+        t.n_pairs = (int)(2 * tail);
+        e = launch_attn_fwd_bf16_tail(t, d, st);
+    }
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 

@@ -29,11 +29,16 @@ struct PrefillParams {
     int n_qblk;           // ceil(Sq / 128)
     int n_pairs;          // work items: pairs of Q tiles, or single Q tiles with kv_split
     int kv_split;         // 1: each CTA splits one Q tile's KV range over its two slots
+    int tail0;            // KV split: -1, or the first pair whose two Q tiles the CTAs take
+                          // (the last, partly filled wave of a pair-mode call)
     int causal;
     float scale_log2;     // scale * log2(e)
     int* err;             // device error word of bounded waits
 };
 cudaError_t launch_attn_fwd_bf16(const PrefillParams& p, int d, cudaStream_t stream);
+// The Q tiles of pairs [p.tail0, p.tail0 + p.n_pairs / 2) in KV-split mode, launched as a
+// programmatic dependent of the pair-mode launch just before it (p.n_pairs = tiles).
+cudaError_t launch_attn_fwd_bf16_tail(const PrefillParams& p, int d, cudaStream_t stream);
 
 // ---- bf16 split-KV decode path (decode_splitkv.cu) --------------------------------------
 struct DecodeParams {

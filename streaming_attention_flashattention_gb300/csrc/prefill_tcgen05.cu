@@ -100,6 +100,21 @@ __device__ __forceinline__ void split_tiles(const PrefillParams& p, int rank, in
 }
 
 __device__ __forceinline__ void pair_tiles(const PrefillParams& p, int rank, int& b, int& kvh,
+                                           TileDesc (&t)[2]);
+
+// KV-split mode over the last pairs of a pair-mode call: item `rank` is Q tile rank % 2 of
+// pair tail0 + rank / 2; slot 0 takes KV tiles [0, n0), slot 1 takes [n0, n).
+__device__ __forceinline__ void tail_tiles(const PrefillParams& p, int rank, int& b, int& kvh,
+                                           TileDesc (&t)[2]) {
+    TileDesc pt[2];
+    pair_tiles(p, p.tail0 + rank / 2, b, kvh, pt);
+    const TileDesc me = (rank & 1) ? pt[1] : pt[0];
+    const int n0 = (me.n_kv + 1) / 2;
+    t[0] = me; t[0].n_kv = n0; t[0].kv0 = 0;
+    t[1] = me; t[1].present = me.present && me.n_kv - n0 > 0; t[1].n_kv = me.n_kv - n0; t[1].kv0 = n0;
+}
+
+__device__ __forceinline__ void pair_tiles(const PrefillParams& p, int rank, int& b, int& kvh,
                                            TileDesc (&t)[2]) {
     const int n_groups = p.B * p.Hkv;
     const int cnt = p.n_qblk * p.G;                 // Q tiles per (b, kv head)
@@ -121,7 +136,8 @@ __device__ __forceinline__ void pair_tiles(const PrefillParams& p, int rank, int
     }
 }
 
-template <int D, bool kSplit>
+// kTail (with kSplit): the Q tiles of a pair-mode call's last pairs, launched behind it
+template <int D, bool kSplit, bool kTail = false>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
     constexpr int KS = kSplit ? 3 : 2;   // K ring slots
@@ -146,8 +162,16 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
 
     int b, kvh;
     TileDesc td[2];
-    if constexpr (kSplit) split_tiles(p, blockIdx.x, b, kvh, td);
-    else pair_tiles(p, blockIdx.x, b, kvh, td);
+    if constexpr (kTail) {
+        tail_tiles(p, blockIdx.x, b, kvh, td);
+        if (!td[0].present) return;          // the absent second tile of an odd last pair
+    } else if constexpr (kSplit) {
+        split_tiles(p, blockIdx.x, b, kvh, td);
+    } else {
+        pair_tiles(p, blockIdx.x, b, kvh, td);
+        // a KV-split launch of the last pairs may start on SMs this grid leaves free
+        if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
     const int n_kv_max = max(td[0].n_kv, td[1].n_kv);
     // K ring slot of fill f: with KV split, slot 0 is the unused second Q buffer
     auto k_slot = [&](uint32_t f) -> uint8_t* {
@@ -534,6 +558,9 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
         tc_fence_after();
         tmem_dealloc(tmem, L::kTmemCols);
     }
+    // a tail launch finishes only after the pair-mode grid it overlaps
+    if constexpr (kTail)
+        if (blockIdx.x == 0 && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int D, bool kSplit>
@@ -547,6 +574,30 @@ cudaError_t launch_variant(const PrefillParams& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+template <int D>
+cudaError_t launch_tail(const PrefillParams& p, cudaStream_t stream) {
+    constexpr int smem = PLayout<D>::kAlloc;
+    cudaError_t err = cudaFuncSetAttribute(prefill_fwd_kernel<D, true, true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.n_pairs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_fwd_kernel<D, true, true>, p);
+}
+
+cudaError_t launch_attn_fwd_bf16_tail(const PrefillParams& p, int d, cudaStream_t stream) {
+    if (p.n_pairs <= 0) return cudaSuccess;
+    return d == 128 ? launch_tail<128>(p, stream) : launch_tail<64>(p, stream);
+}
 
 cudaError_t launch_attn_fwd_bf16(const PrefillParams& p, int d, cudaStream_t stream) {
     if (p.n_pairs <= 0) return cudaSuccess;

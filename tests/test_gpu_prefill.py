@@ -186,3 +186,42 @@ def test_bf16_single_sm_pair_mode_d64():
 def test_bf16_split_mode_ragged_noncausal_long_kv():
     # few Q tiles and a long KV range: one tile's two KV halves merged in the CTA
     check(small(1, 2, 1, 100, 3000, 128, False, seed=19))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S", [(1, 32, 8, 4096), (2, 32, 8, 3072)])
+def test_noncausal_with_split_tail_sampled(B, Hq, Hkv, S):
+    # 512 (768) equal pairs on 152 SMs leave a last wave of 56 (8) pairs: those run as single
+    # Q tiles in KV-split mode in a second launch (the first Q blocks of every head, since
+    # they are the last in the pairs' order); sample rows there and elsewhere
+    w = small(B, Hq, Hkv, S, S, 128, False, seed=31)
+    rng = np.random.default_rng(31)
+    n_rows = B * Hq * S
+    heads = np.arange(B * Hq)
+    rows = np.unique(np.concatenate([
+        (heads[:, None] * S + rng.integers(0, 512, (B * Hq, 4))).reshape(-1),   # tail tiles
+        rng.integers(0, n_rows, 200),
+        [0, n_rows - 1],
+    ]))
+    check(w, rows=rows)
+
+
+def test_noncausal_tail_launch_repeat_and_graph():
+    # the two launches of a call with a KV-split tail replay in a CUDA graph as one step
+    w = small(1, 32, 8, 4096, 4096, 128, False, seed=33)
+    q, k, v = (t.cuda() for t in wl.prefill_inputs(w))
+    o1, l1 = gb.attn_fwd(q, k, v, causal=False)
+    o = torch.empty_like(o1)
+    lse = torch.empty_like(l1)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        gb.attn_fwd(q, k, v, causal=False, out=o, lse=lse)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        gb.attn_fwd(q, k, v, causal=False, out=o, lse=lse)
+    o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, o1) and torch.equal(lse, l1)
