@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_FLUSH_BYTES = 512 << 20
 # DRAM bytes per launch from the committed ncu captures (profiles/); None when the kernel
 # changed after the capture.
-NCU_TRAFFIC = {"prefill": 266_044_672, "decode": 541_500_672}
+NCU_TRAFFIC = {"prefill": 266_501_376, "decode": 541_500_672}
 
 
 def prefill_flops(w: wl.Workload) -> float:
@@ -424,7 +424,7 @@ def run_gpu(args, rank, world, local_rank):
         "data": "synthetic", "config": config_dict(args),
         "roofline": {"bound": "tensor", "achieved": per_gpu_tf, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": per_gpu_tf / peak_tf,
-                     "traffic": NCU_TRAFFIC["prefill"], "kernel": "prefill_fwd_kernel<128>",
+                     "traffic": NCU_TRAFFIC["prefill"], "kernel": "prefill_fwd_kernel<128, 0, 0> (pairs)",
                      "ms": pre_avg, "peak_source": f"{peak_src} bf16 burst"},
         "decode": {"value": dec_gbs, "unit": "GB/s", "ms": dec_avg,
                    "roofline": {"bound": "hbm", "achieved": per_gpu_bw, "peak": peak_bw,
