@@ -75,6 +75,12 @@ enum {
  * causal requires Sq <= Skv; all pointers 16-byte aligned.
  * Tile classes follow "ADR-0060" section 5.4: KV tiles entirely in a query tile's future
  * are skipped, tiles crossing the diagonal are masked, the rest run unmasked.
+ * bf16 work items are pairs of Q tiles (one CTA each), or single Q tiles with their KV range
+ * split over a CTA's two slots when pairs would not fill the GPU twice over.  When the pairs
+ * weigh nearly the same (non-causal calls, or a chunk at the end of a long context) and
+ * their last wave is at most half full, that wave's Q tiles run split in a second launch,
+ * a programmatic dependent of the first that ends after it.  Stream order and CUDA graph
+ * capture see one call either way.
  * Returns GBATTN_OK or a negative status; nothing is launched on error.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
