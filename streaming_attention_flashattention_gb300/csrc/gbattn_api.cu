@@ -125,6 +125,7 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, fl
     p.n_pairs = (int)(p.kv_split ? n_tiles : n_pairs);
     p.tail0 = -1;
     p.causal = causal;
+    p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = device_error_word();
     if (!p.err) return GBATTN_ERR_CUDA;

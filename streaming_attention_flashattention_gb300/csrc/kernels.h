@@ -32,6 +32,7 @@ struct PrefillParams {
     int tail0;            // KV split: -1, or the first pair whose two Q tiles the CTAs take
                           // (the last, partly filled wave of a pair-mode call)
     int causal;
+    int o_align32;        // o is 32-byte aligned: the epilogue may use 32-byte stores
     float scale_log2;     // scale * log2(e)
     int* err;             // device error word of bounded waits
 };

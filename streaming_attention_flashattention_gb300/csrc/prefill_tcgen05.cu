@@ -532,15 +532,23 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
                         uint32_t rr[32];
                         tmem_ld32(t_o + ch * 32, rr);
                         if (live) {
-                            uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+                            uint32_t w[16];
                             #pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4) {
-                                uint4 w;
-                                w.x = pack_bf16(__uint_as_float(rr[8 * q4 + 0]) * inv, __uint_as_float(rr[8 * q4 + 1]) * inv);
-                                w.y = pack_bf16(__uint_as_float(rr[8 * q4 + 2]) * inv, __uint_as_float(rr[8 * q4 + 3]) * inv);
-                                w.z = pack_bf16(__uint_as_float(rr[8 * q4 + 4]) * inv, __uint_as_float(rr[8 * q4 + 5]) * inv);
-                                w.w = pack_bf16(__uint_as_float(rr[8 * q4 + 6]) * inv, __uint_as_float(rr[8 * q4 + 7]) * inv);
-                                dst[q4] = w;
+                            for (int e = 0; e < 16; ++e)
+                                w[e] = pack_bf16(__uint_as_float(rr[2 * e]) * inv, __uint_as_float(rr[2 * e + 1]) * inv);
+                            if (p.o_align32) {          // 32-byte stores: half the store instructions
+                                #pragma unroll
+                                for (int h = 0; h < 2; ++h)
+                                    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                                                 :: "l"(orow + ch * 32 + h * 16), "r"(w[8 * h]), "r"(w[8 * h + 1]),
+                                                    "r"(w[8 * h + 2]), "r"(w[8 * h + 3]), "r"(w[8 * h + 4]),
+                                                    "r"(w[8 * h + 5]), "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
+                                                 : "memory");
+                            } else {
+                                uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+                                #pragma unroll
+                                for (int q4 = 0; q4 < 4; ++q4)
+                                    dst[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
                             }
                         }
                     }

@@ -225,3 +225,17 @@ def test_noncausal_tail_launch_repeat_and_graph():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(o, o1) and torch.equal(lse, l1)
+
+
+def test_output_16_byte_aligned_only():
+    # an output that is 16- but not 32-byte aligned takes the epilogue's 16-byte stores; the
+    # result is the same bits as with an aligned output
+    w = small(1, 16, 2, 2048, 2048, 128, True, seed=35)
+    q, k, v = (t.cuda() for t in wl.prefill_inputs(w))
+    o_ref, l_ref = gb.attn_fwd(q, k, v, causal=True)
+    buf = torch.empty(q.numel() + 64, dtype=torch.bfloat16, device="cuda")
+    o = buf[8:8 + q.numel()].view(q.shape)          # 16 bytes past a 256-byte boundary
+    assert o.data_ptr() % 32 == 16
+    _, lse = gb.attn_fwd(q, k, v, causal=True, out=o)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
