@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_FLUSH_BYTES = 512 << 20
 # DRAM bytes per launch from the committed ncu captures (profiles/); None when the kernel
 # changed after the capture.
-NCU_TRAFFIC = {"prefill": 266_501_376, "decode": 541_500_672}
+NCU_TRAFFIC = {"prefill": 275_330_304, "decode": 541_500_672}
 
 
 def prefill_flops(w: wl.Workload) -> float:
