@@ -242,6 +242,35 @@ int attn_decode_splitkv_noalloc(const void* q, const void* kcache, const void* v
                                 void* stream);
 
 /*
+ * attn_decode_plan -- what attn_decode_multitoken / attn_decode_splitkv (Tq = 1) decide for
+ * these sizes on a GPU with num_sms SMs.  Host only: no device access, for tests and
+ * capacity planning.  plan (host, 6 ints) receives:
+ *   plan[0]  splits per sequence the workspace holds (the automatic count for Lmax when
+ *            num_splits = 0)
+ *   plan[1]  kernel: 0 warp-level MMAs (8 query rows at a time), 1 tcgen05 (M = 128 rows)
+ *   plan[2]  merge: 1 in the split kernel (single launch), 0 a dependent combine kernel
+ *   plan[3]  work items of the kernel
+ *   plan[4]  query rows per KV head, G * Tq
+ *   plan[5]  combine lanes per (row, 4 columns)
+ * Returns GBATTN_OK or the status the decode call would return for these sizes.
+ */
+int attn_decode_plan(int B, int Hq, int Hkv, int Tq, int Lmax, int d, int num_splits,
+                     int num_sms, int* plan);
+
+/*
+ * attn_prefill_plan -- the work split attn_fwd (bf16) and attn_prefill_kvcache choose for
+ * these sizes on a GPU with num_sms SMs.  Host only.  plan (host, 4 ints) receives:
+ *   plan[0]  mode of the first launch: 0 pairs of Q tiles per CTA, 1 one Q tile per CTA with
+ *            its KV range split over the CTA's two slots
+ *   plan[1]  CTAs of the first launch
+ *   plan[2]  pairs whose Q tiles run KV-split in a second, dependent launch (0: none)
+ *   plan[3]  Q tiles in all
+ * Returns GBATTN_OK or a negative status for invalid sizes.
+ */
+int attn_prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int num_sms,
+                      int* plan);
+
+/*
  * attn_last_device_error -- synchronise `stream`, then read and clear the device error
  * word that bounded waits inside the kernels set when they give up (they never trap).
  * Returns GBATTN_OK, GBATTN_ERR_TIMEOUT (the word was set) or GBATTN_ERR_CUDA.

@@ -47,6 +47,8 @@ EXPORTS = {
     "attn_decode_multitoken_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "attn_decode_multitoken": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "attn_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "attn_decode_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
+    "attn_prefill_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
     "attn_last_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_int)]),
     "attn_selftest_bounded_wait": (_I, [_P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
@@ -334,6 +336,27 @@ def attn_decode_splitkv_noalloc(q: torch.Tensor, kcache: torch.Tensor, vcache: t
                                          _stream_ptr(stream))
     _check("attn_decode_splitkv_noalloc", st)
     return out, lse
+
+
+def attn_decode_plan(B: int, Hq: int, Hkv: int, Tq: int, Lmax: int, d: int, num_splits: int,
+                     num_sms: int) -> dict:
+    """The decode call's choices for these sizes on a GPU with num_sms SMs (host only)."""
+    plan = (ctypes.c_int * 6)()
+    _check("attn_decode_plan", load_library().attn_decode_plan(
+        B, Hq, Hkv, Tq, Lmax, d, num_splits, num_sms, plan))
+    return {"splits": plan[0], "kernel": "tcgen05" if plan[1] else "warp",
+            "merge": "single_launch" if plan[2] else "combine", "items": plan[3],
+            "rows_per_kv_head": plan[4], "combine_lanes": plan[5]}
+
+
+def attn_prefill_plan(B: int, Hq: int, Hkv: int, Sq: int, Skv: int, causal: bool,
+                      num_sms: int) -> dict:
+    """The bf16 prefill's work split for these sizes on a GPU with num_sms SMs (host only)."""
+    plan = (ctypes.c_int * 4)()
+    _check("attn_prefill_plan", load_library().attn_prefill_plan(
+        B, Hq, Hkv, Sq, Skv, 1 if causal else 0, num_sms, plan))
+    return {"mode": "kv_split" if plan[0] else "pairs", "first_launch_ctas": plan[1],
+            "tail_pairs": plan[2], "q_tiles": plan[3]}
 
 
 def attn_selftest_bounded_wait(stream=None) -> None:

@@ -98,6 +98,48 @@ constexpr long long kFusedMinKeys = 1024;   // with splits of at least this many
 constexpr long long kTcMinKeys = 1024;      // 9-15 rows per KV head: tcgen05 path from this
                                             // many keys per split
 
+// The work split of a bf16 prefill, from its sizes alone (used by the launch and by
+// attn_prefill_plan()).
+struct PrefillPlan {
+    int n_qblk;
+    long long n_pairs, n_tiles;
+    bool kv_split;           // one Q tile per CTA, its KV range over the CTA's two slots
+    long long first;         // CTAs of the first launch
+    long long tail;          // pairs run as KV-split tiles in a second launch
+};
+
+PrefillPlan prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int nsm) {
+    PrefillPlan pl{};
+    const int G = Hq / Hkv;
+    pl.n_qblk = (Sq + 127) / 128;
+    const long long per_group = ((long long)pl.n_qblk * G + 1) / 2;
+    pl.n_pairs = per_group * B * Hkv;
+    pl.n_tiles = (long long)pl.n_qblk * B * Hq;
+    // Pairs of Q tiles keep both ping-pong slots busy with independent work; when they
+    // would not fill the SMs twice over, splitting each tile's KV range over the two slots
+    // halves the longest item instead.
+    pl.kv_split = pl.n_pairs < 2LL * nsm;
+    // Pairs of nearly equal weight (non-causal, or a chunk at the end of a long context)
+    // whose last wave is at most half full: those last pairs run as single Q tiles in
+    // KV-split mode, launched behind the pair grid as a programmatic dependent so that they
+    // fill SMs as the pair grid drains -- half a pair's time instead of a whole one.
+    // (Causal prefill over its whole context has pairs of all weights, heaviest first, and
+    // keeps one launch.)
+    if (!pl.kv_split) {
+        auto kv_tiles = [&](long long q0) {
+            if (!causal) return ((long long)Skv + 127) / 128;
+            const long long last = std::min<long long>(q0 + 128, Sq) - 1;
+            const long long keys = std::min<long long>(Skv, last + (Skv - Sq) + 1);
+            return (keys + 127) / 128;
+        };
+        const long long lo = kv_tiles(0), hi = kv_tiles((long long)(pl.n_qblk - 1) * 128);
+        const long long rem = pl.n_pairs % nsm;
+        if (lo > 0 && 4 * hi <= 5 * lo && rem > 0 && rem <= nsm / 2) pl.tail = rem;
+    }
+    pl.first = pl.kv_split ? pl.n_tiles : pl.n_pairs - pl.tail;
+    return pl;
+}
+
 // bf16 tcgen05 prefill; K/V rows of one head are `kv_stride` rows apart (>= Skv).
 int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int Hq, int Hkv, int Sq, int Skv, int kv_stride, int d, float scale,
@@ -111,49 +153,25 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, fl
     p.lse = lse;
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv;
     p.G = Hq / Hkv;
-    p.n_qblk = (Sq + 127) / 128;
-    const long long per_group = ((long long)p.n_qblk * p.G + 1) / 2;
-    const long long n_pairs = per_group * B * Hkv;
-    const long long n_tiles = (long long)p.n_qblk * B * Hq;
-    if (n_pairs > kIntMax || n_tiles > kIntMax) return GBATTN_ERR_TOO_LARGE;
-    // Pairs of Q tiles keep both ping-pong slots busy with independent work; when they
-    // would not fill the SMs twice over, splitting each tile's KV range over the two slots
-    // halves the longest item instead.
     const int nsm = sm_count();
     if (nsm <= 0) return GBATTN_ERR_CUDA;
-    p.kv_split = n_pairs < 2LL * nsm ? 1 : 0;
-    p.n_pairs = (int)(p.kv_split ? n_tiles : n_pairs);
+    const PrefillPlan pl = prefill_plan(B, Hq, Hkv, Sq, Skv, causal, nsm);
+    if (pl.n_pairs > kIntMax || pl.n_tiles > kIntMax) return GBATTN_ERR_TOO_LARGE;
+    p.n_qblk = pl.n_qblk;
+    p.kv_split = pl.kv_split ? 1 : 0;
+    p.n_pairs = (int)pl.first;
     p.tail0 = -1;
     p.causal = causal;
     p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = device_error_word();
     if (!p.err) return GBATTN_ERR_CUDA;
-    // Pairs of nearly equal weight (non-causal, or a chunk at the end of a long context)
-    // whose last wave is at most half full: those last pairs run as single Q tiles in
-    // KV-split mode, launched behind the pair grid as a programmatic dependent so that they
-    // fill SMs as the pair grid drains -- half a pair's time instead of a whole one.
-    // (Causal prefill over its whole context has pairs of all weights, heaviest first, and
-    // keeps one launch.)
-    long long tail = 0;
-    if (!p.kv_split) {
-        auto kv_tiles = [&](long long q0) {
-            if (!causal) return ((long long)Skv + 127) / 128;
-            const long long last = std::min<long long>(q0 + 128, Sq) - 1;
-            const long long keys = std::min<long long>(Skv, last + (Skv - Sq) + 1);
-            return (keys + 127) / 128;
-        };
-        const long long lo = kv_tiles(0), hi = kv_tiles((long long)(p.n_qblk - 1) * 128);
-        const long long rem = n_pairs % nsm;
-        if (lo > 0 && 4 * hi <= 5 * lo && rem > 0 && rem <= nsm / 2) tail = rem;
-    }
-    p.n_pairs = (int)(p.n_pairs - tail);
     cudaError_t e = launch_attn_fwd_bf16(p, d, st);
-    if (e == cudaSuccess && tail > 0) {
+    if (e == cudaSuccess && pl.tail > 0) {
         PrefillParams t = p;
         t.kv_split = 1;
-        t.tail0 = (int)(n_pairs - tail);
-        t.n_pairs = (int)(2 * tail);
+        t.tail0 = (int)(pl.n_pairs - pl.tail);
+        t.n_pairs = (int)(2 * pl.tail);
         e = launch_attn_fwd_bf16_tail(t, d, st);
     }
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
@@ -250,6 +268,49 @@ int auto_floor(int B, int Hkv, const DecodeRows& dr) {
     const long long per_split = (long long)B * Hkv * (dr.R >= 16 ? (dr.R + 127) / 128 : dr.n_hg);
     const long long f = kAutoItems / per_split;
     return (int)(f < 1 ? 1 : (f > kMaxSplits ? kMaxSplits : f));
+}
+
+// Everything a decode call decides from its sizes alone, before any device access: the
+// split count, the kernel, the merge.  The launch code and attn_decode_plan() both use it.
+struct DecodePlan {
+    DecodeRows dr;
+    int floor_splits, n_slots;
+    long long n_items;       // work items of the warp-level kernel
+    bool tc;                 // the tcgen05 kernel runs the call
+    int n_rt, q_rows;        // tcgen05 kernel: 128-row tiles per KV head, Q rows loaded
+    long long tc_items;      // tcgen05 kernel: work items
+    bool fused;              // warp-level kernel: the merge happens in the split kernel
+    int combine_lanes;       // combine kernel: lanes per (row, 4 columns)
+};
+
+DecodePlan decode_plan(int B, int Hq, int Hkv, int Tq, int Lmax, int num_splits, int nsm) {
+    DecodePlan pl{};
+    pl.dr = decode_rows(Hq, Hkv, Tq);
+    pl.floor_splits = auto_floor(B, Hkv, pl.dr);
+    pl.n_slots = decode_slots(Lmax, num_splits, pl.floor_splits);
+    pl.n_items = (long long)pl.n_slots * B * Hkv * pl.dr.n_hg;
+    // tcgen05 path: 16 or more query rows per KV head (several new tokens, or G >= 16), or 9
+    // to 15 with long splits; 8 rows and fewer, and short splits of 9 to 15 rows, run best on
+    // the warp-level kernel, whose work items carry less fixed cost
+    const int R = pl.dr.R;
+    pl.tc = R >= 16 || (R >= 9 && (long long)Lmax >= kTcMinKeys * pl.n_slots);
+    pl.n_rt = (R + 127) / 128;
+    // only the item's own rows of Q are loaded (R rounded up to 8); the MMA's other rows of
+    // the M = 128 operand hold whatever the buffer held and only produce rows that are never
+    // stored (each output row depends on its own query row alone)
+    pl.q_rows = R >= 128 ? 128 : (R + 7) / 8 * 8;
+    pl.tc_items = (long long)pl.n_slots * B * Hkv * pl.n_rt;
+    // single launch (the group's last split merges) when every item runs in the first wave,
+    // where the combine's launch is a large part of the call, or when there are few groups
+    // with long splits, where the combine's few threads wait on long partial lists; with
+    // many groups or short splits the per-split count and rendezvous cost more than the
+    // combine
+    const long long groups = (long long)B * Hkv * pl.dr.n_hg;
+    const bool few_long = groups <= kFusedMaxGroups && (long long)Lmax >= kFusedMinKeys * pl.n_slots;
+    pl.fused = !pl.tc && pl.dr.nci == 1 && (pl.n_items <= nsm || few_long);
+    pl.combine_lanes = 1;
+    while (pl.combine_lanes * 8 < pl.n_slots) pl.combine_lanes *= 2;   // n_slots <= 256: at most 32
+    return pl;
 }
 
 }  // namespace
@@ -440,17 +501,17 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
         return GBATTN_ERR_MISALIGNED;
     if ((long long)B * Hq * Tq > kIntMax / 8) return GBATTN_ERR_TOO_LARGE;
     const DecodeRows dr = decode_rows(Hq, Hkv, Tq);
-    const int floor_splits = auto_floor(B, Hkv, dr);
-    const int n_slots = decode_slots(Lmax, num_splits, floor_splits);
+    const int n_slots = decode_slots(Lmax, num_splits, auto_floor(B, Hkv, dr));
     const size_t need = decode_workspace_bytes(B * Tq, Hq, B * Hkv, dr.n_hg, d, n_slots);
     if (!workspace || ws_bytes < need) return GBATTN_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GBATTN_ERR_MISALIGNED;
-    const int G = Hq / Hkv;
-    const int R = dr.R, n_hc = dr.n_hc, nci = dr.nci, n_hg = dr.n_hg;
-    const long long n_items = (long long)n_slots * B * Hkv * n_hg;
-    if (n_items > kIntMax || (long long)B * Hkv * Lmax > kIntMax) return GBATTN_ERR_TOO_LARGE;
     const int nsm = sm_count();
     if (nsm <= 0) return GBATTN_ERR_CUDA;
+    const DecodePlan pl = decode_plan(B, Hq, Hkv, Tq, Lmax, num_splits, nsm);
+    const int G = Hq / Hkv;
+    const int R = dr.R, n_hc = dr.n_hc, nci = dr.nci, n_hg = dr.n_hg;
+    const long long n_items = pl.n_items;
+    if (n_items > kIntMax || (long long)B * Hkv * Lmax > kIntMax) return GBATTN_ERR_TOO_LARGE;
 
     DecodeParams p{};
     if (!make_map_bf16_3d(&p.tmap_k, kcache, d, Lmax, (uint64_t)B * Hkv, 64) ||
@@ -475,34 +536,19 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
     p.n_hg = n_hg;
     p.n_slots = n_slots;
     p.fixed_splits = num_splits;
-    p.auto_floor = floor_splits;
-    p.combine_lanes = 1;
-    while (p.combine_lanes * 8 < n_slots) p.combine_lanes *= 2;   // n_slots <= 256: at most 32
+    p.auto_floor = pl.floor_splits;
+    p.combine_lanes = pl.combine_lanes;
     p.n_items = (int)n_items;
-    // single launch (the group's last split merges) when every item runs in the first wave,
-    // where the combine's launch is a large part of the call, or when there are few groups
-    // with long splits, where the combine's few threads wait on long partial lists; with
-    // many groups or short splits the per-split count and rendezvous cost more than the
-    // combine
-    const long long groups = (long long)B * Hkv * n_hg;
-    const bool few_long = groups <= kFusedMaxGroups && (long long)Lmax >= kFusedMinKeys * n_slots;
-    p.fused = (nci == 1 && (n_items <= nsm || few_long)) ? 1 : 0;
+    p.fused = pl.fused ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = device_error_word();
     if (!p.err) return GBATTN_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // tcgen05 path: 16 or more query rows per KV head (several new tokens, or G >= 16), or 9
-    // to 15 with long splits; 8 rows and fewer, and short splits of 9 to 15 rows, run best on
-    // the warp-level kernel, whose work items carry less fixed cost
-    if (R >= 16 || (R >= 9 && (long long)Lmax >= kTcMinKeys * n_slots)) {
-        // tcgen05 path:
-        // the KV head's rows as the M = 128 operand, each K/V tile read once per 128 rows;
-        // the combine folds the partials as for the split kernel
+    if (pl.tc) {
+        // tcgen05 path: the KV head's rows as the M = 128 operand, each K/V tile read once
+        // per 128 rows; the combine folds the partials as for the split kernel
         DecodeTcParams tp{};
-        // only the item's own rows of Q are loaded (R rounded up to 8); the MMA's other rows
-        // of the M = 128 operand hold whatever the buffer held and only produce rows that are
-        // never stored (each output row depends on its own query row alone)
-        const int q_rows = R >= 128 ? 128 : (R + 7) / 8 * 8;
+        const int q_rows = pl.q_rows;
         if (!make_map_bf16_3d(&tp.tmap_q, q, d, (uint64_t)B * Hq * Tq, 1, (uint32_t)q_rows) ||
             !make_map_bf16_3d(&tp.tmap_k, kcache, d, Lmax, (uint64_t)B * Hkv, 128) ||
             !make_map_bf16_3d(&tp.tmap_v, vcache, d, Lmax, (uint64_t)B * Hkv, 128))
@@ -515,11 +561,11 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
         tp.B = B; tp.Hq = Hq; tp.Hkv = Hkv; tp.Lmax = Lmax; tp.Tq = Tq;
         tp.R = R;
         tp.q_rows = q_rows;
-        tp.n_rt = (R + 127) / 128;
+        tp.n_rt = pl.n_rt;
         tp.n_slots = n_slots;
         tp.fixed_splits = num_splits;
-        tp.auto_floor = floor_splits;
-        const long long tc_items = (long long)n_slots * B * Hkv * tp.n_rt;
+        tp.auto_floor = pl.floor_splits;
+        const long long tc_items = pl.tc_items;
         if (tc_items > kIntMax) return GBATTN_ERR_TOO_LARGE;
         tp.n_items = (int)tc_items;
         tp.counter = p.counter;
@@ -539,6 +585,43 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
                         size_t ws_bytes, void* stream) {
     return attn_decode_multitoken(q, kcache, vcache, kv_lens, o, lse, B, Hq, Hkv, 1, Lmax, d,
                                   scale, num_splits, workspace, ws_bytes, stream);
+}
+
+int attn_decode_plan(int B, int Hq, int Hkv, int Tq, int Lmax, int d, int num_splits,
+                     int num_sms, int* plan) {
+    if (!plan) return GBATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Tq <= 0 || Lmax <= 0 || num_sms <= 0)
+        return GBATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || num_splits < 0 || num_splits > kMaxSplits) return GBATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return GBATTN_ERR_UNSUPPORTED;
+    if (Tq > 64) return GBATTN_ERR_UNSUPPORTED;
+    if ((long long)B * Hq * Tq > kIntMax / 8) return GBATTN_ERR_TOO_LARGE;
+    const DecodePlan pl = decode_plan(B, Hq, Hkv, Tq, Lmax, num_splits, num_sms);
+    const long long items = pl.tc ? pl.tc_items : pl.n_items;
+    if (items > kIntMax) return GBATTN_ERR_TOO_LARGE;
+    plan[0] = pl.n_slots;
+    plan[1] = pl.tc ? 1 : 0;
+    plan[2] = pl.fused ? 1 : 0;
+    plan[3] = (int)items;
+    plan[4] = pl.dr.R;
+    plan[5] = pl.combine_lanes;
+    return GBATTN_OK;
+}
+
+int attn_prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int num_sms,
+                      int* plan) {
+    if (!plan) return GBATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || num_sms <= 0)
+        return GBATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return GBATTN_ERR_INVALID_ARG;
+    if (causal && Sq > Skv) return GBATTN_ERR_UNSUPPORTED;
+    const PrefillPlan pl = prefill_plan(B, Hq, Hkv, Sq, Skv, causal, num_sms);
+    if (pl.n_pairs > kIntMax || pl.n_tiles > kIntMax) return GBATTN_ERR_TOO_LARGE;
+    plan[0] = pl.kv_split ? 1 : 0;
+    plan[1] = (int)pl.first;
+    plan[2] = (int)pl.tail;
+    plan[3] = (int)pl.n_tiles;
+    return GBATTN_OK;
 }
 
 int attn_selftest_bounded_wait(void* stream) {

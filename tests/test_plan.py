@@ -1,0 +1,116 @@
+"""Host-side planning of the library calls, pinned without a GPU.
+
+attn_decode_plan / attn_prefill_plan return what a call decides from its sizes alone (the
+split count, the kernel, the merge, the prefill work split); the launch code uses the same
+functions.  The expected values restate the rules in the header, on a 152-SM GB300.
+"""
+import pytest
+
+import streaming_attention_flashattention_gb300 as gb
+
+NSM = 152
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from streaming_attention_flashattention_gb300 import build
+    build.build()
+    gb.load_library()
+
+
+def dec(B, Hq, Hkv, Tq, L, ns, d=128):
+    return gb.attn_decode_plan(B, Hq, Hkv, Tq, L, d, ns, NSM)
+
+
+def test_llama70b_decode_16_splits():
+    p = dec(4, 64, 8, 1, 32768, 16)
+    assert p == {"splits": 16, "kernel": "warp", "merge": "combine", "items": 512,
+                 "rows_per_kv_head": 8, "combine_lanes": 2}
+
+
+def test_automatic_splits_fill_one_wave():
+    # 8 (sequence, KV head) groups: 152 // 8 = 19 splits, capped by 256 keys per split
+    assert dec(1, 64, 8, 1, 4096, 0)["splits"] == 16
+    assert dec(1, 64, 8, 1, 16384, 0)["splits"] == 19
+    # one split per 4096 keys wins when it is larger
+    assert dec(1, 64, 8, 1, 131072, 0)["splits"] == 32
+    # 64 groups: 152 // 64 = 2
+    assert dec(8, 64, 8, 1, 8192, 0)["splits"] == 2
+    # 128 groups: the floor is 1, the per-length rule decides
+    assert dec(16, 64, 8, 1, 131072, 0)["splits"] == 32
+    # fixed counts are kept
+    assert dec(1, 64, 8, 1, 4096, 7)["splits"] == 7
+
+
+def test_single_launch_merge_rule():
+    # one wave of work items
+    assert dec(1, 64, 8, 1, 4096, 0)["merge"] == "single_launch"          # 128 items
+    # few groups with long splits
+    p = dec(1, 64, 8, 1, 131072, 0)                                       # 8 groups, 4096 keys
+    assert p["items"] > NSM and p["merge"] == "single_launch"
+    # few groups, short splits (512 keys): combine
+    assert dec(1, 64, 8, 1, 32768, 64)["merge"] == "combine"
+    # many groups: combine
+    assert dec(4, 64, 8, 1, 32768, 16)["merge"] == "combine"
+
+
+def test_kernel_choice_by_rows_per_kv_head():
+    assert dec(4, 64, 8, 4, 32768, 16)["kernel"] == "tcgen05"             # 32 rows
+    assert dec(2, 32, 2, 1, 8192, 0)["kernel"] == "tcgen05"               # G = 16
+    assert dec(4, 64, 8, 2, 32768, 16)["kernel"] == "tcgen05"             # 16 rows
+    assert dec(4, 32, 8, 2, 32768, 16)["kernel"] == "warp"                # 8 rows
+    # 9 to 15 rows: tcgen05 only with splits of >= 1024 keys
+    assert dec(4, 32, 8, 3, 32768, 16)["kernel"] == "tcgen05"             # 12 rows, 2048 keys
+    p = dec(1, 32, 8, 3, 8192, 0)                                         # 12 rows, 19 x 431 keys
+    assert p["kernel"] == "warp" and p["splits"] == 19
+    # the tcgen05 kernel keeps the combine
+    assert dec(1, 64, 8, 4, 4096, 0)["merge"] == "combine"
+
+
+def test_combine_lanes_cover_every_split():
+    for ns, lanes in [(1, 1), (8, 1), (9, 2), (16, 2), (17, 4), (64, 8), (65, 16), (256, 32)]:
+        p = dec(64, 64, 8, 1, 300000, ns)
+        assert p["combine_lanes"] == lanes and 8 * lanes >= ns
+
+
+def test_decode_plan_rejects_what_the_call_rejects():
+    for args in [(0, 64, 8, 1, 100, 128, 0), (1, 64, 7, 1, 100, 128, 0), (1, 64, 8, 1, 100, 128, 257)]:
+        with pytest.raises(gb.GbAttnError) as e:
+            gb.attn_decode_plan(*args, NSM)
+        assert e.value.status == -1
+    with pytest.raises(gb.GbAttnError) as e:
+        gb.attn_decode_plan(1, 64, 8, 1, 100, 96, 0, NSM)
+    assert e.value.status == -2
+
+
+def pre(B, Hq, Hkv, Sq, Skv, causal):
+    return gb.attn_prefill_plan(B, Hq, Hkv, Sq, Skv, causal, NSM)
+
+
+def test_prefill_pairs_and_kv_split_mode():
+    # Llama3-70B causal prefill: 2048 pairs, heaviest first, one launch
+    assert pre(1, 64, 8, 8192, 8192, True) == {"mode": "pairs", "first_launch_ctas": 2048,
+                                               "tail_pairs": 0, "q_tiles": 4096}
+    # fewer than two pairs per SM: one Q tile per CTA
+    assert pre(2, 8, 2, 2048, 2048, True) == {"mode": "kv_split", "first_launch_ctas": 256,
+                                              "tail_pairs": 0, "q_tiles": 256}
+
+
+def test_prefill_tail_for_equal_pairs():
+    # a 2048-query chunk after a 16384-key context: 512 near-equal pairs, last wave of 56
+    assert pre(1, 64, 8, 2048, 16384, True) == {"mode": "pairs", "first_launch_ctas": 456,
+                                                "tail_pairs": 56, "q_tiles": 1024}
+    # non-causal, last wave 56 of 152: tail; last wave 112 (more than half): no tail
+    assert pre(1, 32, 8, 4096, 4096, False)["tail_pairs"] == 56
+    assert pre(1, 64, 8, 4096, 4096, False)["tail_pairs"] == 0
+    # causal over the whole context: weights 1..32 tiles, no tail however the waves fall
+    assert pre(1, 32, 8, 4096, 4096, True)["tail_pairs"] == 0
+    # a last wave that is exactly full: nothing to move
+    assert pre(1, 64, 8, 2432, 2432, False)["tail_pairs"] == 0
+
+
+def test_prefill_plan_rejects_invalid_sizes():
+    with pytest.raises(gb.GbAttnError):
+        gb.attn_prefill_plan(1, 64, 8, 4096, 2048, True, NSM)      # causal with Sq > Skv
+    with pytest.raises(gb.GbAttnError):
+        gb.attn_prefill_plan(1, 64, 7, 128, 128, False, NSM)
