@@ -114,3 +114,36 @@ def test_prefill_plan_rejects_invalid_sizes():
         gb.attn_prefill_plan(1, 64, 8, 4096, 2048, True, NSM)      # causal with Sq > Skv
     with pytest.raises(gb.GbAttnError):
         gb.attn_prefill_plan(1, 64, 7, 128, 128, False, NSM)
+
+
+def test_plan_agrees_with_workspace_size_and_invariants():
+    # seeded random sizes: the workspace the caller sizes holds exactly the plan's splits,
+    # items are splits x groups of the chosen kernel, lanes cover every split
+    import random
+    rng = random.Random(2024)
+    for _ in range(400):
+        Hkv = rng.choice([1, 2, 4, 8])
+        G = rng.choice([1, 2, 4, 8, 16])
+        B, Tq = rng.randint(1, 24), rng.choice([1, 1, 2, 3, 4, 5, 8, 16, 40])
+        L, d = rng.randint(1, 200000), rng.choice([64, 128])
+        ns = rng.choice([0, 0, 1, 3, 16, 64, 256])
+        p = gb.attn_decode_plan(B, G * Hkv, Hkv, Tq, L, d, ns, NSM)
+        rows = B * G * Hkv * Tq * p["splits"]
+        n_hc = (G * Tq + 7) // 8
+        nci = 4 if n_hc >= 3 else n_hc
+        n_hg = (n_hc + nci - 1) // nci
+        counters = ((1 + B * Hkv * n_hg) * 4 + 255) // 256 * 256
+        expect = counters + (rows * 4 + 255) // 256 * 256 + rows * d * 4
+        assert gb.load_library().attn_decode_multitoken_workspace_size(B, G * Hkv, Hkv, Tq, L, d, ns) == expect
+        assert 1 <= p["splits"] <= 256 and (ns == 0 or p["splits"] == ns)
+        per_split = B * Hkv * ((G * Tq + 127) // 128 if p["kernel"] == "tcgen05" else n_hg)
+        assert p["items"] == p["splits"] * per_split
+        assert p["rows_per_kv_head"] == G * Tq
+        lanes = p["combine_lanes"]
+        assert lanes & (lanes - 1) == 0 and 8 * lanes >= p["splits"] and 8 * (lanes // 2) < max(p["splits"], 2)
+        if p["merge"] == "single_launch":
+            assert p["kernel"] == "warp" and G * Tq <= 8
+        if G * Tq >= 16:
+            assert p["kernel"] == "tcgen05"
+        if G * Tq <= 8:
+            assert p["kernel"] == "warp"
