@@ -8,12 +8,17 @@ Printed JSON line (rank 0):
   value      prefill TFLOP/s, FLOPs = 4 B Hq Sq Skv d / 2 (causal), inputs resident in HBM
   decode     the decode half: KV GB/s (algorithmic bytes: K, V, Q, O, LSE) with its roofline
   roofline   prefill kernel: achieved TFLOP/s vs the measured dense bf16 peak
+  configs    every one of the five workloads timed on its own (L2 flushed before each
+             call, CUDA events): 1 tiny fp32, 2 small causal GQA prefill, 3 and 4 (the
+             step's two calls), 5 ragged decode, each with its fraction of the roofline
   e2e        the same metric through attn_fwd_host: pinned-host inputs copied in and
              outputs copied out by the call (chunked, overlapped with the kernel)
              inside the timed region, every step
-  cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload
-L2 is flushed (a 512 MiB write, then a read of it so no dirty lines remain) before the
-prefill and again before the decode of every step, outside the kernels' event windows.
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload; the same
+             leg compares sampled rows of every timed output with the oracle and fails the
+             run on a mismatch
+L2 is flushed (a 512 MiB write, then a read of it so no dirty lines remain) before every
+timed call, outside the kernels' event windows.
 
 --impl reference times the fp64 CPU oracle instead (a bounded row sample per step).
 Multi-GPU (torchrun, N > 1): N independent replicas, weak scaling, no collective on the
@@ -22,9 +27,10 @@ data path; the step time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
-import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -43,10 +49,43 @@ import attn_workloads as wl
 PREFILL = wl.WORKLOADS[3]
 DECODE = wl.WORKLOADS[4]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_HBM_GBS = 7900.0          # GB300 HBM3e nominal, for the decode fractions' second reading
 L2_FLUSH_BYTES = 512 << 20
-# DRAM bytes per launch from the committed ncu captures (profiles/); None when the kernel
-# changed after the capture.
-NCU_TRAFFIC = {"prefill": 275_330_304, "decode": 541_500_672}
+METRIC = "prefill attn TFLOP/s & decode KV GB/s at 1 GB300, % of roofline"
+CSRC = os.path.join(ROOT, "streaming_attention_flashattention_gb300", "csrc")
+# DRAM traffic per launch from the committed ncu summaries: each summary carries a line
+#   bench-traffic: bytes_per_launch=<n> sources_sha256=<hash of the kernel's sources>
+# and the figure is reported only while the sources still hash to the same value.
+TRAFFIC_SOURCES = {
+    "prefill": ("prefill_fwd_kernel_llama70b_causal_s8192.md",
+                ["prefill_tcgen05.cu", "common.cuh", "kernels.h"]),
+    "decode": ("decode_split_kernel_llama70b_l32768.md",
+               ["decode_splitkv.cu", "decode_splits.cuh", "common.cuh", "kernels.h"]),
+}
+
+
+def sources_sha256(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def committed_traffic(kind: str):
+    """(bytes per launch, note) from the ncu summary, or (None, why) when stale or absent."""
+    md, files = TRAFFIC_SOURCES[kind]
+    path = os.path.join(ROOT, "profiles", md)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None, f"no summary {md}"
+    m = re.search(r"bench-traffic: bytes_per_launch=(\d+) sources_sha256=([0-9a-f]{64})", text)
+    if not m:
+        return None, f"{md} has no bench-traffic line"
+    if m.group(2) != sources_sha256(files):
+        return None, f"kernel sources changed since the capture in {md}"
+    return int(m.group(1)), f"ncu capture in profiles/{md}"
 
 
 def prefill_flops(w: wl.Workload) -> float:
@@ -150,21 +189,67 @@ def oracle_sample_prefill(q_np, k_np, v_np, w: wl.Workload, n_rows: int, seed: i
     i = rows % w.Sq
     flops = float(np.sum(4.0 * w.d * ((i + 1 + (w.Skv - w.Sq)) if w.causal else np.full_like(i, w.Skv))))
     t0 = time.perf_counter()
-    oracle.attention(q_np, k_np, v_np, w.scale, w.causal, rows=rows)
-    return flops, time.perf_counter() - t0
+    o, lse = oracle.attention(q_np, k_np, v_np, w.scale, w.causal, rows=rows)
+    return flops, time.perf_counter() - t0, rows, o, lse
 
 
-def cpu_baseline_prefill(q, k, v, w: wl.Workload, target_s: float = 12.0):
+def _check_rows(name, o_gpu, lse_gpu, o_ref, lse_ref, dtype):
+    """Max / mean |dO| and max |dLSE| of sampled rows against the oracle; raises past the
+    parity bars (bf16: 2e-2 / 2e-3, fp32: 1e-4; LSE 1e-3)."""
+    o_gpu = np.asarray(o_gpu, dtype=np.float64)
+    err = np.abs(o_gpu - o_ref)
+    lerr = float(np.abs(np.asarray(lse_gpu, dtype=np.float64) - lse_ref).max())
+    mx, mean = float(err.max()), float(err.mean())
+    ok = np.all(np.isfinite(o_gpu)) and lerr <= 1e-3 and (
+        mx <= 1e-4 if dtype == "fp32" else (mx <= 2e-2 and mean <= 2e-3))
+    rec = {"rows": int(o_ref.reshape(-1, o_ref.shape[-1]).shape[0]), "max_abs": mx,
+           "mean_abs": mean, "lse_max_abs": lerr, "ok": bool(ok)}
+    if not ok:
+        raise RuntimeError(f"parity check failed on {name}: {rec}")
+    return rec
+
+
+def cpu_baseline_and_check(inputs, outputs, target_s: float = 12.0):
+    """The fp64 oracle timed on a bounded sample of the prefill workload (the baseline), and
+    every timed GPU output compared with the oracle on sampled rows (outside any timing)."""
     import oracle
+    w = PREFILL
+    q, k, v = inputs[3]
     q_np, k_np, v_np = wl.to_oracle(q), wl.to_oracle(k), wl.to_oracle(v)
     n = 256
-    flops, dt = oracle_sample_prefill(q_np, k_np, v_np, w, n, 1)
+    _, dt, _, _, _ = oracle_sample_prefill(q_np, k_np, v_np, w, n, 1)
     n2 = int(min(200000, max(n, n * target_s / max(dt, 1e-3))))
-    flops, dt = oracle_sample_prefill(q_np, k_np, v_np, w, n2, 2)
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+    flops, dt, rows, o_ref, lse_ref = oracle_sample_prefill(q_np, k_np, v_np, w, n2, 2)
+    base = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
             "kind": "oracle",
             "sample": f"{n2} random query rows of {w.name} (fp64 two-pass definition, "
                       f"{dt:.1f} s, {flops / 1e9:.1f} GFLOP algorithmic)"}
+    checks = {}
+    o3, l3 = outputs[3]
+    checks["3"] = _check_rows(w.name, o3.reshape(-1, w.d)[rows], l3.reshape(-1)[rows],
+                              o_ref, lse_ref, "bf16")
+    rng = np.random.default_rng(7)
+    for idx in (1, 2):
+        wi = wl.WORKLOADS[idx]
+        qi, ki, vi = inputs[idx]
+        oi, li = outputs[idx]
+        n_rows = wi.B * wi.Hq * wi.Sq
+        r = np.arange(n_rows) if n_rows <= 512 else rng.integers(0, n_rows, 512)
+        o_ref, lse_ref = oracle.attention(wl.to_oracle(qi), wl.to_oracle(ki), wl.to_oracle(vi),
+                                          wi.scale, wi.causal, rows=r)
+        checks[str(idx)] = _check_rows(wi.name, oi.reshape(-1, wi.d)[r], li.reshape(-1)[r],
+                                       o_ref, lse_ref, wi.dtype)
+    for idx in (4, 5):
+        wi = wl.WORKLOADS[idx]
+        qi, kc, vc, kl = inputs[idx]
+        oi, li = outputs[idx]
+        r = rng.choice(wi.B * wi.Hq, 96, replace=False)
+        o_ref, lse_ref = oracle.attention(wl.to_oracle(qi), wl.to_oracle(kc), wl.to_oracle(vc),
+                                          wi.scale, False, kv_len=kl.numpy(), rows=r)
+        checks[str(idx)] = _check_rows(wi.name, oi.reshape(-1, wi.d)[r], li.reshape(-1)[r],
+                                       o_ref, lse_ref, "bf16")
+    base["checked"] = checks
+    return base
 
 
 def run_reference(args, rank, world):
@@ -179,12 +264,12 @@ def run_reference(args, rank, world):
         oracle_sample_prefill(q_np, k_np, v_np, PREFILL, rows_per_step, 100 + s)
     tot_f, tot_t = 0.0, 0.0
     for s in range(args.steps):
-        f, t = oracle_sample_prefill(q_np, k_np, v_np, PREFILL, rows_per_step, 1000 + s)
+        f, t, _, _, _ = oracle_sample_prefill(q_np, k_np, v_np, PREFILL, rows_per_step, 1000 + s)
         tot_f += f
         tot_t += t
     val = tot_f / tot_t / 1e12
     line = {
-        "impl": "reference", "metric": "prefill attn TFLOP/s & decode KV GB/s at 1 GB300, % of roofline",
+        "impl": "reference", "metric": METRIC,
         "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -214,7 +299,8 @@ def config_dict(args):
                         "q_scale": PREFILL.q_scale},
             "decode": {"B": DECODE.B, "Hq": DECODE.Hq, "Hkv": DECODE.Hkv, "kv_len": DECODE.len_hi,
                        "d": DECODE.d, "num_splits": DECODE.num_splits},
-            "parallelism": f"replicas{args.gpus}", "l2": "flushed before each of the two calls of every step (512 MiB write, then read back)"}
+            "parallelism": f"replicas{args.gpus}",
+            "l2": "flushed before every timed call (512 MiB write, then read back)"}
 
 
 # ---------------------------------------------------------------------------------------
@@ -232,6 +318,7 @@ def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
 
     # inputs (seeded, CPU-generated), resident in HBM before timing
     q_c, k_c, v_c = wl.prefill_inputs(PREFILL)
@@ -246,20 +333,16 @@ def run_gpu(args, rank, world, local_rank):
                                                    DECODE.d, DECODE.num_splits),
                      dtype=torch.uint8, device=dev)
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
-    class _Flush:
-        """Evict L2: write a buffer 4x its size, then read it back so that no dirty
-        lines are left for the next timed kernel to write back."""
-
-        def zero_(self):
-            flush_buf.zero_()
-            flush_buf.sum()
-
-    flush = _Flush()
     stream = torch.cuda.current_stream(dev)
 
+    def flush():
+        """Evict L2: write a buffer 4x its size, then read it back so that no dirty lines
+        are left for the next timed kernel to write back."""
+        flush_buf.zero_()
+        flush_buf.sum()
+
     def step(evs=None):
-        flush.zero_()
+        flush()
         if evs is not None:
             evs[0].record(stream)
         gb.attn_fwd(q, k, v, causal=PREFILL.causal, scale=PREFILL.scale, out=o, lse=lse)
@@ -267,7 +350,7 @@ def run_gpu(args, rank, world, local_rank):
             evs[1].record(stream)
         # flush again: the prefill's dirty output lines would otherwise be written back
         # inside the decode window
-        flush.zero_()
+        flush()
         if evs is not None:
             evs[2].record(stream)
         gb.attn_decode_splitkv(dq, dk, dv, dl, num_splits=DECODE.num_splits,
@@ -275,12 +358,54 @@ def run_gpu(args, rank, world, local_rank):
         if evs is not None:
             evs[3].record(stream)
 
+    def time_calls(fn, reps):
+        """Mean CUDA-event time (ms) of `fn` over `reps` calls, L2 flushed before each."""
+        ms = []
+        for _ in range(reps):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms.append(e0.elapsed_time(e1))
+        return sum(ms) / len(ms)
+
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
     st, word = gb.attn_last_device_error()
     if st != 0:
         raise RuntimeError(f"device error word {word} during warm-up")
+
+    # the other three workloads, timed one call at a time (inputs resident, outputs kept
+    # for the oracle check)
+    extra_in, extra_out, extra_fn = {}, {}, {}
+    for idx in (1, 2):
+        wi = wl.WORKLOADS[idx]
+        qi, ki, vi = wl.prefill_inputs(wi)
+        extra_in[idx] = (qi, ki, vi)
+        gq, gk, gv = qi.to(dev), ki.to(dev), vi.to(dev)
+        go = torch.empty_like(gq)
+        gl = torch.empty(gq.shape[:3], dtype=torch.float32, device=dev)
+        extra_out[idx] = (go, gl)
+        extra_fn[idx] = (lambda gq=gq, gk=gk, gv=gv, go=go, gl=gl, wi=wi:
+                         gb.attn_fwd(gq, gk, gv, causal=wi.causal, scale=wi.scale, out=go, lse=gl))
+    w5 = wl.WORKLOADS[5]
+    q5, k5, v5, l5 = wl.decode_inputs(w5)
+    extra_in[5] = (q5, k5, v5, l5)
+    g5 = [t.to(dev) for t in (q5, k5, v5, l5)]
+    o5 = torch.empty_like(g5[0])
+    lse5 = torch.empty(g5[0].shape[:2], dtype=torch.float32, device=dev)
+    ws5 = torch.empty(gb.attn_decode_workspace_size(w5.B, w5.Hq, w5.Hkv, w5.Skv, w5.d, w5.num_splits),
+                      dtype=torch.uint8, device=dev)
+    extra_out[5] = (o5, lse5)
+    extra_fn[5] = lambda: gb.attn_decode_splitkv(*g5, num_splits=w5.num_splits, scale=w5.scale,
+                                                 out=o5, lse=lse5, workspace=ws5)
+    for idx in extra_fn:
+        for _ in range(3):
+            extra_fn[idx]()
+    torch.cuda.synchronize(dev)
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if world > 1:
@@ -292,14 +417,17 @@ def run_gpu(args, rank, world, local_rank):
             step(evs[s])
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall0
-    if world > 1:
-        torch.distributed.barrier()
+        if world > 1:
+            torch.distributed.barrier()
+        extra_ms = {idx: time_calls(extra_fn[idx], max(args.steps, 10)) for idx in (1, 2, 5)}
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
     dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
     pre_avg = sum(pre_ms) / len(pre_ms)
     dec_avg = sum(dec_ms) / len(dec_ms)
     step_ms = pre_avg + dec_avg
     pre_avg, dec_avg, step_ms = max_over_ranks([pre_avg, dec_avg, step_ms], dev)
+    for idx in extra_ms:
+        extra_ms[idx] = max_over_ranks([extra_ms[idx]], dev)[0]
 
     # chunked prefill against a KV cache (a widening beyond the step's two calls)
     chunk = None
@@ -310,16 +438,8 @@ def run_gpu(args, rank, world, local_rank):
         clse = torch.empty(cq.shape[:3], dtype=torch.float32, device=dev)
         for _ in range(3):
             gb.attn_prefill_kvcache(cq, ckc, cvc, cctx, causal=wc.causal, scale=wc.scale, out=co, lse=clse)
-        cms = []
-        for _ in range(10):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            gb.attn_prefill_kvcache(cq, ckc, cvc, cctx, causal=wc.causal, scale=wc.scale, out=co, lse=clse)
-            e1.record(stream)
-            torch.cuda.synchronize(dev)
-            cms.append(e0.elapsed_time(e1))
-        cm = max_over_ranks([sum(cms) / len(cms)], dev)[0]
+        cm = max_over_ranks([time_calls(lambda: gb.attn_prefill_kvcache(
+            cq, ckc, cvc, cctx, causal=wc.causal, scale=wc.scale, out=co, lse=clse), 10)], dev)[0]
         chunk = {"workload": wc.name, "ms": cm, "value": chunk_flops(wc) / (cm * 1e-3) / 1e12,
                  "unit": "TFLOP/s"}
         del cq, ckc, cvc, co, clse
@@ -334,20 +454,11 @@ def run_gpu(args, rank, world, local_rank):
         mlse = torch.empty(mq.shape[:3], dtype=torch.float32, device=dev)
         mws = torch.empty(gb.load_library().attn_decode_multitoken_workspace_size(
             wm.B, wm.Hq, wm.Hkv, wm.Sq, wm.Skv, wm.d, wm.num_splits), dtype=torch.uint8, device=dev)
+        run_m = lambda: gb.attn_decode_multitoken(mq, mkc, mvc, mkl, num_splits=wm.num_splits,
+                                                  scale=wm.scale, out=mo, lse=mlse, workspace=mws)
         for _ in range(3):
-            gb.attn_decode_multitoken(mq, mkc, mvc, mkl, num_splits=wm.num_splits, scale=wm.scale,
-                                      out=mo, lse=mlse, workspace=mws)
-        mms = []
-        for _ in range(10):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            gb.attn_decode_multitoken(mq, mkc, mvc, mkl, num_splits=wm.num_splits, scale=wm.scale,
-                                      out=mo, lse=mlse, workspace=mws)
-            e1.record(stream)
-            torch.cuda.synchronize(dev)
-            mms.append(e0.elapsed_time(e1))
-        mm = max_over_ranks([sum(mms) / len(mms)], dev)[0]
+            run_m()
+        mm = max_over_ranks([time_calls(run_m, 10)], dev)[0]
         mbytes = float(mkl_c.sum()) * wm.Hkv * wm.d * 2 * 2 + 2.0 * wm.B * wm.Hq * wm.Sq * wm.d * 2
         mtok = {"workload": wm.name, "ms": mm, "value": mbytes / (mm * 1e-3) / 1e9, "unit": "GB/s"}
         del mq, mkc, mvc, mkl, mo, mlse, mws
@@ -355,6 +466,13 @@ def run_gpu(args, rank, world, local_rank):
     st, word = gb.attn_last_device_error()
     if st != 0:
         raise RuntimeError(f"device error word {word} during the timed steps")
+
+    # outputs of the timed calls, for the oracle check (copied after timing)
+    outputs = {3: (o.float().cpu().numpy(), lse.cpu().numpy()),
+               4: (do.float().cpu().numpy(), dlse.cpu().numpy())}
+    for idx in (1, 2, 5):
+        outputs[idx] = (extra_out[idx][0].float().cpu().numpy(), extra_out[idx][1].cpu().numpy())
+    del g5, o5, lse5, ws5
 
     e2e_pre = e2e_dec = float("nan")
     h2d = d2h = 0
@@ -372,7 +490,7 @@ def run_gpu(args, rank, world, local_rank):
         d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdo, hdlse))
 
         def e2e_step(ev=None):
-            flush.zero_()
+            flush()
             if ev is not None:
                 ev[0].record(stream)
             # the C-ABI call on host buffers: inputs copied in, outputs copied back, the
@@ -391,13 +509,14 @@ def run_gpu(args, rank, world, local_rank):
 
         e2e_step()
         torch.cuda.synchronize(dev)
-        n_e2e = max(1, min(args.steps, 5))
+        n_e2e = args.steps
         evs2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_e2e)]
         for s in range(n_e2e):
             e2e_step(evs2[s])
         torch.cuda.synchronize(dev)
         e2e_pre = sum(e[0].elapsed_time(e[1]) for e in evs2) / n_e2e
         e2e_dec = sum(e[1].elapsed_time(e[2]) for e in evs2) / n_e2e
+        e2e_pre, e2e_dec = max_over_ranks([e2e_pre, e2e_dec], dev)
         ok = bool(torch.isfinite(ho.float()).all()) and bool(torch.isfinite(hdo.float()).all())
         if not ok:
             raise RuntimeError("non-finite output in the end-to-end run")
@@ -416,34 +535,73 @@ def run_gpu(args, rank, world, local_rank):
         chunk["frac"] = chunk["value"] / peak_tf      # per GPU
     if mtok is not None:
         mtok["frac"] = mtok["value"] / peak_bw         # per GPU
+    pre_plan = gb.attn_prefill_plan(PREFILL.B, PREFILL.Hq, PREFILL.Hkv, PREFILL.Sq, PREFILL.Skv,
+                                    PREFILL.causal, nsm)
+    dec_plan = gb.attn_decode_plan(DECODE.B, DECODE.Hq, DECODE.Hkv, 1, DECODE.Skv, DECODE.d,
+                                   DECODE.num_splits, nsm)
+    launches = (1 + (pre_plan["tail_pairs"] > 0)) + (1 + (dec_plan["merge"] == "combine"))
+    traffic_pre, traffic_pre_src = committed_traffic("prefill")
+    traffic_dec, traffic_dec_src = committed_traffic("decode")
+
+    def prefill_entry(idx, ms):
+        wi = wl.WORKLOADS[idx]
+        tf = prefill_flops(wi) / (ms * 1e-3) / 1e12
+        pl = gb.attn_prefill_plan(wi.B, wi.Hq, wi.Hkv, wi.Sq, wi.Skv, wi.causal, nsm)
+        e = {"workload": wi.name, "ms": ms, "value": tf, "unit": "TFLOP/s"}
+        if wi.dtype == "fp32":
+            e.update({"frac": None, "bound": "fp32 CUDA cores (correctness path, no roofline target)",
+                      "kernel": f"attn_fwd_f32_kernel<{wi.d}>"})
+        else:
+            e.update({"frac": tf / peak_tf, "bound": "tensor", "peak": peak_tf,
+                      "kernel": f"prefill_fwd_kernel<{wi.d}> ({pl['mode']})"})
+        return e
+
+    def decode_entry(w, lens, ms):
+        gbs = decode_bytes(w, lens) / (ms * 1e-3) / 1e9
+        pl = gb.attn_decode_plan(w.B, w.Hq, w.Hkv, 1, w.Skv, w.d, w.num_splits, nsm)
+        return {"workload": w.name, "ms": ms, "value": gbs, "unit": "GB/s", "frac": gbs / peak_bw,
+                "frac_of_nominal_7900": gbs / NOMINAL_HBM_GBS, "bound": "hbm", "peak": peak_bw,
+                "kernel": f"decode_split_kernel<{w.d}> ({pl['splits']} splits, {pl['merge']})"}
+
+    configs = {
+        "1": prefill_entry(1, extra_ms[1]),
+        "2": prefill_entry(2, extra_ms[2]),
+        "3": prefill_entry(3, pre_avg),
+        "4": decode_entry(DECODE, dl_c.tolist(), dec_avg),
+        "5": decode_entry(w5, l5.tolist(), extra_ms[5]),
+    }
     line = {
-        "metric": "prefill attn TFLOP/s & decode KV GB/s at 1 GB300, % of roofline",
+        "metric": METRIC,
         "value": pre_tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "wall_ms_per_step": t_wall / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config_dict(args),
         "roofline": {"bound": "tensor", "achieved": per_gpu_tf, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": per_gpu_tf / peak_tf,
-                     "traffic": NCU_TRAFFIC["prefill"], "kernel": "prefill_fwd_kernel<128, 0, 0> (pairs)",
+                     "traffic": traffic_pre, "traffic_source": traffic_pre_src,
+                     "kernel": f"prefill_fwd_kernel<128> ({pre_plan['mode']})",
                      "ms": pre_avg, "peak_source": f"{peak_src} bf16 burst"},
         "decode": {"value": dec_gbs, "unit": "GB/s", "ms": dec_avg,
                    "roofline": {"bound": "hbm", "achieved": per_gpu_bw, "peak": peak_bw,
                                 "unit": "GB/s", "frac": per_gpu_bw / peak_bw,
-                                "traffic": NCU_TRAFFIC["decode"],
-                                "kernel": "decode_split_kernel<128> + decode_combine_kernel<128> (PDL)",
+                                "traffic": traffic_dec, "traffic_source": traffic_dec_src,
+                                "kernel": configs["4"]["kernel"] + " + decode_combine_kernel (PDL)",
                                 "peak_source": f"{peak_src} HBM copy"}},
+        "configs": configs,
         "e2e": {"value": (flops / (e2e_pre * 1e-3) / 1e12 * world) if not args.no_e2e else None,
                 "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "decode_gbs": (dbytes / (e2e_dec * 1e-3) / 1e9 * world) if not args.no_e2e else None,
-                "ms_per_step": e2e_pre + e2e_dec},
-        "gpu_launches": 3 * args.steps,
+                "ms_per_step": e2e_pre + e2e_dec, "steps": args.steps},
+        "gpu_launches": launches * args.steps,
         "chunked_prefill": chunk,
         "multitoken_decode": mtok,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_prefill(q_c, k_c, v_c, PREFILL)
+        inputs = {3: (q_c, k_c, v_c), 4: (dq_c, dk_c, dv_c, dl_c)}
+        inputs.update(extra_in)
+        line["cpu_baseline"] = cpu_baseline_and_check(inputs, outputs)
     print(json.dumps(line), flush=True)
 
 
@@ -453,17 +611,12 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gbattn", "reference"], default="gbattn")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle leg (its timing and the check of the outputs)")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-chunk", action="store_true", help="skip the chunked-prefill measurement")
-    ap.add_argument("--prefill", type=int, default=3, help="prefill workload index (1-3)")
-    ap.add_argument("--decode", type=int, default=4, help="decode workload index (4-5)")
+    ap.add_argument("--no-chunk", action="store_true",
+                    help="skip the chunked-prefill and multi-token measurements")
     args = ap.parse_args()
-    global PREFILL, DECODE
-    PREFILL = wl.WORKLOADS[args.prefill]
-    DECODE = wl.WORKLOADS[args.decode]
-    if PREFILL.kind != "prefill" or DECODE.kind != "decode":
-        ap.error("--prefill takes a prefill workload, --decode a decode workload")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

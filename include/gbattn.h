@@ -88,6 +88,26 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              void* stream);
 
 /*
+ * attn_fwd_counted -- attn_fwd (bf16 only) that also reports the work it issued, so that
+ * the causal tile skipping can be checked: "ADR-0060" section 11 asks that a causal
+ * prefill skip every KV tile wholly in a query tile's future, so that the number of
+ * S = Q K^T tile products equals the lower-triangular count, not the full grid.
+ *
+ *   s_tiles  DEVICE int, 4-byte aligned, owned by the caller: the kernels ADD to it the
+ *            number of 128-query x 128-key S tile products they issued (one atomic per
+ *            CTA); the caller zeroes it first.  The expected value for a call is
+ *            sum over 128-row Q tiles of ceil(visible keys of the tile's last row / 128),
+ *            where a row i sees min(Skv, i + Skv - Sq + 1) keys (causal) or Skv keys.
+ *
+ * Same arguments, numerics, output and status codes as attn_fwd with dtype GBATTN_BF16,
+ * plus GBATTN_ERR_INVALID_ARG for a NULL s_tiles.  The counter adds one atomic per CTA;
+ * attn_fwd passes no counter and skips it.
+ */
+int attn_fwd_counted(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int Hq, int Hkv, int Sq, int Skv, int d, float scale, int causal,
+                     int* s_tiles, void* stream);
+
+/*
  * attn_fwd_host_workspace_size -- device bytes attn_fwd_host needs for these sizes on the
  * current device (two staging buffer sets); 0 for invalid sizes.
  */
@@ -140,16 +160,28 @@ int attn_prefill_kvcache(const void* q, const void* kcache, const void* vcache, 
                          float scale, int causal, void* stream);
 
 /*
- * attn_decode_workspace_size -- bytes of device workspace attn_decode_splitkv needs.
- * Holds the per-split partial results (lse_s and O_s / l_s, fp32), a work counter and
- * one finished-split counter per (sequence, KV head); the counters are cleared on the
- * call's stream at the start of every call, so the caller need not initialise anything.
- * num_splits > 0: fixed split count; 0: automatic: one split per 4096 keys of a sequence,
- * raised for calls with few (sequence, KV head) groups to the most splits that still fit
- * one wave of 152 work items (the SM count of a GB300), but never below 256 keys per split.
- * Returns 0 for invalid arguments.
+ * attn_decode_workspace_size -- bytes of device workspace attn_decode_splitkv needs on the
+ * CURRENT device.  Holds the per-split partial results (lse_s and O_s / l_s, fp32), a work
+ * counter and one finished-split counter per (sequence, KV head); the counters are cleared
+ * on the call's stream at the start of every call, so the caller need not initialise
+ * anything.  num_splits > 0: fixed split count; 0: automatic: one split per 4096 keys of a
+ * sequence, raised for calls with few (sequence, KV head) groups to the most splits that
+ * still fit one wave of work items -- one per SM of the device, so the size depends on the
+ * device's SM count (queried here) -- but never below 256 keys per split.  A workspace
+ * sized on one device serves calls on devices with the same SM count.
+ * Returns 0 for invalid arguments, or when no CUDA device can be queried (use
+ * attn_decode_workspace_bytes to size for a given SM count without a device).
  */
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int num_splits);
+
+/*
+ * attn_decode_workspace_bytes -- the workspace of a decode call with Tq new tokens per
+ * sequence (Tq = 1: attn_decode_splitkv) on a GPU with num_sms SMs.  Host only: no device
+ * access.  attn_decode_workspace_size and attn_decode_multitoken_workspace_size are this
+ * function with the current device's SM count.  Returns 0 for invalid arguments.
+ */
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Tq, int Lmax, int d,
+                                   int num_splits, int num_sms);
 
 /*
  * attn_decode_splitkv -- single-token (T_q = 1) decode against a KV cache, split-KV with a
@@ -206,6 +238,7 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
  *   o       [B, Hq, Tq, d]      device, bf16    output (written)
  *   lse     [B, Hq, Tq]         device, fp32    log-sum-exp (written); may be NULL
  *   workspace, ws_bytes                         >= attn_decode_multitoken_workspace_size(...)
+ *                                               (sized for the current device's SM count)
  *
  * New token t (0-based) sees keys j <= len - Tq + t (causal among the new tokens; every
  * older key).  A row that sees no key (len < Tq) gets O = 0, LSE = -inf.  Requirements
@@ -231,7 +264,10 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
  *  - Sizes whose attn_decode_workspace_size(...) exceeds 8 MiB (8388608 bytes) are
  *    rejected with GBATTN_ERR_WORKSPACE before anything is launched.
  *  - The first call on a device looks up the array's device address for that device;
- *    make that first call before any stream capture starts.
+ *    make that first call before any stream capture starts.  If that lookup fails (for
+ *    example because the first call was made while a stream was being captured) the call
+ *    returns GBATTN_ERR_CUDA, launches nothing and clears the CUDA error it caused; a
+ *    later call outside capture repeats the lookup.
  *  - Every call shares the one array: calls whose GPU work may overlap (different
  *    streams, or unordered host threads) race and give wrong results.  The counters
  *    that must start at zero are cleared on `stream` by each call.

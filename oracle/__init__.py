@@ -256,11 +256,6 @@ def split_bounds(length: int, num_splits: int, align: int = 64):
     return [(min(s * c, length), min((s + 1) * c, length)) for s in range(num_splits)]
 
 
-def auto_num_splits(length: int, chunk: int = 4096, max_splits: int = 256) -> int:
-    """Split count for the automatic decode mode: one split per `chunk` keys (>= 1)."""
-    return max(1, min(max_splits, -(-length // chunk)))
-
-
 def splitkv_decode(q, k, v, scale: float, num_splits: int, tile: int = 64, align: int = 64):
     """Split-KV decode for one KV head group ([ADR-0060] s.4 and s.5.2).
 

@@ -7,6 +7,7 @@ or was not built for this machine, loading raises.
 
 Entry points (same names as the C ABI in include/gbattn.h):
   attn_fwd(q, k, v, causal, scale=None, out=None, lse=None)
+  attn_fwd_counted(q, k, v, causal, s_tiles, ...)   attn_fwd plus the S tile products issued
   attn_decode_splitkv(q, kcache, vcache, kv_lens, num_splits=0, scale=None, ...)
   attn_decode_workspace_size(B, Hq, Hkv, Lmax, d, num_splits)
   attn_last_device_error(stream=None)
@@ -39,10 +40,12 @@ _F = ctypes.c_float
 _SZ = ctypes.c_size_t
 EXPORTS = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "attn_fwd_counted": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P]),
     "attn_fwd_host_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "attn_prefill_kvcache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "attn_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "attn_decode_multitoken_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "attn_decode_multitoken": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
@@ -146,6 +149,33 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool,
     return out, lse
 
 
+def attn_fwd_counted(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool,
+                     s_tiles: torch.Tensor, scale: float | None = None,
+                     out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                     stream=None):
+    """attn_fwd (bf16) that also adds the S = Q K^T tile products its kernels issued to
+    s_tiles (an int32 CUDA tensor of one element, zeroed by the caller).  Returns (out, lse)."""
+    lib = load_library()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _dev_tensor(n, t, (torch.bfloat16,))
+    _dev_tensor("s_tiles", s_tiles, (torch.int32,))
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("expected q [B,Hq,Sq,d] and k, v [B,Hkv,Skv,d]")
+    B, Hq, Sq, d = q.shape
+    _, Hkv, Skv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    st = lib.attn_fwd_counted(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr(), B, Hq, Hkv, Sq, Skv, d, float(scale),
+                              1 if causal else 0, s_tiles.data_ptr(), _stream_ptr(stream))
+    _check("attn_fwd_counted", st)
+    return out, lse
+
+
 def _host_tensor(name: str, t: torch.Tensor, dtypes):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -238,7 +268,16 @@ def attn_prefill_kvcache(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Te
 
 def attn_decode_workspace_size(B: int, Hq: int, Hkv: int, Lmax: int, d: int,
                                num_splits: int = 0) -> int:
+    """Workspace bytes of attn_decode_splitkv on the current device (0: invalid, or no
+    device to query)."""
     return int(load_library().attn_decode_workspace_size(B, Hq, Hkv, Lmax, d, num_splits))
+
+
+def attn_decode_workspace_bytes(B: int, Hq: int, Hkv: int, Tq: int, Lmax: int, d: int,
+                                num_splits: int, num_sms: int) -> int:
+    """Workspace bytes of a decode call on a GPU with num_sms SMs (host only)."""
+    return int(load_library().attn_decode_workspace_bytes(B, Hq, Hkv, Tq, Lmax, d, num_splits,
+                                                          num_sms))
 
 
 def attn_decode_splitkv(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,

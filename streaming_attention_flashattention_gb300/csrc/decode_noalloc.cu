@@ -44,7 +44,12 @@ void* scratch_for_current_device() {
     std::lock_guard<std::mutex> lock(mu);
     if (addr[dev] == nullptr) {
         void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) {
+            // the lookup's error is not sticky: clear it so that the caller's next
+            // cudaGetLastError() does not report it a second time
+            (void)cudaGetLastError();
+            return nullptr;
+        }
         addr[dev] = ptr;
     }
     return addr[dev];

@@ -29,7 +29,7 @@ __device__ __forceinline__ int nonempty_splits(int len, int n) {
 }
 
 // Splits of a sequence of len keys.  Automatic mode: one per kAutoChunk keys, raised to
-// auto_floor (the count that gives the call about kAutoItems work items, chosen on the host)
+// auto_floor (the count that gives the call about one work item per SM, chosen on the host)
 // as long as each split keeps kAutoMinKeys keys.  Non-decreasing in len, so the host sizes
 // the workspace with len = Lmax.
 __host__ __device__ __forceinline__ int splits_for(int len, int fixed_splits, int auto_floor) {

@@ -141,9 +141,10 @@ PrefillPlan prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, in
 }
 
 // bf16 tcgen05 prefill; K/V rows of one head are `kv_stride` rows apart (>= Skv).
+// tiles: null, or a device counter that receives the S tile products the kernels issue.
 int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int Hq, int Hkv, int Sq, int Skv, int kv_stride, int d, float scale,
-                        int causal, cudaStream_t st) {
+                        int causal, cudaStream_t st, int* tiles = nullptr) {
     PrefillParams p{};
     if (!make_map_bf16_3d(&p.tmap_q, q, d, Sq, (uint64_t)B * Hq, 128) ||
         !make_map_bf16_3d(&p.tmap_k, k, d, Skv, (uint64_t)B * Hkv, 128, kv_stride) ||
@@ -166,6 +167,7 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, fl
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = device_error_word();
     if (!p.err) return GBATTN_ERR_CUDA;
+    p.tiles_issued = tiles;
     cudaError_t e = launch_attn_fwd_bf16(p, d, st);
     if (e == cudaSuccess && pl.tail > 0) {
         PrefillParams t = p;
@@ -261,12 +263,12 @@ DecodeRows decode_rows(int Hq, int Hkv, int Tq) {
 }
 
 // Automatic split mode: the most splits per sequence that keep the call within one wave of
-// kAutoItems work items.  A work item is one split of one (sequence, KV head) and one row
-// group: a 128-row tile on the tensor-core path (R >= 16), a chunk group on the warp-level
-// path.  Never below one.
-int auto_floor(int B, int Hkv, const DecodeRows& dr) {
+// work items on a GPU with nsm SMs (one persistent CTA per SM).  A work item is one split
+// of one (sequence, KV head) and one row group: a 128-row tile on the tensor-core path
+// (R >= 16), a chunk group on the warp-level path.  Never below one.
+int auto_floor(int B, int Hkv, const DecodeRows& dr, int nsm) {
     const long long per_split = (long long)B * Hkv * (dr.R >= 16 ? (dr.R + 127) / 128 : dr.n_hg);
-    const long long f = kAutoItems / per_split;
+    const long long f = nsm / per_split;
     return (int)(f < 1 ? 1 : (f > kMaxSplits ? kMaxSplits : f));
 }
 
@@ -286,7 +288,7 @@ struct DecodePlan {
 DecodePlan decode_plan(int B, int Hq, int Hkv, int Tq, int Lmax, int num_splits, int nsm) {
     DecodePlan pl{};
     pl.dr = decode_rows(Hq, Hkv, Tq);
-    pl.floor_splits = auto_floor(B, Hkv, pl.dr);
+    pl.floor_splits = auto_floor(B, Hkv, pl.dr, nsm);
     pl.n_slots = decode_slots(Lmax, num_splits, pl.floor_splits);
     pl.n_items = (long long)pl.n_slots * B * Hkv * pl.dr.n_hg;
     // tcgen05 path: 16 or more query rows per KV head (several new tokens, or G >= 16), or 9
@@ -334,6 +336,30 @@ const char* attn_status_string(int status) {
         case GBATTN_ERR_TOO_LARGE: return "size exceeds kernel indexing range";
         default: return "unknown status";
     }
+}
+
+int attn_fwd_counted(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int Hq, int Hkv, int Sq, int Skv, int d, float scale, int causal,
+                     int* s_tiles, void* stream) {
+    if (!s_tiles) return GBATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(s_tiles) & 3u) return GBATTN_ERR_MISALIGNED;
+    // the same checks as attn_fwd (bf16)
+    if (!q || !k || !v || !o) return GBATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || d <= 0)
+        return GBATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return GBATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || scale != scale) return GBATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return GBATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return GBATTN_ERR_UNSUPPORTED;
+    if (causal && Sq > Skv) return GBATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (lse && !aligned16(lse)))
+        return GBATTN_ERR_MISALIGNED;
+    if ((long long)B * Hq > 65535LL * 65535LL || (long long)B * Hq * Sq > kIntMax ||
+        (long long)B * Hkv * Skv > kIntMax)
+        return GBATTN_ERR_TOO_LARGE;
+    return launch_prefill_bf16(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, Skv, d, scale, causal,
+                               static_cast<cudaStream_t>(stream), s_tiles);
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
@@ -469,19 +495,26 @@ int attn_prefill_kvcache(const void* q, const void* kcache, const void* vcache, 
                                causal, static_cast<cudaStream_t>(stream));
 }
 
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Tq, int Lmax, int d,
+                                   int num_splits, int num_sms) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Tq <= 0 || Lmax <= 0 || (d != 64 && d != 128)) return 0;
+    if (num_splits < 0 || num_splits > kMaxSplits || num_sms <= 0) return 0;
+    if (Hq % Hkv != 0) return 0;
+    if ((long long)B * Hq * Tq > kIntMax) return 0;
+    const DecodeRows dr = decode_rows(Hq, Hkv, Tq);
+    return decode_workspace_bytes(B * Tq, Hq, B * Hkv, dr.n_hg, d,
+                                  decode_slots(Lmax, num_splits, auto_floor(B, Hkv, dr, num_sms)));
+}
+
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int num_splits) {
     return attn_decode_multitoken_workspace_size(B, Hq, Hkv, 1, Lmax, d, num_splits);
 }
 
 size_t attn_decode_multitoken_workspace_size(int B, int Hq, int Hkv, int Tq, int Lmax, int d,
                                              int num_splits) {
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Tq <= 0 || Lmax <= 0 || (d != 64 && d != 128)) return 0;
-    if (num_splits < 0 || num_splits > kMaxSplits) return 0;
-    if (Hq % Hkv != 0) return 0;
-    if ((long long)B * Hq * Tq > kIntMax) return 0;
-    const DecodeRows dr = decode_rows(Hq, Hkv, Tq);
-    return decode_workspace_bytes(B * Tq, Hq, B * Hkv, dr.n_hg, d,
-                                  decode_slots(Lmax, num_splits, auto_floor(B, Hkv, dr)));
+    const int nsm = sm_count();
+    if (nsm <= 0) return 0;
+    return attn_decode_workspace_bytes(B, Hq, Hkv, Tq, Lmax, d, num_splits, nsm);
 }
 
 int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache,
@@ -500,13 +533,13 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
         (lse && !aligned16(lse)) || (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
         return GBATTN_ERR_MISALIGNED;
     if ((long long)B * Hq * Tq > kIntMax / 8) return GBATTN_ERR_TOO_LARGE;
+    const int nsm = sm_count();
+    if (nsm <= 0) return GBATTN_ERR_CUDA;
     const DecodeRows dr = decode_rows(Hq, Hkv, Tq);
-    const int n_slots = decode_slots(Lmax, num_splits, auto_floor(B, Hkv, dr));
+    const int n_slots = decode_slots(Lmax, num_splits, auto_floor(B, Hkv, dr, nsm));
     const size_t need = decode_workspace_bytes(B * Tq, Hq, B * Hkv, dr.n_hg, d, n_slots);
     if (!workspace || ws_bytes < need) return GBATTN_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GBATTN_ERR_MISALIGNED;
-    const int nsm = sm_count();
-    if (nsm <= 0) return GBATTN_ERR_CUDA;
     const DecodePlan pl = decode_plan(B, Hq, Hkv, Tq, Lmax, num_splits, nsm);
     const int G = Hq / Hkv;
     const int R = dr.R, n_hc = dr.n_hc, nci = dr.nci, n_hg = dr.n_hg;

@@ -35,6 +35,8 @@ struct PrefillParams {
     int o_align32;        // o is 32-byte aligned: the epilogue may use 32-byte stores
     float scale_log2;     // scale * log2(e)
     int* err;             // device error word of bounded waits
+    int* tiles_issued;    // null, or a device counter the MMA issuer adds its S = Q K^T
+                          // tile products to (one atomic per CTA at its end)
 };
 cudaError_t launch_attn_fwd_bf16(const PrefillParams& p, int d, cudaStream_t stream);
 // The Q tiles of pairs [p.tail0, p.tail0 + p.n_pairs / 2) in KV-split mode, launched as a
@@ -69,10 +71,10 @@ struct DecodeParams {
     int* err;             // device error word of bounded waits
 };
 // Split-count rule of the automatic mode: one split per kAutoChunk keys, raised for calls
-// with few (sequence, KV head) groups to as many splits as still fit one wave of kAutoItems
-// work items (the SM count of a GB300), but never to fewer than kAutoMinKeys keys per split.
+// with few (sequence, KV head) groups to as many splits as still fit one wave of work items
+// (one per SM of the device; the host passes the resulting count as auto_floor), but never
+// to fewer than kAutoMinKeys keys per split.
 constexpr int kAutoChunk = 4096;
-constexpr int kAutoItems = 152;
 constexpr int kAutoMinKeys = 256;
 constexpr int kMaxSplits = 256;
 constexpr int kSplitAlign = 64;

@@ -282,8 +282,10 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
             const uint64_t dk1 = make_sdesc_sw128(smem_u32(k_slot(1)), 16, 1024);
             const uint64_t dk2 = make_sdesc_sw128(smem_u32(k_slot(KS - 1)), 16, 1024);
 
+            int n_s = 0;       // S tile products issued (reported through p.tiles_issued)
             // S_t = Q K^T with the K tile of fill f (Q buffer t for pairs, 0 with KV split)
             auto issue_s = [&](int t, uint32_t f) {
+                ++n_s;
                 const uint64_t a0 = (kSplit || t == 0) ? dq0 : dq1;
                 const uint32_t ks = f % KS;
                 const uint64_t b0 = ks == 0 ? dk0 : (ks == 1 ? dk1 : dk2);
@@ -376,6 +378,7 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
                     }
                 }
             }
+            if (p.tiles_issued != nullptr) atomicAdd(p.tiles_issued, n_s);
         }
     } else if (warp >= kSoftmaxWarp0) {
         // =============================== softmax warps ================================

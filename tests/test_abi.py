@@ -95,12 +95,29 @@ def test_decode_argument_validation(lib):
     assert dec(lib, d=80) == -2
     assert dec(lib, q=MIS) == -3
     assert dec(lib, lens=0x10002) == -3
-    assert dec(lib, ws=None) == -6
-    assert dec(lib, wsb=16) == -6
+    # the workspace check sizes for the current device's SM count: without a device the
+    # call stops there with GBATTN_ERR_CUDA, with one it rejects the missing or short
+    # workspace -- before anything is launched either way
+    import torch
+    want = -6 if torch.cuda.is_available() else -4
+    assert dec(lib, ws=None, wsb=0) == want
+    assert dec(lib, wsb=16) == want
+
+
+def test_counted_prefill_argument_checks(lib):
+    f = lib.attn_fwd_counted
+    cnt = 0x30000
+    assert f(A, A, A, B_, None, 1, 2, 1, 128, 128, 128, 0.1, 1, None, None) == -1   # no counter
+    assert f(A, A, A, B_, None, 1, 2, 1, 128, 128, 128, 0.1, 1, 0x30002, None) == -3  # misaligned
+    assert f(None, A, A, B_, None, 1, 2, 1, 128, 128, 128, 0.1, 1, cnt, None) == -1
+    assert f(A, A, A, B_, None, 1, 2, 1, 128, 128, 96, 0.1, 1, cnt, None) == -2     # d
+    assert f(A, A, A, B_, None, 1, 2, 1, 256, 128, 128, 0.1, 1, cnt, None) == -2   # causal Sq > Skv
+    assert f(A, A, A, B_, None, 1, 3, 2, 128, 128, 128, 0.1, 0, cnt, None) == -1    # Hq % Hkv
 
 
 def test_workspace_size(lib):
-    ws = gb.attn_decode_workspace_size
+    def ws(B, Hq, Hkv, L, d, ns, nsm=152):
+        return gb.attn_decode_workspace_bytes(B, Hq, Hkv, 1, L, d, ns, nsm)
 
     def expect(B, Hq, Hkv, slots, d):
         # counters (the work queue, then one finished-split counter per (b, KV head, chunk
@@ -125,6 +142,23 @@ def test_workspace_size(lib):
     assert ws(0, 64, 8, 10, 128, 0) == 0
     assert ws(1, 64, 8, 10, 96, 0) == 0
     assert ws(1, 64, 8, 10, 128, 300) == 0
+    assert ws(1, 64, 8, 10, 128, 0, nsm=0) == 0
+    # the automatic floor follows the SM count: 76 SMs give 76 // 8 = 9 splits for 8 groups
+    # (16384 keys: one split per 4096 keys would give 4)
+    assert ws(1, 64, 8, 16384, 128, 0, nsm=76) == expect(1, 64, 8, 9, 128)
+    assert ws(1, 64, 8, 16384, 128, 0, nsm=304) == expect(1, 64, 8, 38, 128)
+    # fixed split counts do not depend on it
+    assert ws(4, 64, 8, 32768, 128, 16, nsm=76) == ws(4, 64, 8, 32768, 128, 16)
+
+
+def test_current_device_workspace_size_needs_a_device(lib):
+    import torch
+    n = gb.attn_decode_workspace_size(4, 64, 8, 32768, 128, 16)
+    if torch.cuda.is_available():
+        nsm = torch.cuda.get_device_properties(0).multi_processor_count
+        assert n == gb.attn_decode_workspace_bytes(4, 64, 8, 1, 32768, 128, 16, nsm)
+    else:
+        assert n == 0
 
 
 def test_profile_case_driver_parses_without_gpu():

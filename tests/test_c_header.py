@@ -24,8 +24,9 @@ typedef void (*any_fn)(void);
 int main(void) {
     /* every entry point is a C symbol the program can take the address of */
     any_fn fns[] = {
-        (any_fn)attn_fwd, (any_fn)attn_fwd_host_workspace_size, (any_fn)attn_fwd_host,
+        (any_fn)attn_fwd, (any_fn)attn_fwd_counted, (any_fn)attn_fwd_host_workspace_size, (any_fn)attn_fwd_host,
         (any_fn)attn_prefill_kvcache, (any_fn)attn_decode_workspace_size,
+        (any_fn)attn_decode_workspace_bytes,
         (any_fn)attn_decode_splitkv, (any_fn)attn_decode_multitoken_workspace_size,
         (any_fn)attn_decode_multitoken, (any_fn)attn_decode_splitkv_noalloc,
         (any_fn)attn_decode_plan, (any_fn)attn_prefill_plan, (any_fn)attn_last_device_error,
@@ -35,7 +36,7 @@ int main(void) {
     if (attn_version() < 100) return 11;
     if (strcmp(attn_status_string(GBATTN_OK), "ok") != 0) return 12;
     /* host-only queries */
-    if (attn_decode_workspace_size(4, 64, 8, 32768, 128, 16) == 0) return 13;
+    if (attn_decode_workspace_bytes(4, 64, 8, 1, 32768, 128, 16, 152) == 0) return 13;
     int plan[6];
     if (attn_decode_plan(4, 64, 8, 1, 32768, 128, 16, 152, plan) != GBATTN_OK) return 14;
     if (plan[0] != 16 || plan[1] != 0 || plan[3] != 512) return 15;
@@ -45,6 +46,8 @@ int main(void) {
     /* argument checks come before any device work */
     if (attn_fwd(0, 0, 0, 0, 0, 1, 2, 1, 128, 128, 128, 0.1f, 0, GBATTN_BF16, 0)
         != GBATTN_ERR_INVALID_ARG) return 18;
+    if (attn_fwd_counted((void*)0x10000, (void*)0x10000, (void*)0x10000, (void*)0x20000, 0, 1, 2,
+                         1, 128, 128, 128, 0.1f, 0, 0, 0) != GBATTN_ERR_INVALID_ARG) return 19;
     printf("c abi ok\n");
     return 0;
 }

@@ -1,7 +1,6 @@
 """GPU parity of attn_decode_splitkv against the fp64 oracle (plain definition with
 kv_len); the cache rows past each sequence's length hold NaN, so any read of them that
 reaches the output fails the test."""
-import numpy as np
 import pytest
 import torch
 
@@ -23,7 +22,7 @@ def _built():
     assert st == 0 and word == 0, f"device error word set: {word}"
 
 
-def run_decode(w: wl.Workload, lens=None, rows_per_seq=None):
+def run_decode(w: wl.Workload, lens=None):
     q, kc, vc, kl = wl.decode_inputs(w)
     if lens is not None:
         kl = torch.tensor(lens, dtype=torch.int32)
@@ -35,17 +34,9 @@ def run_decode(w: wl.Workload, lens=None, rows_per_seq=None):
     torch.cuda.synchronize()
     o = o.float().cpu().numpy()[:, :, 0]
     lse = lse.cpu().numpy()
-    if rows_per_seq is None:
-        o_ref, lse_ref = oracle.attention(wl.to_oracle(q), wl.to_oracle(kc), wl.to_oracle(vc),
-                                          w.scale, False, kv_len=kl.numpy())
-        return compare(o, lse, o_ref[:, :, 0], lse_ref[:, :, 0], w.dtype, w.name)
-    rng = np.random.default_rng(0)
-    heads = np.stack([np.sort(rng.choice(w.Hq, rows_per_seq, replace=False)) for _ in range(w.B)])
-    rows = (np.arange(w.B)[:, None] * w.Hq + heads).reshape(-1)
     o_ref, lse_ref = oracle.attention(wl.to_oracle(q), wl.to_oracle(kc), wl.to_oracle(vc),
-                                      w.scale, False, kv_len=kl.numpy(), rows=rows)
-    return compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, w.dtype,
-                   w.name)
+                                      w.scale, False, kv_len=kl.numpy())
+    return compare(o, lse, o_ref[:, :, 0], lse_ref[:, :, 0], w.dtype, w.name)
 
 
 def small(B, Hq, Hkv, Lmax, d, num_splits, lo, hi, seed=3):
@@ -76,8 +67,9 @@ def test_workload4_llama70b_decode_full():
 
 
 @pytest.mark.slow
-def test_workload5_ragged_decode_sampled():
-    run_decode(wl.WORKLOADS[5], rows_per_seq=4)
+def test_workload5_ragged_decode_all_rows():
+    # every one of the 16 x 64 output rows against the oracle (lengths 1024 to 131072)
+    run_decode(wl.WORKLOADS[5])
 
 
 def test_decode_deterministic_repeat():

@@ -104,15 +104,19 @@ def test_workload2_causal_gqa_prefill_full():
 
 
 @pytest.mark.slow
-def test_workload3_llama70b_prefill_sampled_rows():
+def test_workload3_llama70b_prefill_100k_rows():
+    # 100,000 random rows, every row of one whole query head (all 64 Q tiles, the diagonal
+    # tile of each), the first Q tile of head 0 and the last rows of the last head
     w = wl.WORKLOADS[3]
     rng = np.random.default_rng(3)
     n_rows = w.B * w.Hq * w.Sq
     rows = np.unique(np.concatenate([
-        rng.integers(0, n_rows, 1500),
+        rng.choice(n_rows, 100_000, replace=False),
+        37 * w.Sq + np.arange(w.Sq),                         # head 37, all 8192 rows
         np.arange(0, 128),                                   # head 0, first tile (diagonal)
         (w.Hq - 1) * w.Sq + np.arange(w.Sq - 130, w.Sq),     # last head, last rows
     ]))
+    assert rows.size >= 100_000
     check(w, rows=rows)
 
 

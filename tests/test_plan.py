@@ -134,7 +134,7 @@ def test_plan_agrees_with_workspace_size_and_invariants():
         n_hg = (n_hc + nci - 1) // nci
         counters = ((1 + B * Hkv * n_hg) * 4 + 255) // 256 * 256
         expect = counters + (rows * 4 + 255) // 256 * 256 + rows * d * 4
-        assert gb.load_library().attn_decode_multitoken_workspace_size(B, G * Hkv, Hkv, Tq, L, d, ns) == expect
+        assert gb.attn_decode_workspace_bytes(B, G * Hkv, Hkv, Tq, L, d, ns, NSM) == expect
         assert 1 <= p["splits"] <= 256 and (ns == 0 or p["splits"] == ns)
         per_split = B * Hkv * ((G * Tq + 127) // 128 if p["kernel"] == "tcgen05" else n_hg)
         assert p["items"] == p["splits"] * per_split
