@@ -75,8 +75,9 @@ enum {
  * causal requires Sq <= Skv; all pointers 16-byte aligned.
  * Tile classes follow "ADR-0060" section 5.4: KV tiles entirely in a query tile's future
  * are skipped, tiles crossing the diagonal are masked, the rest run unmasked.
- * bf16 work items are pairs of Q tiles (one CTA each), or single Q tiles with their KV range
- * split over a CTA's two slots when pairs would not fill the GPU twice over.  When the pairs
+ * bf16 work items are pairs of Q tiles (one CTA each), or -- when pairs would not fill the
+ * GPU twice over -- single Q tiles with their KV range split over a CTA's two slots, run by
+ * at most one persistent CTA per SM that takes its tiles heaviest first.  When the pairs
  * weigh nearly the same (non-causal calls, or a chunk at the end of a long context) and
  * their last wave is at most half full, that wave's Q tiles run split in a second launch,
  * a programmatic dependent of the first that ends after it.  Stream order and CUDA graph
@@ -296,8 +297,9 @@ int attn_decode_plan(int B, int Hq, int Hkv, int Tq, int Lmax, int d, int num_sp
 /*
  * attn_prefill_plan -- the work split attn_fwd (bf16) and attn_prefill_kvcache choose for
  * these sizes on a GPU with num_sms SMs.  Host only.  plan (host, 4 ints) receives:
- *   plan[0]  mode of the first launch: 0 pairs of Q tiles per CTA, 1 one Q tile per CTA with
- *            its KV range split over the CTA's two slots
+ *   plan[0]  mode of the first launch: 0 pairs of Q tiles per CTA, 1 single Q tiles with
+ *            their KV range split over a CTA's two slots, on persistent CTAs (at most one
+ *            per SM) that take the tiles heaviest first
  *   plan[1]  CTAs of the first launch
  *   plan[2]  pairs whose Q tiles run KV-split in a second, dependent launch (0: none)
  *   plan[3]  Q tiles in all

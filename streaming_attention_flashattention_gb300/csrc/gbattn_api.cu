@@ -117,7 +117,8 @@ PrefillPlan prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, in
     pl.n_tiles = (long long)pl.n_qblk * B * Hq;
     // Pairs of Q tiles keep both ping-pong slots busy with independent work; when they
     // would not fill the SMs twice over, splitting each tile's KV range over the two slots
-    // halves the longest item instead.
+    // halves the longest item instead, and the tiles run on persistent CTAs (one per SM,
+    // heaviest tiles dealt first) so that each SM pays the start-up once.
     pl.kv_split = pl.n_pairs < 2LL * nsm;
     // Pairs of nearly equal weight (non-causal, or a chunk at the end of a long context)
     // whose last wave is at most half full: those last pairs run as single Q tiles in
@@ -136,7 +137,7 @@ PrefillPlan prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, in
         const long long rem = pl.n_pairs % nsm;
         if (lo > 0 && 4 * hi <= 5 * lo && rem > 0 && rem <= nsm / 2) pl.tail = rem;
     }
-    pl.first = pl.kv_split ? pl.n_tiles : pl.n_pairs - pl.tail;
+    pl.first = pl.kv_split ? std::min<long long>(pl.n_tiles, nsm) : pl.n_pairs - pl.tail;
     return pl;
 }
 
@@ -148,7 +149,8 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, fl
     PrefillParams p{};
     if (!make_map_bf16_3d(&p.tmap_q, q, d, Sq, (uint64_t)B * Hq, 128) ||
         !make_map_bf16_3d(&p.tmap_k, k, d, Skv, (uint64_t)B * Hkv, 128, kv_stride) ||
-        !make_map_bf16_3d(&p.tmap_v, v, d, Skv, (uint64_t)B * Hkv, 128, kv_stride))
+        !make_map_bf16_3d(&p.tmap_v, v, d, Skv, (uint64_t)B * Hkv, 128, kv_stride) ||
+        !make_map_bf16_3d(&p.tmap_o, o, d, Sq, (uint64_t)B * Hq, 128))
         return GBATTN_ERR_CUDA;
     p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
@@ -160,7 +162,7 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, fl
     if (pl.n_pairs > kIntMax || pl.n_tiles > kIntMax) return GBATTN_ERR_TOO_LARGE;
     p.n_qblk = pl.n_qblk;
     p.kv_split = pl.kv_split ? 1 : 0;
-    p.n_pairs = (int)pl.first;
+    p.n_pairs = (int)(pl.kv_split ? pl.n_tiles : pl.first);
     p.tail0 = -1;
     p.causal = causal;
     p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
@@ -168,7 +170,8 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, fl
     p.err = device_error_word();
     if (!p.err) return GBATTN_ERR_CUDA;
     p.tiles_issued = tiles;
-    cudaError_t e = launch_attn_fwd_bf16(p, d, st);
+    cudaError_t e = pl.kv_split ? launch_attn_fwd_bf16_persistent(p, d, nsm, st)
+                                : launch_attn_fwd_bf16(p, d, st);
     if (e == cudaSuccess && pl.tail > 0) {
         PrefillParams t = p;
         t.kv_split = 1;

@@ -22,13 +22,15 @@ struct PrefillParams {
     CUtensorMap tmap_q;   // 3-D (d, Sq, B*Hq), box (64, 128, 1), 128B swizzle
     CUtensorMap tmap_k;   // 3-D (d, Skv, B*Hkv), box (64, 128, 1), 128B swizzle
     CUtensorMap tmap_v;   // same as K
+    CUtensorMap tmap_o;   // 3-D (d, Sq, B*Hq), box (64, 128, 1), 128B swizzle (TMA stores of
+                          // the persistent kernel)
     __nv_bfloat16* o;     // [B, Hq, Sq, d]
     float* lse;           // [B, Hq, Sq] or null
     int B, Hq, Hkv, Sq, Skv;
     int G;                // Hq / Hkv
     int n_qblk;           // ceil(Sq / 128)
     int n_pairs;          // work items: pairs of Q tiles, or single Q tiles with kv_split
-    int kv_split;         // 1: each CTA splits one Q tile's KV range over its two slots
+    int kv_split;         // 1: a CTA splits each of its Q tiles' KV range over its two slots
     int tail0;            // KV split: -1, or the first pair whose two Q tiles the CTAs take
                           // (the last, partly filled wave of a pair-mode call)
     int causal;
@@ -42,6 +44,12 @@ cudaError_t launch_attn_fwd_bf16(const PrefillParams& p, int d, cudaStream_t str
 // The Q tiles of pairs [p.tail0, p.tail0 + p.n_pairs / 2) in KV-split mode, launched as a
 // programmatic dependent of the pair-mode launch just before it (p.n_pairs = tiles).
 cudaError_t launch_attn_fwd_bf16_tail(const PrefillParams& p, int d, cudaStream_t stream);
+
+// ---- bf16 persistent KV-split prefill (prefill_persist.cu) ------------------------------
+// p.n_pairs single Q tiles (all of the call's), dealt heaviest first in snake order to
+// min(p.n_pairs, nsm) persistent CTAs; each tile's KV range is split over a CTA's two slots.
+cudaError_t launch_attn_fwd_bf16_persistent(const PrefillParams& p, int d, int nsm,
+                                            cudaStream_t stream);
 
 // ---- bf16 split-KV decode path (decode_splitkv.cu) --------------------------------------
 struct DecodeParams {

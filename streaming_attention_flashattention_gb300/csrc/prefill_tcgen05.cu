@@ -26,13 +26,14 @@
 // (b, kv head, q block, head in group), so for G >= 2 they are two query heads of one KV
 // head at the same query block and share every K/V tile and the same causal extent.
 //
-// KV-split mode (small problems, where pairs would leave SMs idle): a CTA takes ONE Q tile
-// and gives its two ping-pong slots the two halves of that tile's KV range, [0, n0) and
+// KV-split instance (kSplit): the Q tiles of a pair-mode call's last, partly filled wave,
+// launched behind the pair grid as a programmatic dependent.  A CTA takes ONE Q tile and
+// gives its two ping-pong slots the two halves of that tile's KV range, [0, n0) and
 // [n0, n).  Each slot keeps its own (m, l, O); at the end the two states are merged
 // inside the CTA with the log-sum-exp rule of "ADR-0060" section 4 (slot 1's O goes
-// through shared memory).  The heaviest causal tiles then take half as long.  The K ring
-// gets a third slot (the unused second Q buffer) because each K/V tile now feeds one
-// S/PV pair instead of two.
+// through shared memory).  The K ring gets a third slot (the unused second Q buffer)
+// because each K/V tile now feeds one S/PV pair instead of two.  (Calls too small for
+// pairs run the same split on persistent CTAs: prefill_persist.cu.)
 #include "common.cuh"
 #include "kernels.h"
 
@@ -82,23 +83,6 @@ __device__ __forceinline__ int kv_tiles_of(const PrefillParams& p, int q0) {
     return (keys + kBlockN - 1) / kBlockN;
 }
 
-// KV-split mode: item `rank` is one Q tile (heaviest first); slot 0 takes KV tiles
-// [0, n0), slot 1 takes [n0, n), n0 = ceil(n / 2).
-__device__ __forceinline__ void split_tiles(const PrefillParams& p, int rank, int& b, int& kvh,
-                                            TileDesc (&t)[2]) {
-    const int bh_count = p.B * p.Hq;
-    const int qb = p.n_qblk - 1 - rank / bh_count;
-    const int bh = rank % bh_count;
-    b = bh / p.Hq;
-    const int h = bh % p.Hq;
-    kvh = h / p.G;
-    const int q0 = qb * kBlockM;
-    const int n = kv_tiles_of(p, q0);
-    const int n0 = (n + 1) / 2;
-    t[0].present = 1; t[0].h = h; t[0].q0 = q0; t[0].n_kv = n0; t[0].kv0 = 0;
-    t[1].present = n - n0 > 0; t[1].h = h; t[1].q0 = q0; t[1].n_kv = n - n0; t[1].kv0 = n0;
-}
-
 __device__ __forceinline__ void pair_tiles(const PrefillParams& p, int rank, int& b, int& kvh,
                                            TileDesc (&t)[2]);
 
@@ -136,8 +120,8 @@ __device__ __forceinline__ void pair_tiles(const PrefillParams& p, int rank, int
     }
 }
 
-// kTail (with kSplit): the Q tiles of a pair-mode call's last pairs, launched behind it
-template <int D, bool kSplit, bool kTail = false>
+// kSplit: the KV-split tail launch of a pair-mode call (its last pairs' Q tiles)
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
     constexpr int KS = kSplit ? 3 : 2;   // K ring slots
@@ -162,11 +146,9 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
 
     int b, kvh;
     TileDesc td[2];
-    if constexpr (kTail) {
+    if constexpr (kSplit) {
         tail_tiles(p, blockIdx.x, b, kvh, td);
         if (!td[0].present) return;          // the absent second tile of an odd last pair
-    } else if constexpr (kSplit) {
-        split_tiles(p, blockIdx.x, b, kvh, td);
     } else {
         pair_tiles(p, blockIdx.x, b, kvh, td);
         // a KV-split launch of the last pairs may start on SMs this grid leaves free
@@ -570,17 +552,17 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
         tmem_dealloc(tmem, L::kTmemCols);
     }
     // a tail launch finishes only after the pair-mode grid it overlaps
-    if constexpr (kTail)
+    if constexpr (kSplit)
         if (blockIdx.x == 0 && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-template <int D, bool kSplit>
-cudaError_t launch_variant(const PrefillParams& p, cudaStream_t stream) {
+template <int D>
+cudaError_t launch_pairs(const PrefillParams& p, cudaStream_t stream) {
     constexpr int smem = PLayout<D>::kAlloc;
-    cudaError_t err = cudaFuncSetAttribute(prefill_fwd_kernel<D, kSplit>,
+    cudaError_t err = cudaFuncSetAttribute(prefill_fwd_kernel<D, false>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    prefill_fwd_kernel<D, kSplit><<<p.n_pairs, kThreads, smem, stream>>>(p);
+    prefill_fwd_kernel<D, false><<<p.n_pairs, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -589,7 +571,7 @@ cudaError_t launch_variant(const PrefillParams& p, cudaStream_t stream) {
 template <int D>
 cudaError_t launch_tail(const PrefillParams& p, cudaStream_t stream) {
     constexpr int smem = PLayout<D>::kAlloc;
-    cudaError_t err = cudaFuncSetAttribute(prefill_fwd_kernel<D, true, true>,
+    cudaError_t err = cudaFuncSetAttribute(prefill_fwd_kernel<D, true>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
@@ -602,7 +584,7 @@ cudaError_t launch_tail(const PrefillParams& p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_fwd_kernel<D, true, true>, p);
+    return cudaLaunchKernelEx(&cfg, prefill_fwd_kernel<D, true>, p);
 }
 
 cudaError_t launch_attn_fwd_bf16_tail(const PrefillParams& p, int d, cudaStream_t stream) {
@@ -612,9 +594,8 @@ cudaError_t launch_attn_fwd_bf16_tail(const PrefillParams& p, int d, cudaStream_
 
 cudaError_t launch_attn_fwd_bf16(const PrefillParams& p, int d, cudaStream_t stream) {
     if (p.n_pairs <= 0) return cudaSuccess;
-    if (d == 128)
-        return p.kv_split ? launch_variant<128, true>(p, stream) : launch_variant<128, false>(p, stream);
-    return p.kv_split ? launch_variant<64, true>(p, stream) : launch_variant<64, false>(p, stream);
+    if (p.kv_split) return cudaErrorInvalidValue;   // small calls run prefill_persist.cu
+    return d == 128 ? launch_pairs<128>(p, stream) : launch_pairs<64>(p, stream);
 }
 
 }  // namespace gbattn

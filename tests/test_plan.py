@@ -91,9 +91,12 @@ def test_prefill_pairs_and_kv_split_mode():
     # Llama3-70B causal prefill: 2048 pairs, heaviest first, one launch
     assert pre(1, 64, 8, 8192, 8192, True) == {"mode": "pairs", "first_launch_ctas": 2048,
                                                "tail_pairs": 0, "q_tiles": 4096}
-    # fewer than two pairs per SM: one Q tile per CTA
-    assert pre(2, 8, 2, 2048, 2048, True) == {"mode": "kv_split", "first_launch_ctas": 256,
+    # fewer than two pairs per SM: single Q tiles with their KV range split over a CTA's
+    # two slots, on one persistent CTA per SM
+    assert pre(2, 8, 2, 2048, 2048, True) == {"mode": "kv_split", "first_launch_ctas": 152,
                                               "tail_pairs": 0, "q_tiles": 256}
+    # fewer Q tiles than SMs: one CTA per tile
+    assert pre(1, 8, 2, 1024, 1024, True)["first_launch_ctas"] == 64
 
 
 def test_prefill_tail_for_equal_pairs():
