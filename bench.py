@@ -539,7 +539,7 @@ def run_gpu(args, rank, world, local_rank):
                                     PREFILL.causal, nsm)
     dec_plan = gb.attn_decode_plan(DECODE.B, DECODE.Hq, DECODE.Hkv, 1, DECODE.Skv, DECODE.d,
                                    DECODE.num_splits, nsm)
-    launches = (1 + (pre_plan["tail_pairs"] > 0)) + (1 + (dec_plan["merge"] == "combine"))
+    launches = (1 + (pre_plan["tail_pairs"] > 0)) + (1 + (dec_plan["merge"] != "single_launch"))
     traffic_pre, traffic_pre_src = committed_traffic("prefill")
     traffic_dec, traffic_dec_src = committed_traffic("decode")
 

@@ -207,7 +207,11 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Tq, int Lmax, int
  * split streams its chunk once for all G = Hq / Hkv query heads of a KV head (the heads
  * are stacked into one MMA operand, "ADR-0060" section 5.2), and the partial (lse_s, O_s)
  * of the splits are merged ("ADR-0060" section 4; a sequence with one split is written
- * directly).  When every work item fits in one wave of the GPU, or the call has at most
+ * directly).  When the (split, KV head) work items of the warp-level kernel would leave the
+ * GPU's last wave mostly idle, each split is processed as up to 4 contiguous pieces (at
+ * least 512 keys each),
+ * each with a partial of its own in the same merge: the result is the same up to fp32
+ * rounding, and attn_decode_plan reports the piece count.  When every work item fits in one wave of the GPU, or the call has at most
  * 16 (sequence, KV head) groups with splits of at least 1024 keys (Lmax / splits), the
  * merge is done by the CTA that finishes a group's last split (one launch, "ADR-0060"
  * section 4.3); otherwise a combine kernel, launched dependent on the split kernel, merges.  With G >= 16 query
@@ -281,14 +285,18 @@ int attn_decode_splitkv_noalloc(const void* q, const void* kcache, const void* v
 /*
  * attn_decode_plan -- what attn_decode_multitoken / attn_decode_splitkv (Tq = 1) decide for
  * these sizes on a GPU with num_sms SMs.  Host only: no device access, for tests and
- * capacity planning.  plan (host, 6 ints) receives:
+ * capacity planning.  plan (host, 7 ints) receives:
  *   plan[0]  splits per sequence the workspace holds (the automatic count for Lmax when
  *            num_splits = 0)
  *   plan[1]  kernel: 0 warp-level MMAs (8 query rows at a time), 1 tcgen05 (M = 128 rows)
- *   plan[2]  merge: 1 in the split kernel (single launch), 0 a dependent combine kernel
+ *   plan[2]  merge: 0 a dependent combine kernel that waits for the whole split grid, 1 the
+ *            CTA that finishes a group's last split merges it (single launch), 2 a dependent
+ *            combine kernel that merges each (sequence, KV head) group as soon as all of its
+ *            partials are counted in
  *   plan[3]  work items of the kernel
  *   plan[4]  query rows per KV head, G * Tq
  *   plan[5]  combine lanes per (row, 4 columns)
+ *   plan[6]  pieces per split (work items, and partials, per split)
  * Returns GBATTN_OK or the status the decode call would return for these sizes.
  */
 int attn_decode_plan(int B, int Hq, int Hkv, int Tq, int Lmax, int d, int num_splits,
@@ -314,7 +322,7 @@ int attn_prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int n
  * Returns GBATTN_OK, GBATTN_ERR_TIMEOUT (the word was set) or GBATTN_ERR_CUDA.
  * If detail != NULL it receives the raw word (which wait gave up): 1 producer (free ring
  * slot), 2 consumer (filled slot), 3 MMA issuer, 4 softmax warps, 5 exit drain of
- * in-flight copies, 6 the self-test wait.
+ * in-flight copies, 6 the self-test wait, 7 a decode row's merge waiting for its partials.
  */
 int attn_last_device_error(void* stream, int* detail);
 

@@ -380,12 +380,13 @@ def attn_decode_splitkv_noalloc(q: torch.Tensor, kcache: torch.Tensor, vcache: t
 def attn_decode_plan(B: int, Hq: int, Hkv: int, Tq: int, Lmax: int, d: int, num_splits: int,
                      num_sms: int) -> dict:
     """The decode call's choices for these sizes on a GPU with num_sms SMs (host only)."""
-    plan = (ctypes.c_int * 6)()
+    plan = (ctypes.c_int * 7)()
     _check("attn_decode_plan", load_library().attn_decode_plan(
         B, Hq, Hkv, Tq, Lmax, d, num_splits, num_sms, plan))
     return {"splits": plan[0], "kernel": "tcgen05" if plan[1] else "warp",
-            "merge": "single_launch" if plan[2] else "combine", "items": plan[3],
-            "rows_per_kv_head": plan[4], "combine_lanes": plan[5]}
+            "merge": {0: "combine", 1: "single_launch", 2: "combine_per_group"}[plan[2]],
+            "items": plan[3],
+            "rows_per_kv_head": plan[4], "combine_lanes": plan[5], "pieces": plan[6]}
 
 
 def attn_prefill_plan(B: int, Hq: int, Hkv: int, Sq: int, Skv: int, causal: bool,

@@ -25,6 +25,7 @@ enum : int {
     kErrWaitSoftmax = 4,     // softmax warps gave up waiting for S or O
     kErrWaitDrain = 5,       // drain of in-flight copies at exit gave up
     kErrSelfTest = 6,        // the self-test wait that is never satisfied gave up (expected)
+    kErrWaitMerge = 7,       // a decode row's merge gave up waiting for its group's partials
 };
 
 // A wait gives up after this many clock cycles (~1 s at 2 GHz).  Correct code never gets
@@ -95,6 +96,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int er
                 record_error(err_word, err);
                 return false;
             }
+        }
+    }
+}
+
+// Add `v` to a device-scope counter with release semantics: every write that this thread has
+// observed -- its own, and those of threads that synchronised with it before (a CTA barrier or
+// an mbarrier phase) -- is visible to a thread that reads the new count with acquire
+// semantics (counter_wait_geq).
+__device__ __forceinline__ void counter_add_release(int* addr, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+// Wait until the device-scope counter at `addr` reaches `target`, reading it with acquire
+// semantics (writes that the counting threads fenced before incrementing it are then
+// visible).  Returns false (after recording `err`) past kWaitLimitCycles, or when another
+// part of the grid already recorded an error.
+__device__ __forceinline__ bool counter_wait_geq(const int* addr, int target, int err,
+                                                 int* err_word) {
+    const long long t0 = clock64();
+    while (true) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+        if (v >= target) return true;
+        __nanosleep(64);
+        if (device_error_set(err_word)) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            record_error(err_word, err);
+            return false;
         }
     }
 }

@@ -65,14 +65,21 @@ struct Cfg {
     static constexpr int kStages = NCI == 1 ? 5 : 4;
 };
 constexpr int kHeads = 8;                  // query heads per work item (MMA N)
+constexpr int kPubSlots = 4;               // publisher ring entries (finished partials)
+
+// Single-token instances that count their partials (for the combine's per-group wait) have a
+// publisher warp after the producer: the consumers hand it each finished partial and it
+// issues the device-scope release of the count, off the streaming path.
+template <int NCI, bool kFused>
+constexpr int split_threads() { return Cfg<NCI>::kThreads + ((NCI == 1 && !kFused) ? 32 : 0); }
 
 struct StageInfo {
-    int b, kvh, hc, s;
+    int b, kvh, hc, s;            // s: the item's partial slot (split * pieces + piece)
     int tile, ntok, last, done;
     int n_ne;                     // non-empty splits of the sequence
     int key0;                     // first key of this tile
     int len;                      // keys of the sequence
-    int pad;
+    int direct;                   // the item is the row's only partial: write O and LSE
 };
 
 template <int D, int NCI>
@@ -92,7 +99,8 @@ struct Layout {
     static constexpr int kRedLOff = kRedMOff + kConsumerWarps * kHeads * 4;
     static constexpr int kRedOOff = kRedLOff + kConsumerWarps * kHeads * 4;
     static constexpr int kFusedOff = kRedOOff + kConsumerWarps * kHeads * D * 4;  // sync_c, flag
-    static constexpr int kBytes = kFusedOff + 16;
+    static constexpr int kPubOff = kFusedOff + 16;      // publisher ring: full, empty, group
+    static constexpr int kBytes = kPubOff + kPubSlots * (8 + 8 + 4);
     static constexpr int kAlloc = kBytes + 1024;                // slack for 1024-B alignment
     static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
 };
@@ -156,15 +164,15 @@ __device__ __forceinline__ void store_final(const DecodeParams& p, long long row
     if (with_lse && p.lse != nullptr) p.lse[row] = lse2 * 0.69314718055994531f;
 }
 
-// Final O (columns [d0, d0 + per)) and LSE of one query row from the n_ne split partials in
+// Final O (columns [d0, d0 + per)) and LSE of one query row from the n_ne partials in
 // the workspace: O = sum_s w_s O_s / sum_s w_s, w_s = 2^(lse_s - max lse) ("ADR-0060"
 // section 4), 8 partials loaded per batch; partials with lse = -inf (a row that saw no key
 // of that split) weigh nothing.
 template <int D, int per>
 __device__ __forceinline__ void fold_partials(const DecodeParams& p, long long row, int d0,
                                               int n_ne, bool with_lse) {
-    const float* lse_s = p.ws_lse + row * p.n_slots;
-    const float* o_s = p.ws_o + row * p.n_slots * D + d0;
+    const float* lse_s = p.ws_lse + row * p.n_parts;
+    const float* o_s = p.ws_o + row * p.n_parts * D + d0;
     constexpr int kChunk = 8;
     float M = -INFINITY, Ltot = 0.f, acc[per];
     #pragma unroll
@@ -207,8 +215,81 @@ __device__ __forceinline__ void fold_partials(const DecodeParams& p, long long r
     store_final<D, per>(p, row, d0, acc, with_lse, Ltot > 0.f ? M + __log2f(Ltot) : -INFINITY);
 }
 
+// The merge of a row's partials ("ADR-0060" section 4): O = sum_s w_s O_s / sum_s w_s with
+// w_s = 2^(lse_s - max lse) over the non-empty splits (every piece of a split is a partial of
+// its own).  Each (row, 4 output columns) piece of the output is shared by p.combine_lanes
+// adjacent lanes c (a power of two, at most 32): lane j merges partials [8 j, 8 j + 8) with
+// all its loads in flight at once, and the lanes' (max, sum, O) states are then merged with
+// shuffles -- one round of partial loads instead of one per 8.  This is lane j's share for
+// columns [4 cg, 4 cg + 4) of `row`, which has n_parts partials; every lane of the warp
+// calls it (inactive ones with active = false), since all take part in the shuffles.
+template <int D>
+__device__ __forceinline__ void merge_columns(const DecodeParams& p, long long row, int cg, int j,
+                                              int n_parts, bool active) {
+    constexpr int kChunk = 8;
+    const int c = p.combine_lanes;
+    const bool merge = active && n_parts > 1;   // (one partial: the split kernel wrote the row)
+    float M = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (merge) {
+        const float* lse_s = p.ws_lse + row * p.n_parts;
+        const float* o_s = p.ws_o + row * p.n_parts * D + cg * 4;
+        const int s0 = j * kChunk;
+        float ls[kChunk];
+        float4 ox[kChunk];
+        #pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const bool in = s0 + i < n_parts;
+            ls[i] = in ? __ldcg(lse_s + s0 + i) : -INFINITY;
+            ox[i] = in ? __ldcg(reinterpret_cast<const float4*>(o_s + (long long)(s0 + i) * D))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        #pragma unroll
+        for (int i = 0; i < kChunk; ++i) M = fmaxf(M, ls[i]);
+        #pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            if (ls[i] == -INFINITY) continue;     // a split (or piece) this row saw no key of
+            const float w = ex2_approx(ls[i] - M);
+            L += w;
+            acc.x += w * ox[i].x; acc.y += w * ox[i].y; acc.z += w * ox[i].z; acc.w += w * ox[i].w;
+        }
+    }
+    // merge the c lanes' states: (M, L, acc) with L and acc relative to 2^M
+    for (int off = 1; off < c; off <<= 1) {
+        const float Mo = __shfl_xor_sync(0xffffffffu, M, off);
+        const float Lo = __shfl_xor_sync(0xffffffffu, L, off);
+        float4 ao;
+        ao.x = __shfl_xor_sync(0xffffffffu, acc.x, off);
+        ao.y = __shfl_xor_sync(0xffffffffu, acc.y, off);
+        ao.z = __shfl_xor_sync(0xffffffffu, acc.z, off);
+        ao.w = __shfl_xor_sync(0xffffffffu, acc.w, off);
+        const float Mn = fmaxf(M, Mo);
+        const float a = (M == -INFINITY) ? 0.f : ex2_approx(M - Mn);
+        const float bo = (Mo == -INFINITY) ? 0.f : ex2_approx(Mo - Mn);
+        L = L * a + Lo * bo;
+        acc.x = acc.x * a + ao.x * bo; acc.y = acc.y * a + ao.y * bo;
+        acc.z = acc.z * a + ao.z * bo; acc.w = acc.w * a + ao.w * bo;
+        M = Mn;
+    }
+    if (!merge || j != 0) return;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint2 packed;
+    packed.x = pack_bf16(acc.x * inv, acc.y * inv);
+    packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(p.o + row * D + cg * 4) = packed;
+    if (cg == 0 && p.lse != nullptr)
+        p.lse[row] = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+}
+
+// Partials of a row of sequence b: pieces of its non-empty splits.
+__device__ __forceinline__ int row_partials(const DecodeParams& p, int b) {
+    int len = __ldg(&p.kv_lens[b]);
+    len = max(0, min(len, p.Lmax));
+    return nonempty_splits(len, splits_for(len, p.fixed_splits, p.auto_floor)) * p.pieces;
+}
+
 template <int D, int NCI, bool kFused>
-__global__ void __launch_bounds__(Cfg<NCI>::kThreads, 1)
+__global__ void __launch_bounds__(split_threads<NCI, kFused>(), 1)
 decode_split_kernel(const __grid_constant__ DecodeParams p) {
     static_assert(!kFused || NCI == 1, "single-launch mode is for single-token items");
     using L = Layout<D, NCI>;
@@ -230,6 +311,10 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
     float* red_o = reinterpret_cast<float*>(smem + L::kRedOOff);
     uint64_t* sync_c = reinterpret_cast<uint64_t*>(smem + L::kFusedOff);   // single-launch mode
     int* last_flag = reinterpret_cast<int*>(smem + L::kFusedOff + 8);
+    constexpr bool kPub = NCI == 1 && !kFused;                              // publisher warp
+    uint64_t* pub_full = reinterpret_cast<uint64_t*>(smem + L::kPubOff);  // [kPubSlots]
+    uint64_t* pub_empty = pub_full + kPubSlots;                             // [kPubSlots]
+    int* pub_group = reinterpret_cast<int*>(pub_empty + kPubSlots);         // [kPubSlots]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -240,6 +325,12 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
         mbar_init(sync_a, kConsumerWarps);
         mbar_init(sync_b, kConsumerWarps);
         if constexpr (kFused) mbar_init(sync_c, kConsumerWarps);
+        if constexpr (kPub) {
+            for (int i = 0; i < kPubSlots; ++i) {
+                mbar_init(&pub_full[i], 1);
+                mbar_init(&pub_empty[i], 1);
+            }
+        }
         fence_barrier_init();
     }
     __syncthreads();
@@ -258,11 +349,12 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
             // more (a static round-robin measured slower even for equal-size splits).
             for (int item = atomicAdd(p.counter, 1); ok && item < p.n_items;
                  item = atomicAdd(p.counter, 1)) {
-                // order: row chunk innermost, then split, then KV head, then sequence.  The
-                // row chunks of one split (several when G * Tq > 8) read the same K/V tiles
-                // and run side by side, so all but the first pass hit L2.
+                // order: row chunk innermost, then piece, then split, then KV head, then
+                // sequence.  The row chunks of one split (several when G * Tq > 8) read the
+                // same K/V tiles and run side by side, so all but the first pass hit L2.
                 int rem = item;
                 const int hc = rem % p.n_hg; rem /= p.n_hg;         // chunk group
+                const int pc = rem % p.pieces; rem /= p.pieces;     // piece of the split
                 const int s = rem % p.n_slots; rem /= p.n_slots;
                 const int kvh = rem % p.Hkv; rem /= p.Hkv;
                 const int b = rem;
@@ -278,7 +370,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 if (s >= n_ne) {
                     // empty split: no partial.  A sequence with no keys at all gets
                     // O = 0, LSE = -inf from its split 0.
-                    if (s == 0) {
+                    if (s == 0 && pc == 0) {
                         for (int g = 0; g < gcnt; ++g) {
                             uint4* dst = reinterpret_cast<uint4*>(p.o + (row0 + g) * D);
                             for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
@@ -289,6 +381,15 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 }
                 int t0, t1;
                 split_range(len, nb, s, t0, t1);
+                piece_range(t0, t1, p.pieces, pc, t0, t1);
+                const int part = s * p.pieces + pc;
+                if (t0 >= t1) {
+                    // an empty piece of a non-empty split: a partial that weighs nothing
+                    for (int g = 0; g < gcnt; ++g) p.ws_lse[(row0 + g) * p.n_parts + part] = -INFINITY;
+                    if (p.counted)
+                        counter_add_release(p.group_cnt + ((long long)b * p.Hkv + kvh) * p.n_hg + hc, 1);
+                    continue;
+                }
                 const int ntiles = (t1 - t0 + kKeysPerStage - 1) / kKeysPerStage;
                 const int zkv = b * p.Hkv + kvh;
                 for (int tile = 0; tile < ntiles; ++tile) {
@@ -298,7 +399,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                     }
                     const int y = t0 + tile * kKeysPerStage;
                     StageInfo& si = info[stage];
-                    si.b = b; si.kvh = kvh; si.hc = hc; si.s = s;
+                    si.b = b; si.kvh = kvh; si.hc = hc; si.s = part;
                     si.tile = tile;
                     si.ntok = min(kKeysPerStage, t1 - y);
                     si.last = (tile == ntiles - 1);
@@ -306,6 +407,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                     si.n_ne = n_ne;
                     si.key0 = y;
                     si.len = len;
+                    si.direct = (n_ne == 1 && p.pieces == 1) ? 1 : 0;
                     uint8_t* st = smem + stage * L::kStageBytes;
                     // single-token items load Q with their first tile only; stacked
                     // multi-token items re-read it from every stage (no registers to keep
@@ -351,6 +453,25 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
             for (int i = 0; i < kStages; ++i)
                 if (filled & (1u << i)) mbar_wait(&full[i], (fill_parity >> i) & 1u, kErrWaitDrain, p.err);
         }
+    } else if (warp == kConsumerWarps + 1) {
+        // ============================= publisher warp ==============================
+        // Counts each finished partial into its (sequence, KV head) group with a device-scope
+        // release: the consumers' writes of the partial happen before their hand-over here
+        // (CTA-scope mbarrier release / acquire), so the release covers them, and the
+        // combine, which reads the count with acquire, sees the whole partial.  The release
+        // waits for those writes to land; on this warp that costs the stream nothing.
+        if constexpr (kPub) {
+            if (lane == 0 && p.counted) {
+                for (uint32_t k = 0;; ++k) {
+                    const uint32_t ps = k % kPubSlots;
+                    if (!mbar_wait(&pub_full[ps], (k / kPubSlots) & 1, kErrWaitConsumer, p.err)) break;
+                    const int g = pub_group[ps];
+                    if (g < 0) break;                    // the consumers are done
+                    counter_add_release(p.group_cnt + g, 1);
+                    mbar_arrive(&pub_empty[ps]);
+                }
+            }
+        }
     } else if constexpr (NCI == 1) {
         // ======================= consumer warps (single token) ======================
         const int g = lane >> 2, c = lane & 3;
@@ -365,6 +486,16 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
         const int cw = warp / W;                 // row chunk of this warp within the group
         const int kp0 = (warp % W) * kKeysPerWarp;   // this warp's first key within a stage
         int gcnt = 0;                            // rows of this warp's chunk (<= 0: none)
+        uint32_t n_pub = 0;                      // partials handed to the publisher (thread 0)
+        // thread 0: hand group g (or -1: no more) to the publisher warp
+        auto publish = [&](int g) {
+            const uint32_t ps = n_pub % kPubSlots;
+            if (mbar_wait(&pub_empty[ps], ((n_pub / kPubSlots) & 1) ^ 1u, kErrWaitConsumer, p.err)) {
+                pub_group[ps] = g;
+                mbar_arrive(&pub_full[ps]);
+            }
+            ++n_pub;
+        };
         while (true) {
             if (!mbar_wait(&full[stage], phase, kErrWaitConsumer, p.err)) break;
             const StageInfo si = info[stage];
@@ -546,10 +677,10 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                             sum += wt[i] * red_o[((cr * W + i) * kHeads + head) * D + d0 + u];
                         ov[u] = sum * inv;
                     }
-                    if (si.n_ne == 1) {
+                    if (si.direct) {
                         store_final<D, per>(p, row, d0, ov, (t % kThrPerRow) == 0, lse2);
                     } else {
-                        const long long slot = row * p.n_slots + si.s;
+                        const long long slot = row * p.n_parts + si.s;
                         float* dst = p.ws_o + slot * D + d0;
                         #pragma unroll
                         for (int e = 0; e < per; e += 4)
@@ -562,9 +693,17 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 if (lane == 0) mbar_arrive(sync_b);
                 if (!mbar_wait(sync_b, sync_phase, kErrWaitConsumer, p.err)) break;
                 sync_phase ^= 1u;
+                if constexpr (kPub) {
+                    // count the partial in (the combine merges a group's rows once its count
+                    // is complete): all of its rows are written -- the rendezvous just passed
+                    // orders them before this hand-over -- and the publisher warp releases it
+                    if (p.counted && !si.direct && t == 0)
+                        publish((int)(((long long)si.b * p.Hkv + si.kvh) * p.n_hg + si.hc));
+                }
                 if constexpr (kFused) {
-                    if (si.n_ne > 1) {
+                    if (!si.direct) {
                         // count this split in; the CTA that completes the group folds it
+                        // (single-launch mode has one piece per split)
                         if (t == 0)
                             *last_flag = atomicAdd(p.group_cnt + ((long long)si.b * p.Hkv + si.kvh) * p.n_hg + si.hc, 1)
                                          == si.n_ne - 1;
@@ -581,6 +720,8 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
             }
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
+        if constexpr (kPub)
+            if (p.counted && threadIdx.x == 0) publish(-1);   // the publisher may stop
     } else {
         // ================== consumer warps (multi-token: chunks stacked) ==================
         // Warp w takes keys [16 (w % 4), +16) of every stage for chunks
@@ -788,10 +929,10 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                                 sum += wt[i] * red_o[((w0 + i) * kHeads + head) * D + d0 + u];
                             ov[u] = sum * inv;
                         }
-                        if (si.n_ne == 1) {
+                        if (si.direct) {
                             store_final<D, per>(p, row, d0, ov, (t & 15) == 0, lse2);
                         } else {
-                            const long long slot = row * p.n_slots + si.s;
+                            const long long slot = row * p.n_parts + si.s;
                             float* dst = p.ws_o + slot * D + d0;
                             #pragma unroll
                             for (int e = 0; e < per; e += 4)
@@ -811,85 +952,50 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
     __syncthreads();
 }
 
-// The merge of the split partials ("ADR-0060" section 4): O = sum_s w_s O_s / sum_s w_s with
-// w_s = 2^(lse_s - max lse) over the non-empty splits.  Each (b, query head, 4 output
-// columns) piece is shared by p.combine_lanes adjacent lanes (a power of two, at most 32):
-// lane j merges splits [8 j, 8 j + 8) with all its loads in flight at once, and the lanes'
-// (max, sum, O) states are then merged with shuffles -- one round of partial loads instead
-// of one per 8 splits.
+// The merges as a kernel of their own, launched dependent on the split kernel: one thread
+// per (row, 4 columns, lane).  The partials come from the split kernel launched just before
+// this one.  When that kernel counts each partial into its group (p.counted: calls with at
+// most 8 rows per KV head), a block waits only for its own rows' groups -- its CTAs are
+// launched as the split kernel's CTAs run out of work items and sit beside them, so each
+// group is merged as soon as its last partial lands instead of after the whole grid;
+// otherwise it waits for the split grid to complete.
 template <int D>
 __global__ void __launch_bounds__(256)
 decode_combine_kernel(const __grid_constant__ DecodeParams p) {
     constexpr int kGroups = D / 4;
-    constexpr int kChunk = 8;
     const int c = p.combine_lanes;
+    const long long rows = (long long)p.B * p.Hq * p.Tq;
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const int j = (int)(idx % c);
     const long long piece = idx / c;
     const long long row = piece / kGroups;
     const int cg = (int)(piece % kGroups);
-    // the partials come from the split kernel launched just before this one
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    // every lane takes part in the shuffles below; rows past the end or written directly by
-    // the split kernel just contribute nothing and store nothing
-    int n_ne = 0;
-    if (row < (long long)p.B * p.Hq * p.Tq) {
-        const int b = (int)(row / ((long long)p.Hq * p.Tq));
-        int len = __ldg(&p.kv_lens[b]);
-        len = max(0, min(len, p.Lmax));
-        n_ne = nonempty_splits(len, splits_for(len, p.fixed_splits, p.auto_floor));
-    }
-    const bool merge = n_ne > 1;
-    float M = -INFINITY, L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (merge) {
-        const float* lse_s = p.ws_lse + row * p.n_slots;
-        const float* o_s = p.ws_o + row * p.n_slots * D + cg * 4;
-        const int s0 = j * kChunk;
-        float ls[kChunk];
-        float4 ox[kChunk];
-        #pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            const bool in = s0 + i < n_ne;
-            ls[i] = in ? __ldcg(lse_s + s0 + i) : -INFINITY;
-            ox[i] = in ? __ldcg(reinterpret_cast<const float4*>(o_s + (long long)(s0 + i) * D))
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.counted) {
+        // the block's rows [r0, r1], groups of R rows (R <= 8: the group of a row is row / R)
+        const long long per_row = (long long)kGroups * c;
+        const long long r0 = (long long)blockIdx.x * blockDim.x / per_row;
+        const long long r1 = min(rows - 1, ((long long)blockIdx.x * blockDim.x + blockDim.x - 1) / per_row);
+        __shared__ int ok;
+        if (threadIdx.x == 0) {
+            ok = 1;
+            for (long long g = r0 / p.R; g <= r1 / p.R && ok; ++g) {
+                const int n = row_partials(p, (int)(g * p.R / ((long long)p.Hq * p.Tq)));
+                if (n > 1 && !counter_wait_geq(p.group_cnt + g, n, kErrWaitMerge, p.err)) ok = 0;
+            }
         }
-        #pragma unroll
-        for (int i = 0; i < kChunk; ++i) M = fmaxf(M, ls[i]);
-        #pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            if (ls[i] == -INFINITY) continue;     // a split this row saw no key of
-            const float w = ex2_approx(ls[i] - M);
-            L += w;
-            acc.x += w * ox[i].x; acc.y += w * ox[i].y; acc.z += w * ox[i].z; acc.w += w * ox[i].w;
-        }
+        __syncthreads();
+        if (!ok) return;
+    } else {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
     }
-    // merge the c lanes' states: (M, L, acc) with L and acc relative to 2^M
-    for (int off = 1; off < c; off <<= 1) {
-        const float Mo = __shfl_xor_sync(0xffffffffu, M, off);
-        const float Lo = __shfl_xor_sync(0xffffffffu, L, off);
-        float4 ao;
-        ao.x = __shfl_xor_sync(0xffffffffu, acc.x, off);
-        ao.y = __shfl_xor_sync(0xffffffffu, acc.y, off);
-        ao.z = __shfl_xor_sync(0xffffffffu, acc.z, off);
-        ao.w = __shfl_xor_sync(0xffffffffu, acc.w, off);
-        const float Mn = fmaxf(M, Mo);
-        const float a = (M == -INFINITY) ? 0.f : ex2_approx(M - Mn);
-        const float bo = (Mo == -INFINITY) ? 0.f : ex2_approx(Mo - Mn);
-        L = L * a + Lo * bo;
-        acc.x = acc.x * a + ao.x * bo; acc.y = acc.y * a + ao.y * bo;
-        acc.z = acc.z * a + ao.z * bo; acc.w = acc.w * a + ao.w * bo;
-        M = Mn;
-    }
-    if (!merge || j != 0) return;
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    uint2 packed;
-    packed.x = pack_bf16(acc.x * inv, acc.y * inv);
-    packed.y = pack_bf16(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(p.o + row * D + cg * 4) = packed;
-    if (cg == 0 && p.lse != nullptr)
-        p.lse[row] = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+    // rows past the end, or written directly by the split kernel, merge nothing
+    const bool in = row < rows;
+    const int n_parts = in ? row_partials(p, (int)(row / ((long long)p.Hq * p.Tq))) : 0;
+    merge_columns<D>(p, in ? row : 0, cg, j, n_parts, in);
+    // the call ends after both grids: one thread holds this grid open until the split grid
+    // has completed
+    if (p.counted && blockIdx.x == 0 && threadIdx.x == 0)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
@@ -899,12 +1005,12 @@ int decode_slots(int Lmax, int num_splits, int auto_floor) {
 }
 
 size_t decode_counter_bytes(int B, int Hkv, int n_hg) {
-    // the work queue counter, then one split counter per (b, KV head, chunk group)
+    // the work queue counter, then one partial counter per (b, KV head, chunk group)
     return (((size_t)1 + (size_t)B * Hkv * n_hg) * 4 + 255) / 256 * 256;
 }
 
-size_t decode_workspace_bytes(int B_rows, int Hq, int kv_groups, int n_hg, int d, int n_slots) {
-    const size_t rows = (size_t)B_rows * Hq * n_slots;
+size_t decode_workspace_bytes(int B_rows, int Hq, int kv_groups, int n_hg, int d, int n_parts) {
+    const size_t rows = (size_t)B_rows * Hq * n_parts;
     size_t bytes = decode_counter_bytes(kv_groups, 1, n_hg);   // counters
     bytes += ((rows * 4 + 255) / 256) * 256;             // lse partials
     bytes += rows * (size_t)d * 4;                       // O partials
@@ -922,7 +1028,7 @@ cudaError_t launch_pair(const DecodeParams& p, int num_sms, cudaStream_t stream)
     cudaError_t err = cudaFuncSetAttribute(decode_split_kernel<D, NCI, kFused>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    decode_split_kernel<D, NCI, kFused><<<grid, Cfg<NCI>::kThreads, smem, stream>>>(p);
+    decode_split_kernel<D, NCI, kFused><<<grid, split_threads<NCI, kFused>(), smem, stream>>>(p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     if constexpr (kFused) return cudaSuccess;      // merged in the split kernel

@@ -28,6 +28,17 @@ __device__ __forceinline__ int nonempty_splits(int len, int n) {
     return (len + c - 1) / c;
 }
 
+// Piece pc of P of the split [t0, t1): contiguous sub-ranges of ceil((t1 - t0) / P) keys
+// rounded up to kSplitAlign (trailing pieces may be empty).  A split cut into pieces is
+// still one contiguous block of keys; its pieces' partial states fold into the same
+// log-sum-exp merge as the splits themselves.
+__device__ __forceinline__ void piece_range(int t0, int t1, int P, int pc, int& a, int& b) {
+    int c = (t1 - t0 + P - 1) / P;
+    c = ((c + kSplitAlign - 1) / kSplitAlign) * kSplitAlign;
+    a = min(t1, t0 + pc * c);
+    b = min(t1, t0 + (pc + 1) * c);
+}
+
 // Splits of a sequence of len keys.  Automatic mode: one per kAutoChunk keys, raised to
 // auto_floor (the count that gives the call about one work item per SM, chosen on the host)
 // as long as each split keeps kAutoMinKeys keys.  Non-decreasing in len, so the host sizes

@@ -54,10 +54,11 @@ static_assert(kKeysT == 128, "the softmax row reductions assume 128 columns");
 
 // One work item as the producer hands it to the MMA and softmax warps.
 struct MtItem {
-    int b, kvh, s, rt;
+    int b, kvh, s, rt;                     // s: the item's partial slot (split * pieces + piece)
     int len, t0, t1, n_ne;
     int done;                              // end-of-work marker
-    int pad[3];
+    int direct;                            // the item is its rows' only partial: write O, LSE
+    int pad[2];
 };
 
 template <int D>
@@ -156,6 +157,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
             if (item >= p.n_items) break;
             int rem = item;
             const int rt = rem % p.n_rt; rem /= p.n_rt;
+            const int pc = rem % p.pieces; rem /= p.pieces;     // piece of the split
             const int s = rem % p.n_slots; rem /= p.n_slots;
             const int kvh = rem % p.Hkv;
             const int b = rem / p.Hkv;
@@ -166,7 +168,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
             const long long row0 = ((long long)b * p.Hkv + kvh) * p.R + (long long)rt * kRowsT;
             if (s >= n_ne) {
                 // no keys in this split; a sequence with no keys at all gets O = 0, LSE = -inf
-                if (s == 0 && n_ne == 0) {
+                if (s == 0 && pc == 0 && n_ne == 0) {
                     const int nrows = min(kRowsT, p.R - rt * kRowsT);
                     for (int i = lane; i < nrows * (D / 8); i += 32) {
                         const int r = i / (D / 8), c = i % (D / 8);
@@ -178,6 +180,14 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
             }
             int t0, t1;
             split_range(len, nb, s, t0, t1);
+            piece_range(t0, t1, p.pieces, pc, t0, t1);
+            const int part = s * p.pieces + pc;
+            if (t0 >= t1) {
+                // an empty piece of a non-empty split: a partial that weighs nothing
+                const int nrows = min(kRowsT, p.R - rt * kRowsT);
+                for (int i = lane; i < nrows; i += 32) p.ws_lse[(row0 + i) * p.n_parts + part] = -INFINITY;
+                continue;
+            }
             const int nt = (t1 - t0 + kKeysT - 1) / kKeysT;
             const int n0 = (nt + 1) / 2, n1 = nt - n0;
             if (lane == 0) {
@@ -186,9 +196,10 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                 ok = mbar_wait(&item_empty[k & 1], ((k >> 1) & 1) ^ 1u, kErrWaitProducer, p.err);
                 if (ok) {
                     MtItem& it = info[k & 1];
-                    it.b = b; it.kvh = kvh; it.s = s; it.rt = rt;
+                    it.b = b; it.kvh = kvh; it.s = part; it.rt = rt;
                     it.len = len; it.t0 = t0; it.t1 = t1; it.n_ne = n_ne;
                     it.done = 0;
+                    it.direct = (n_ne == 1 && p.pieces == 1) ? 1 : 0;
                     mbar_arrive(&item_full[k & 1]);
                 }
                 if (ok && k > 0) ok = mbar_wait(q_empty, (k - 1) & 1, kErrWaitProducer, p.err);
@@ -526,14 +537,14 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                     for (int e = 0; e < 32; ++e)
                         v[e] = (a0 * __uint_as_float(r0[e]) + (n1 > 0 ? a1 * __uint_as_float(r1[e]) : 0.f)) * inv;
                     if (!live) continue;
-                    if (it.n_ne == 1) {
+                    if (it.direct) {
                         uint4* dst = reinterpret_cast<uint4*>(p.o + row * D + col);
                         #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4)
                             dst[q4] = make_uint4(pack_bf16(v[8 * q4 + 0], v[8 * q4 + 1]), pack_bf16(v[8 * q4 + 2], v[8 * q4 + 3]),
                                                  pack_bf16(v[8 * q4 + 4], v[8 * q4 + 5]), pack_bf16(v[8 * q4 + 6], v[8 * q4 + 7]));
                     } else {
-                        float4* dst = reinterpret_cast<float4*>(p.ws_o + (row * p.n_slots + it.s) * D + col);
+                        float4* dst = reinterpret_cast<float4*>(p.ws_o + (row * p.n_parts + it.s) * D + col);
                         #pragma unroll
                         for (int q4 = 0; q4 < 8; ++q4)
                             dst[q4] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
@@ -541,10 +552,10 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                 }
                 if (live && t == 0) {
                     const float lse2 = lt > 0.f ? M + __log2f(lt) : -INFINITY;
-                    if (it.n_ne == 1) {
+                    if (it.direct) {
                         if (p.lse != nullptr) p.lse[row] = lse2 * 0.69314718055994531f;
                     } else {
-                        p.ws_lse[row * p.n_slots + it.s] = lse2;
+                        p.ws_lse[row * p.n_parts + it.s] = lse2;
                     }
                 }
             }

@@ -97,6 +97,10 @@ constexpr long long kFusedMaxGroups = 16;   // single-launch decode: up to this 
 constexpr long long kFusedMinKeys = 1024;   // with splits of at least this many keys
 constexpr long long kTcMinKeys = 1024;      // 9-15 rows per KV head: tcgen05 path from this
                                             // many keys per split
+constexpr int kMaxPieces = 4;               // pieces per split, at most
+constexpr long long kPieceWaves = 6;        // enough waves of work items that the last one
+                                            // no longer matters
+constexpr long long kPieceMinKeys = 512;    // keys per piece, at least (Lmax / (splits * pieces))
 
 // The work split of a bf16 prefill, from its sizes alone (used by the launch and by
 // attn_prefill_plan()).
@@ -275,16 +279,37 @@ int auto_floor(int B, int Hkv, const DecodeRows& dr, int nsm) {
     return (int)(f < 1 ? 1 : (f > kMaxSplits ? kMaxSplits : f));
 }
 
+// Pieces per split.  The work queue hands out whole items; when there are a few waves of
+// them and the last is mostly idle (workload 4: 512 equal splits on 152 SMs, 3.37 waves),
+// each split is cut into P contiguous pieces, each a work item with a partial of its own
+// that the combine folds like any other: the smallest P that gives kPieceWaves waves or a
+// last wave at least 3/4 full.  Pieces keep at least kPieceMinKeys keys, and a row has at
+// most kMaxSplits partials.  Calls within one wave keep whole splits.
+int pieces_for(long long items, int n_slots, int Lmax, int nsm) {
+    if (items <= nsm) return 1;
+    for (int P = 1; P <= kMaxPieces; ++P) {
+        if (P > 1 && ((long long)n_slots * P > kMaxSplits ||
+                      (long long)Lmax < kPieceMinKeys * n_slots * P))
+            return P - 1;
+        const long long it = items * P, rem = it % nsm;
+        if (it >= kPieceWaves * nsm || rem == 0 || 4 * rem >= 3 * (long long)nsm) return P;
+    }
+    return kMaxPieces;
+}
+
 // Everything a decode call decides from its sizes alone, before any device access: the
-// split count, the kernel, the merge.  The launch code and attn_decode_plan() both use it.
+// split count and pieces, the kernel, the merge.  The launch code, the workspace size and
+// attn_decode_plan() all use it.
 struct DecodePlan {
     DecodeRows dr;
     int floor_splits, n_slots;
+    int pieces;              // work items per split
     long long n_items;       // work items of the warp-level kernel
     bool tc;                 // the tcgen05 kernel runs the call
     int n_rt, q_rows;        // tcgen05 kernel: 128-row tiles per KV head, Q rows loaded
     long long tc_items;      // tcgen05 kernel: work items
-    bool fused;              // warp-level kernel: the merge happens in the split kernel
+    bool fused;              // warp-level kernel: the group's last split merges it
+    bool counted;            // warp-level kernel: partials counted per group, per-group combine
     int combine_lanes;       // combine kernel: lanes per (row, 4 columns)
 };
 
@@ -293,6 +318,7 @@ DecodePlan decode_plan(int B, int Hq, int Hkv, int Tq, int Lmax, int num_splits,
     pl.dr = decode_rows(Hq, Hkv, Tq);
     pl.floor_splits = auto_floor(B, Hkv, pl.dr, nsm);
     pl.n_slots = decode_slots(Lmax, num_splits, pl.floor_splits);
+    pl.pieces = 1;
     pl.n_items = (long long)pl.n_slots * B * Hkv * pl.dr.n_hg;
     // tcgen05 path: 16 or more query rows per KV head (several new tokens, or G >= 16), or 9
     // to 15 with long splits; 8 rows and fewer, and short splits of 9 to 15 rows, run best on
@@ -313,8 +339,20 @@ DecodePlan decode_plan(int B, int Hq, int Hkv, int Tq, int Lmax, int num_splits,
     const long long groups = (long long)B * Hkv * pl.dr.n_hg;
     const bool few_long = groups <= kFusedMaxGroups && (long long)Lmax >= kFusedMinKeys * pl.n_slots;
     pl.fused = !pl.tc && pl.dr.nci == 1 && (pl.n_items <= nsm || few_long);
+    // (the tcgen05 kernel's items carry more fixed cost -- a Q tile, two ping-pong slots, a
+    // merge from TMEM -- and measured no faster or slower in pieces: it keeps whole splits)
+    if (!pl.fused && !pl.tc) {
+        pl.pieces = pieces_for(pl.n_items, pl.n_slots, Lmax, nsm);
+        pl.n_items *= pl.pieces;
+    }
+    // calls of the warp-level kernel with one row chunk per KV head (R <= 8) count each
+    // partial into its (sequence, KV head) group, and the combine merges a group as soon as
+    // its count is complete, overlapping the split kernel's last items, instead of waiting
+    // for the whole split grid (that wait and the combine after it cost about 6 us on
+    // workload 4)
+    pl.counted = !pl.tc && !pl.fused && pl.dr.nci == 1;
     pl.combine_lanes = 1;
-    while (pl.combine_lanes * 8 < pl.n_slots) pl.combine_lanes *= 2;   // n_slots <= 256: at most 32
+    while (pl.combine_lanes * 8 < pl.n_slots * pl.pieces) pl.combine_lanes *= 2;   // <= 256 partials: at most 32
     return pl;
 }
 
@@ -504,9 +542,8 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Tq, int Lmax, int
     if (num_splits < 0 || num_splits > kMaxSplits || num_sms <= 0) return 0;
     if (Hq % Hkv != 0) return 0;
     if ((long long)B * Hq * Tq > kIntMax) return 0;
-    const DecodeRows dr = decode_rows(Hq, Hkv, Tq);
-    return decode_workspace_bytes(B * Tq, Hq, B * Hkv, dr.n_hg, d,
-                                  decode_slots(Lmax, num_splits, auto_floor(B, Hkv, dr, num_sms)));
+    const DecodePlan pl = decode_plan(B, Hq, Hkv, Tq, Lmax, num_splits, num_sms);
+    return decode_workspace_bytes(B * Tq, Hq, B * Hkv, pl.dr.n_hg, d, pl.n_slots * pl.pieces);
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int num_splits) {
@@ -538,12 +575,13 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
     if ((long long)B * Hq * Tq > kIntMax / 8) return GBATTN_ERR_TOO_LARGE;
     const int nsm = sm_count();
     if (nsm <= 0) return GBATTN_ERR_CUDA;
-    const DecodeRows dr = decode_rows(Hq, Hkv, Tq);
-    const int n_slots = decode_slots(Lmax, num_splits, auto_floor(B, Hkv, dr, nsm));
-    const size_t need = decode_workspace_bytes(B * Tq, Hq, B * Hkv, dr.n_hg, d, n_slots);
+    const DecodePlan pl = decode_plan(B, Hq, Hkv, Tq, Lmax, num_splits, nsm);
+    const DecodeRows dr = pl.dr;
+    const int n_slots = pl.n_slots;
+    const int n_parts = pl.n_slots * pl.pieces;
+    const size_t need = decode_workspace_bytes(B * Tq, Hq, B * Hkv, dr.n_hg, d, n_parts);
     if (!workspace || ws_bytes < need) return GBATTN_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GBATTN_ERR_MISALIGNED;
-    const DecodePlan pl = decode_plan(B, Hq, Hkv, Tq, Lmax, num_splits, nsm);
     const int G = Hq / Hkv;
     const int R = dr.R, n_hc = dr.n_hc, nci = dr.nci, n_hg = dr.n_hg;
     const long long n_items = pl.n_items;
@@ -555,7 +593,7 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
         !make_map_bf16_3d(&p.tmap_q, q, d, (uint64_t)B * Hq * Tq, 1, 8))
         return GBATTN_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const size_t rows = (size_t)B * Hq * Tq * n_slots;
+    const size_t rows = (size_t)B * Hq * Tq * n_parts;
     const size_t cnt_bytes = decode_counter_bytes(B, Hkv, n_hg);
     p.counter = reinterpret_cast<int*>(ws);
     p.group_cnt = p.counter + 1;
@@ -571,11 +609,14 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
     p.nci = nci;
     p.n_hg = n_hg;
     p.n_slots = n_slots;
+    p.pieces = pl.pieces;
+    p.n_parts = n_parts;
     p.fixed_splits = num_splits;
     p.auto_floor = pl.floor_splits;
     p.combine_lanes = pl.combine_lanes;
     p.n_items = (int)n_items;
     p.fused = pl.fused ? 1 : 0;
+    p.counted = pl.counted ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = device_error_word();
     if (!p.err) return GBATTN_ERR_CUDA;
@@ -599,6 +640,8 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
         tp.q_rows = q_rows;
         tp.n_rt = pl.n_rt;
         tp.n_slots = n_slots;
+        tp.pieces = pl.pieces;
+        tp.n_parts = n_parts;
         tp.fixed_splits = num_splits;
         tp.auto_floor = pl.floor_splits;
         const long long tc_items = pl.tc_items;
@@ -637,10 +680,11 @@ int attn_decode_plan(int B, int Hq, int Hkv, int Tq, int Lmax, int d, int num_sp
     if (items > kIntMax) return GBATTN_ERR_TOO_LARGE;
     plan[0] = pl.n_slots;
     plan[1] = pl.tc ? 1 : 0;
-    plan[2] = pl.fused ? 1 : 0;
+    plan[2] = pl.fused ? 1 : (pl.counted ? 2 : 0);
     plan[3] = (int)items;
     plan[4] = pl.dr.R;
     plan[5] = pl.combine_lanes;
+    plan[6] = pl.pieces;
     return GBATTN_OK;
 }
 

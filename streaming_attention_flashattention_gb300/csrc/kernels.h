@@ -60,9 +60,10 @@ struct DecodeParams {
     __nv_bfloat16* o;     // [B, Hq, d]
     float* lse;           // [B, Hq] or null
     int* counter;         // work queue counter (zeroed before the split kernel)
-    int* group_cnt;       // [B, Hkv, n_hg] finished splits per group (single-launch mode)
-    float* ws_lse;        // [B, Hq, Tq, n_slots] log2-domain partial lse
-    float* ws_o;          // [B, Hq, Tq, n_slots, d] normalised partial outputs
+    int* group_cnt;       // [B, Hkv, n_hg] finished partials per group (single-launch mode and
+                          // the counted combine)
+    float* ws_lse;        // [B, Hq, Tq, n_parts] log2-domain partial lse
+    float* ws_o;          // [B, Hq, Tq, n_parts, d] normalised partial outputs
     int B, Hq, Hkv, Lmax, G;
     int Tq;               // new query tokens per sequence (1: single-token decode)
     int R;                // query rows per KV head: G * Tq (head-major, token-minor)
@@ -70,11 +71,15 @@ struct DecodeParams {
     int nci;              // row chunks per work item: 1, 2 or 4
     int n_hg;             // chunk groups per KV head: ceil(n_hc / nci)
     int n_slots;          // split slots per sequence
+    int pieces;           // work items per split (contiguous pieces, each its own partial)
+    int n_parts;          // partial slots per row: n_slots * pieces (split s, piece c: s * pieces + c)
     int fixed_splits;     // > 0 fixed count, 0 automatic
     int auto_floor;       // automatic mode: split count that fills the GPU (see splits_for)
-    int combine_lanes;    // combine: lanes per (row, 4 columns), a power of two >= n_slots / 8
-    int n_items;          // n_slots * B * Hkv * n_hg
+    int combine_lanes;    // combine: lanes per (row, 4 columns), a power of two >= n_parts / 8
+    int n_items;          // n_slots * pieces * B * Hkv * n_hg
     int fused;            // 1: single launch, the group's last split merges (single token)
+    int counted;          // 1: each partial is counted into group_cnt, and the combine waits
+                          // for its rows' groups only (R <= 8, not fused)
     float scale_log2;
     int* err;             // device error word of bounded waits
 };
@@ -88,8 +93,8 @@ constexpr int kMaxSplits = 256;
 constexpr int kSplitAlign = 64;
 
 size_t decode_counter_bytes(int B, int Hkv, int n_hg);
-// B_rows: B * Tq; kv_groups: B * Hkv
-size_t decode_workspace_bytes(int B_rows, int Hq, int kv_groups, int n_hg, int d, int n_slots);
+// B_rows: B * Tq; kv_groups: B * Hkv; n_parts: partial slots per row
+size_t decode_workspace_bytes(int B_rows, int Hq, int kv_groups, int n_hg, int d, int n_parts);
 int decode_slots(int Lmax, int num_splits, int auto_floor);
 cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
                                   cudaStream_t stream);
@@ -107,15 +112,16 @@ struct DecodeTcParams {
     const int* kv_lens;
     __nv_bfloat16* o;     // [B, Hq, Tq, d]
     float* lse;           // [B, Hq, Tq] or null
-    float* ws_lse;        // [B, Hq, Tq, n_slots] log2-domain partial lse
-    float* ws_o;          // [B, Hq, Tq, n_slots, d]
+    float* ws_lse;        // [B, Hq, Tq, n_parts] log2-domain partial lse
+    float* ws_o;          // [B, Hq, Tq, n_parts, d]
     int B, Hq, Hkv, Lmax, Tq;
     int R;                // query rows per KV head: G * Tq
     int q_rows;           // Q rows loaded per item: R rounded up to 8, at most 128
     int n_rt;             // 128-row tiles per KV head: ceil(R / 128)
     int n_slots, fixed_splits;
+    int pieces, n_parts;  // as in DecodeParams
     int auto_floor;       // automatic mode: split count that fills the GPU (see splits_for)
-    int n_items;          // n_slots * B * Hkv * n_rt
+    int n_items;          // n_slots * pieces * B * Hkv * n_rt
     int* counter;         // work queue counter (zeroed before the kernel)
     float scale_log2;
     int* err;

@@ -120,13 +120,15 @@ def test_workspace_size(lib):
         return gb.attn_decode_workspace_bytes(B, Hq, Hkv, 1, L, d, ns, nsm)
 
     def expect(B, Hq, Hkv, slots, d):
-        # counters (the work queue, then one finished-split counter per (b, KV head, chunk
-        # group); G <= 8 gives one group) rounded to 256, lse partials rounded to 256, O partials
+        # counters (the work queue, then one partial counter per (b, KV head, chunk group);
+        # G <= 8 gives one group) rounded to 256, lse partials rounded to 256, O partials
         rows = B * Hq * slots
         counters = ((1 + B * Hkv) * 4 + 255) // 256 * 256
         return counters + ((rows * 4 + 255) // 256) * 256 + rows * d * 4
 
-    assert ws(4, 64, 8, 32768, 128, 16) == expect(4, 64, 8, 16, 128)
+    # 16 fixed splits x 32 (sequence, KV head) groups = 512 items, 3.37 waves on 152 SMs:
+    # each split runs as 2 pieces, so 32 partials per row
+    assert ws(4, 64, 8, 32768, 128, 16) == expect(4, 64, 8, 32, 128)
     # automatic: one slot per 4096 keys of capacity ...
     assert ws(16, 64, 8, 131072, 128, 0) == expect(16, 64, 8, 32, 128)
     # ... raised for few (sequence, KV head) groups to the most splits that keep one wave of
@@ -147,8 +149,9 @@ def test_workspace_size(lib):
     # (16384 keys: one split per 4096 keys would give 4)
     assert ws(1, 64, 8, 16384, 128, 0, nsm=76) == expect(1, 64, 8, 9, 128)
     assert ws(1, 64, 8, 16384, 128, 0, nsm=304) == expect(1, 64, 8, 38, 128)
-    # fixed split counts do not depend on it
-    assert ws(4, 64, 8, 32768, 128, 16, nsm=76) == ws(4, 64, 8, 32768, 128, 16)
+    # fixed split counts keep their splits; the pieces follow the SM count (512 items are
+    # 6.7 waves on 76 SMs: whole splits)
+    assert ws(4, 64, 8, 32768, 128, 16, nsm=76) == expect(4, 64, 8, 16, 128)
 
 
 def test_current_device_workspace_size_needs_a_device(lib):

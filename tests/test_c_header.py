@@ -37,9 +37,9 @@ int main(void) {
     if (strcmp(attn_status_string(GBATTN_OK), "ok") != 0) return 12;
     /* host-only queries */
     if (attn_decode_workspace_bytes(4, 64, 8, 1, 32768, 128, 16, 152) == 0) return 13;
-    int plan[6];
+    int plan[7];
     if (attn_decode_plan(4, 64, 8, 1, 32768, 128, 16, 152, plan) != GBATTN_OK) return 14;
-    if (plan[0] != 16 || plan[1] != 0 || plan[3] != 512) return 15;
+    if (plan[0] != 16 || plan[1] != 0 || plan[3] != 1024 || plan[6] != 2) return 15;
     int pp[4];
     if (attn_prefill_plan(1, 64, 8, 8192, 8192, 1, 152, pp) != GBATTN_OK) return 16;
     if (pp[0] != 0 || pp[1] != 2048 || pp[3] != 4096) return 17;

@@ -23,9 +23,25 @@ def dec(B, Hq, Hkv, Tq, L, ns, d=128):
 
 
 def test_llama70b_decode_16_splits():
+    # 512 split items would be 3.37 waves on 152 SMs: two pieces per split, 1024 items
     p = dec(4, 64, 8, 1, 32768, 16)
-    assert p == {"splits": 16, "kernel": "warp", "merge": "combine", "items": 512,
-                 "rows_per_kv_head": 8, "combine_lanes": 2}
+    assert p == {"splits": 16, "kernel": "warp", "merge": "combine_per_group", "items": 1024,
+                 "rows_per_kv_head": 8, "combine_lanes": 4, "pieces": 2}
+
+
+def test_pieces_rule():
+    # the smallest piece count giving >= 6 waves or a last wave >= 3/4 full
+    assert dec(16, 64, 8, 1, 131072, 0)["pieces"] == 1          # 4096 items, 27 waves
+    assert dec(4, 64, 8, 1, 32768, 19)["pieces"] == 1           # 608 items: exactly 4 waves
+    assert dec(4, 64, 8, 1, 32768, 8)["pieces"] == 4            # 256 items: 1.7, 3.4, 5.05, 6.7 waves
+    assert dec(4, 64, 8, 4, 32768, 16)["pieces"] == 1           # tcgen05 kernel: whole splits
+    # one wave: whole splits (and the single-launch merge)
+    p = dec(1, 64, 8, 1, 4096, 0)
+    assert p["pieces"] == 1 and p["merge"] == "single_launch"
+    # pieces keep at least 512 keys: 64 splits of 512 keys are not cut
+    assert dec(4, 64, 8, 1, 32768, 64)["pieces"] == 1
+    # at most 256 partials per row
+    assert dec(2, 64, 8, 1, 200000, 200)["pieces"] == 1
 
 
 def test_automatic_splits_fill_one_wave():
@@ -43,15 +59,19 @@ def test_automatic_splits_fill_one_wave():
 
 
 def test_single_launch_merge_rule():
-    # one wave of work items
+    # one wave of work items: the group's last split merges
     assert dec(1, 64, 8, 1, 4096, 0)["merge"] == "single_launch"          # 128 items
-    # few groups with long splits
+    # few groups with long splits: the same
     p = dec(1, 64, 8, 1, 131072, 0)                                       # 8 groups, 4096 keys
     assert p["items"] > NSM and p["merge"] == "single_launch"
-    # few groups, short splits (512 keys): combine
-    assert dec(1, 64, 8, 1, 32768, 64)["merge"] == "combine"
-    # many groups: combine
-    assert dec(4, 64, 8, 1, 32768, 16)["merge"] == "combine"
+    # other single-token calls: the combine merges each group as soon as its partials are
+    # counted in: few groups with short splits (512 keys), many groups
+    assert dec(1, 64, 8, 1, 32768, 64)["merge"] == "combine_per_group"
+    assert dec(4, 64, 8, 1, 32768, 16)["merge"] == "combine_per_group"
+    assert dec(16, 64, 8, 1, 131072, 0)["merge"] == "combine_per_group"
+    # more than 8 rows per KV head: the combine waits for the whole split grid (9 to 15 rows
+    # on the warp-level kernel)
+    assert dec(1, 32, 8, 3, 8192, 0)["merge"] == "combine"
 
 
 def test_kernel_choice_by_rows_per_kv_head():
@@ -131,7 +151,7 @@ def test_plan_agrees_with_workspace_size_and_invariants():
         L, d = rng.randint(1, 200000), rng.choice([64, 128])
         ns = rng.choice([0, 0, 1, 3, 16, 64, 256])
         p = gb.attn_decode_plan(B, G * Hkv, Hkv, Tq, L, d, ns, NSM)
-        rows = B * G * Hkv * Tq * p["splits"]
+        rows = B * G * Hkv * Tq * p["splits"] * p["pieces"]
         n_hc = (G * Tq + 7) // 8
         nci = 4 if n_hc >= 3 else n_hc
         n_hg = (n_hc + nci - 1) // nci
@@ -140,10 +160,19 @@ def test_plan_agrees_with_workspace_size_and_invariants():
         assert gb.attn_decode_workspace_bytes(B, G * Hkv, Hkv, Tq, L, d, ns, NSM) == expect
         assert 1 <= p["splits"] <= 256 and (ns == 0 or p["splits"] == ns)
         per_split = B * Hkv * ((G * Tq + 127) // 128 if p["kernel"] == "tcgen05" else n_hg)
-        assert p["items"] == p["splits"] * per_split
+        assert p["items"] == p["splits"] * p["pieces"] * per_split
         assert p["rows_per_kv_head"] == G * Tq
+        parts = p["splits"] * p["pieces"]
+        assert 1 <= p["pieces"] <= 4 and parts <= 256
+        assert p["pieces"] == 1 or L >= 512 * parts
         lanes = p["combine_lanes"]
-        assert lanes & (lanes - 1) == 0 and 8 * lanes >= p["splits"] and 8 * (lanes // 2) < max(p["splits"], 2)
+        assert lanes & (lanes - 1) == 0 and 8 * lanes >= parts and 8 * (lanes // 2) < max(parts, 2)
+        if p["merge"] == "single_launch":
+            assert p["pieces"] == 1
+        if p["merge"] == "combine_per_group":
+            assert p["kernel"] == "warp" and G * Tq <= 8
+        if p["kernel"] == "warp" and G * Tq <= 8:
+            assert p["merge"] in ("single_launch", "combine_per_group")
         if p["merge"] == "single_launch":
             assert p["kernel"] == "warp" and G * Tq <= 8
         if G * Tq >= 16:
