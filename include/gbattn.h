@@ -30,6 +30,9 @@
  *    sees keys j <= i + Skv - Sq.
  *  - Numerics: bf16 inputs, fp32 scores / running state / accumulators, P rounded to
  *    bf16 for the P.V product, O stored in the input dtype.
+ *  - Each compute call is an NVTX range named after it (attn_fwd, attn_fwd_counted,
+ *    attn_fwd_host, attn_prefill_kvcache, attn_decode), visible to a profiler and free
+ *    without one.
  */
 #ifndef GBATTN_H
 #define GBATTN_H
@@ -322,7 +325,14 @@ int attn_prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int n
  * Returns GBATTN_OK, GBATTN_ERR_TIMEOUT (the word was set) or GBATTN_ERR_CUDA.
  * If detail != NULL it receives the raw word (which wait gave up): 1 producer (free ring
  * slot), 2 consumer (filled slot), 3 MMA issuer, 4 softmax warps, 5 exit drain of
- * in-flight copies, 6 the self-test wait, 7 a decode row's merge waiting for its partials.
+ * in-flight copies, 6 the self-test wait, 7 a decode row's merge waiting for its partials,
+ * 8 a bounds check of a debug build (below) failed.
+ *
+ * Debug build: the library compiled with -DGBATTN_DEBUG_CHECKS (build.py: build(debug=True),
+ * libgbattn_debug.so; same entry points) checks, in every kernel, the index of each plain
+ * global store -- and of the decode merges' partial loads -- against the extent of its
+ * buffer before the access.  A failed check records word 8 and skips that access; nothing
+ * traps.  Release builds contain no checks.
  */
 int attn_last_device_error(void* stream, int* detail);
 

@@ -3,6 +3,10 @@
 Objects go to streaming_attention_flashattention_gb300/_build/, the shared library next
 to this file.  The CUDA runtime is linked statically and the driver's tensor-map encoder
 is looked up at run time, so the library loads on a machine without a GPU driver.
+
+build(debug=True) builds the same sources with -DGBATTN_DEBUG_CHECKS into _build_debug/ and
+libgbattn_debug.so: kernels that check the index of each global store against its buffer
+and record a failed check in the device error word instead of writing (include/gbattn.h).
 """
 from __future__ import annotations
 
@@ -17,6 +21,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgbattn.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libgbattn_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]
@@ -40,33 +46,35 @@ def _headers():
     return hs
 
 
-STAMP = os.path.join(BUILD, "sources.txt")
-
-
 def _source_list() -> str:
     return "\n".join(os.path.basename(f) for f in _sources())
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB) or not os.path.exists(STAMP):
+def up_to_date(debug: bool = False) -> bool:
+    lib, stamp = (LIB_DEBUG, os.path.join(BUILD_DEBUG, "sources.txt")) if debug else \
+        (LIB, os.path.join(BUILD, "sources.txt"))
+    if not os.path.exists(lib) or not os.path.exists(stamp):
         return False
-    with open(STAMP) as f:
+    with open(stamp) as f:
         if f.read() != _source_list():       # a source was added or removed
             return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _sources() + _headers() + [__file__])
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          debug: bool = False) -> str:
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and up_to_date(debug):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
     srcs = _sources()
+    flags = FLAGS + (["-DGBATTN_DEBUG_CHECKS"] if debug else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
         if ptxas_info:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -80,16 +88,17 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for _, log in results:
             if log.strip():
                 print(log, file=sys.stderr)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    with open(STAMP, "w") as f:
+    os.replace(tmp, lib)
+    with open(os.path.join(bdir, "sources.txt"), "w") as f:
         f.write(_source_list())
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas-info" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas-info" in sys.argv,
+                debug="--debug" in sys.argv))

@@ -25,7 +25,8 @@ template <int D>
 __global__ void __launch_bounds__(kWarps * 32)
 attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                     const float* __restrict__ v, float* __restrict__ o, float* __restrict__ lse,
-                    int Hq, int Hkv, int Sq, int Skv, float scale_log2, int causal) {
+                    int Hq, int Hkv, int Sq, int Skv, float scale_log2, int causal,
+                    int* err) {
     constexpr int P = D + 1;  // padded row: lane j reading row j is conflict free
     constexpr int C = D / 32; // output columns per lane
     __shared__ float sq[kRowsPerCta][D];
@@ -109,6 +110,7 @@ attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
     for (int r = 0; r < kRowsPerWarp; ++r) {
         const int i = row0 + warp * kRowsPerWarp + r;
         if (i >= Sq) continue;
+        if (!GBATTN_IN_BOUNDS(q_base + i, (long long)gridDim.z * Hq * Sq, err)) continue;
         const float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
 #pragma unroll
         for (int c = 0; c < C; ++c) o[(q_base + i) * D + lane + 32 * c] = acc[r][c] * inv;
@@ -121,16 +123,16 @@ attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
 
 cudaError_t launch_attn_fwd_f32(const float* q, const float* k, const float* v, float* o,
                                 float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d,
-                                float scale, int causal, cudaStream_t stream) {
+                                float scale, int causal, int* err, cudaStream_t stream) {
     const float scale_log2 = scale * 1.4426950408889634f;
     dim3 grid((Sq + kRowsPerCta - 1) / kRowsPerCta, Hq, B);
     dim3 block(kWarps * 32);
     if (d == 64)
         attn_fwd_f32_kernel<64><<<grid, block, 0, stream>>>(q, k, v, o, lse, Hq, Hkv, Sq, Skv,
-                                                            scale_log2, causal);
+                                                            scale_log2, causal, err);
     else
         attn_fwd_f32_kernel<128><<<grid, block, 0, stream>>>(q, k, v, o, lse, Hq, Hkv, Sq, Skv,
-                                                             scale_log2, causal);
+                                                             scale_log2, causal, err);
     return cudaGetLastError();
 }
 

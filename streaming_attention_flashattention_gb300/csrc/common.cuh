@@ -26,6 +26,7 @@ enum : int {
     kErrWaitDrain = 5,       // drain of in-flight copies at exit gave up
     kErrSelfTest = 6,        // the self-test wait that is never satisfied gave up (expected)
     kErrWaitMerge = 7,       // a decode row's merge gave up waiting for its group's partials
+    kErrBounds = 8,          // debug build: an index fell outside its buffer (access skipped)
 };
 
 // A wait gives up after this many clock cycles (~1 s at 2 GHz).  Correct code never gets
@@ -39,6 +40,23 @@ __device__ __forceinline__ void record_error(int* word, int code) {
 __device__ __forceinline__ bool device_error_set(const int* word) {
     return *((const volatile int*)word) != 0;
 }
+
+// Bounds checks of debug builds.  A library compiled with -DGBATTN_DEBUG_CHECKS checks the
+// index of each plain global store (and of the partial loads of the decode merges) against
+// the extent of its buffer before the access: a failed check records kErrBounds in the
+// error word and the access is skipped -- the kernel never traps.  Release builds compile
+// the checks out (GBATTN_IN_BOUNDS is the constant true).
+__device__ __forceinline__ bool bounds_ok(long long idx, long long extent, int* err_word) {
+    if (idx >= 0 && idx < extent) return true;
+    record_error(err_word, kErrBounds);
+    return false;
+}
+#ifdef GBATTN_DEBUG_CHECKS
+#define GBATTN_IN_BOUNDS(idx, extent, err_word) \
+    (::gbattn::bounds_ok((long long)(idx), (long long)(extent), (err_word)))
+#else
+#define GBATTN_IN_BOUNDS(idx, extent, err_word) true
+#endif
 
 // ---------------------------------------------------------------------------------------
 // Shared-memory addresses and mbarriers

@@ -147,6 +147,7 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 template <int D, int per>
 __device__ __forceinline__ void store_final(const DecodeParams& p, long long row, int d0,
                                             const float* ov, bool with_lse, float lse2) {
+    if (!GBATTN_IN_BOUNDS(row, (long long)p.B * p.Hq * p.Tq, p.err)) return;
     __nv_bfloat16* dst = p.o + row * D + d0;
     if constexpr (per % 8 == 0) {
         #pragma unroll
@@ -171,6 +172,9 @@ __device__ __forceinline__ void store_final(const DecodeParams& p, long long row
 template <int D, int per>
 __device__ __forceinline__ void fold_partials(const DecodeParams& p, long long row, int d0,
                                               int n_ne, bool with_lse) {
+    if (!GBATTN_IN_BOUNDS(row, (long long)p.B * p.Hq * p.Tq, p.err) ||
+        !GBATTN_IN_BOUNDS(n_ne - 1, p.n_parts, p.err))
+        return;
     const float* lse_s = p.ws_lse + row * p.n_parts;
     const float* o_s = p.ws_o + row * p.n_parts * D + d0;
     constexpr int kChunk = 8;
@@ -228,7 +232,9 @@ __device__ __forceinline__ void merge_columns(const DecodeParams& p, long long r
                                               int n_parts, bool active) {
     constexpr int kChunk = 8;
     const int c = p.combine_lanes;
-    const bool merge = active && n_parts > 1;   // (one partial: the split kernel wrote the row)
+    const bool merge = active && n_parts > 1 &&   // (one partial: the split kernel wrote the row)
+                       GBATTN_IN_BOUNDS(row, (long long)p.B * p.Hq * p.Tq, p.err) &&
+                       GBATTN_IN_BOUNDS(n_parts - 1, p.n_parts, p.err);
     float M = -INFINITY, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (merge) {
@@ -372,6 +378,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                     // O = 0, LSE = -inf from its split 0.
                     if (s == 0 && pc == 0) {
                         for (int g = 0; g < gcnt; ++g) {
+                            if (!GBATTN_IN_BOUNDS(row0 + g, (long long)p.B * p.Hq * p.Tq, p.err)) continue;
                             uint4* dst = reinterpret_cast<uint4*>(p.o + (row0 + g) * D);
                             for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
                             if (p.lse != nullptr) p.lse[row0 + g] = -INFINITY;
@@ -385,8 +392,11 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 const int part = s * p.pieces + pc;
                 if (t0 >= t1) {
                     // an empty piece of a non-empty split: a partial that weighs nothing
-                    for (int g = 0; g < gcnt; ++g) p.ws_lse[(row0 + g) * p.n_parts + part] = -INFINITY;
-                    if (p.counted)
+                    for (int g = 0; g < gcnt; ++g)
+                        if (GBATTN_IN_BOUNDS((row0 + g) * p.n_parts + part, (long long)p.B * p.Hq * p.Tq * p.n_parts, p.err))
+                            p.ws_lse[(row0 + g) * p.n_parts + part] = -INFINITY;
+                    if (p.counted && GBATTN_IN_BOUNDS(((long long)b * p.Hkv + kvh) * p.n_hg + hc,
+                                                      (long long)p.B * p.Hkv * p.n_hg, p.err))
                         counter_add_release(p.group_cnt + ((long long)b * p.Hkv + kvh) * p.n_hg + hc, 1);
                     continue;
                 }
@@ -467,7 +477,8 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                     if (!mbar_wait(&pub_full[ps], (k / kPubSlots) & 1, kErrWaitConsumer, p.err)) break;
                     const int g = pub_group[ps];
                     if (g < 0) break;                    // the consumers are done
-                    counter_add_release(p.group_cnt + g, 1);
+                    if (GBATTN_IN_BOUNDS(g, (long long)p.B * p.Hkv * p.n_hg, p.err))
+                        counter_add_release(p.group_cnt + g, 1);
                     mbar_arrive(&pub_empty[ps]);
                 }
             }
@@ -679,7 +690,8 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                     }
                     if (si.direct) {
                         store_final<D, per>(p, row, d0, ov, (t % kThrPerRow) == 0, lse2);
-                    } else {
+                    } else if (GBATTN_IN_BOUNDS(row * p.n_parts + si.s,
+                                                (long long)p.B * p.Hq * p.Tq * p.n_parts, p.err)) {
                         const long long slot = row * p.n_parts + si.s;
                         float* dst = p.ws_o + slot * D + d0;
                         #pragma unroll
@@ -931,7 +943,8 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                         }
                         if (si.direct) {
                             store_final<D, per>(p, row, d0, ov, (t & 15) == 0, lse2);
-                        } else {
+                        } else if (GBATTN_IN_BOUNDS(row * p.n_parts + si.s,
+                                                    (long long)p.B * p.Hq * p.Tq * p.n_parts, p.err)) {
                             const long long slot = row * p.n_parts + si.s;
                             float* dst = p.ws_o + slot * D + d0;
                             #pragma unroll

@@ -172,6 +172,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                     const int nrows = min(kRowsT, p.R - rt * kRowsT);
                     for (int i = lane; i < nrows * (D / 8); i += 32) {
                         const int r = i / (D / 8), c = i % (D / 8);
+                        if (!GBATTN_IN_BOUNDS(row0 + r, (long long)p.B * p.Hq * p.Tq, p.err)) continue;
                         reinterpret_cast<uint4*>(p.o + (row0 + r) * D)[c] = make_uint4(0, 0, 0, 0);
                         if (c == 0 && p.lse != nullptr) p.lse[row0 + r] = -INFINITY;
                     }
@@ -185,7 +186,9 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
             if (t0 >= t1) {
                 // an empty piece of a non-empty split: a partial that weighs nothing
                 const int nrows = min(kRowsT, p.R - rt * kRowsT);
-                for (int i = lane; i < nrows; i += 32) p.ws_lse[(row0 + i) * p.n_parts + part] = -INFINITY;
+                for (int i = lane; i < nrows; i += 32)
+                    if (GBATTN_IN_BOUNDS((row0 + i) * p.n_parts + part, (long long)p.B * p.Hq * p.Tq * p.n_parts, p.err))
+                        p.ws_lse[(row0 + i) * p.n_parts + part] = -INFINITY;
                 continue;
             }
             const int nt = (t1 - t0 + kKeysT - 1) / kKeysT;
@@ -522,9 +525,11 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                 const float a0 = (m0 == -INFINITY) ? 0.f : ex2_approx(m0 - M);
                 const float a1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - M);
                 const float lt = a0 * ls[r] + (n1 > 0 ? a1 * ls[128 + r] : 0.f);
-                const bool live = r < nrows;
                 const long long row0 = ((long long)it.b * p.Hkv + it.kvh) * p.R + (long long)it.rt * kRowsT;
                 const long long row = row0 + r;
+                const bool live = r < nrows &&
+                                  GBATTN_IN_BOUNDS(row * p.n_parts + it.s,
+                                                   (long long)p.B * p.Hq * p.Tq * p.n_parts, p.err);
                 const float inv = lt > 0.f ? 1.f / lt : 0.f;
                 #pragma unroll 1
                 for (int ch = 0; ch < D / 64; ++ch) {

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <algorithm>
 #include <mutex>
 #include <vector>
@@ -91,6 +93,13 @@ __global__ void selftest_wait_kernel(int* err_word, long long limit) {
     fence_barrier_init();
     mbar_wait(&bar, 0, kErrSelfTest, err_word, limit);
 }
+
+// An NVTX range around one library call, so that a profiler's timeline shows the call with
+// the launches it made (without a profiler attached NVTX does nothing).
+struct CallRange {
+    explicit CallRange(const char* name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+};
 
 constexpr long long kIntMax = 2147483647LL;
 constexpr long long kFusedMaxGroups = 16;   // single-launch decode: up to this many groups,
@@ -382,6 +391,7 @@ const char* attn_status_string(int status) {
 int attn_fwd_counted(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                      int Hq, int Hkv, int Sq, int Skv, int d, float scale, int causal,
                      int* s_tiles, void* stream) {
+    CallRange range("attn_fwd_counted");
     if (!s_tiles) return GBATTN_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(s_tiles) & 3u) return GBATTN_ERR_MISALIGNED;
     // the same checks as attn_fwd (bf16)
@@ -406,6 +416,7 @@ int attn_fwd_counted(const void* q, const void* k, const void* v, void* o, float
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
              int Hkv, int Sq, int Skv, int d, float scale, int causal, int dtype,
              void* stream) {
+    CallRange range("attn_fwd");
     if (!q || !k || !v || !o) return GBATTN_ERR_INVALID_ARG;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || d <= 0)
         return GBATTN_ERR_INVALID_ARG;
@@ -425,10 +436,12 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 
     if (dtype == GBATTN_FP32) {
         if (B > 65535 || Hq > 65535) return GBATTN_ERR_TOO_LARGE;
+        int* err = device_error_word();
+        if (!err) return GBATTN_ERR_CUDA;
         cudaError_t e = launch_attn_fwd_f32(static_cast<const float*>(q),
                                             static_cast<const float*>(k),
                                             static_cast<const float*>(v), static_cast<float*>(o),
-                                            lse, B, Hq, Hkv, Sq, Skv, d, scale, causal, st);
+                                            lse, B, Hq, Hkv, Sq, Skv, d, scale, causal, err, st);
         return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
     }
 
@@ -447,6 +460,7 @@ size_t attn_fwd_host_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int
 int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                   int Hq, int Hkv, int Sq, int Skv, int d, float scale, int causal, int dtype,
                   void* workspace, size_t ws_bytes, void* stream) {
+    CallRange range("attn_fwd_host");
     if (!q || !k || !v || !o) return GBATTN_ERR_INVALID_ARG;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || d <= 0)
         return GBATTN_ERR_INVALID_ARG;
@@ -465,6 +479,8 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
     if (!aligned16(workspace)) return GBATTN_ERR_MISALIGNED;
     HostPipe* hp = host_pipe();
     if (!hp) return GBATTN_ERR_CUDA;
+    int* errw = device_error_word();
+    if (!errw) return GBATTN_ERR_CUDA;
     std::lock_guard<std::mutex> lock(hp->mu);
 
     const size_t es = dtype == GBATTN_BF16 ? 2 : 4;
@@ -499,7 +515,8 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
                                      reinterpret_cast<const float*>(base + h.k_off),
                                      reinterpret_cast<const float*>(base + h.v_off),
                                      reinterpret_cast<float*>(base + h.o_off), lse_d, 1, gn * G, gn,
-                                     Sq, Skv, d, scale, causal, st) == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+                                     Sq, Skv, d, scale, causal, errw, st) == cudaSuccess
+                     ? GBATTN_OK : GBATTN_ERR_CUDA;
         } else {
             rc = launch_prefill_bf16(base + h.q_off, base + h.k_off, base + h.v_off, base + h.o_off,
                                      lse_d, 1, gn * G, gn, Sq, Skv, Skv, d, scale, causal, st);
@@ -519,6 +536,7 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
 int attn_prefill_kvcache(const void* q, const void* kcache, const void* vcache, void* o,
                          float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int Lmax, int d,
                          float scale, int causal, void* stream) {
+    CallRange range("attn_prefill_kvcache");
     if (!q || !kcache || !vcache || !o) return GBATTN_ERR_INVALID_ARG;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || Lmax <= 0 || d <= 0)
         return GBATTN_ERR_INVALID_ARG;
@@ -561,6 +579,7 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
                            const int* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
                            int Tq, int Lmax, int d, float scale, int num_splits,
                            void* workspace, size_t ws_bytes, void* stream) {
+    CallRange range("attn_decode");
     if (!q || !kcache || !vcache || !kv_lens || !o) return GBATTN_ERR_INVALID_ARG;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Tq <= 0 || Lmax <= 0 || d <= 0)
         return GBATTN_ERR_INVALID_ARG;

@@ -15,7 +15,7 @@ int* device_error_word();
 // ---- fp32 CUDA-core path (attn_f32.cu) ------------------------------------------------
 cudaError_t launch_attn_fwd_f32(const float* q, const float* k, const float* v, float* o,
                                 float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int d,
-                                float scale, int causal, cudaStream_t stream);
+                                float scale, int causal, int* err, cudaStream_t stream);
 
 // ---- bf16 tcgen05 prefill path (prefill_tcgen05.cu) ------------------------------------
 struct PrefillParams {

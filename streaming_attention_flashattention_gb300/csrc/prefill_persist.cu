@@ -475,14 +475,17 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
                 asm volatile("mov.b32 %0, %1;" : "=r"(k_again) : "r"(k));
                 tile_of(p, k_again, it);
                 const int row = it.q0 + r;
-                if (t == 0 && row < p.Sq && p.lse != nullptr)
+                if (t == 0 && row < p.Sq && p.lse != nullptr &&
+                    GBATTN_IN_BOUNDS(((long long)it.b * p.Hq + it.h) * p.Sq + row,
+                                     (long long)p.B * p.Hq * p.Sq, p.err))
                     p.lse[((long long)it.b * p.Hq + it.h) * p.Sq + row] =
                         lt > 0.f ? (M + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
             }
             // the staged tile is complete once all 256 merge threads pass the barrier
             fence_proxy_async_smem();
             named_barrier_sync(1, 256);
-            if (threadIdx.x == kStoreThread) {
+            if (threadIdx.x == kStoreThread && GBATTN_IN_BOUNDS(it.b * p.Hq + it.h, p.B * p.Hq, p.err) &&
+                GBATTN_IN_BOUNDS(it.q0, p.Sq, p.err)) {
                 #pragma unroll
                 for (int bx = 0; bx < L::kBoxes; ++bx)
                     tma_store_3d(&p.tmap_o, smem + L::kOst + bx * L::kBoxBytes, bx * 64, it.q0,

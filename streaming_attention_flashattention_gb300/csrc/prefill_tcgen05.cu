@@ -452,7 +452,9 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
             if (ok && me.n_kv > 0 && mbar_wait(&o_done[t], (me.n_kv - 1) & 1, kErrWaitSoftmax, p.err)) {
                 tc_fence_after();
                 __nv_bfloat16* orow = p.o + (((long long)b * p.Hq + me.h) * p.Sq + row) * D;
-                const bool live = row < p.Sq;
+                const bool live = row < p.Sq &&
+                                  GBATTN_IN_BOUNDS(((long long)b * p.Hq + me.h) * p.Sq + row,
+                                                   (long long)p.B * p.Hq * p.Sq, p.err);
                 if (kSplit && td[1].present) {
                     // KV split: merge the two halves' states of this row (log-sum-exp):
                     // O = (a0 O0 + a1 O1) / (a0 l0 + a1 l1), a_t = 2^(m_t - max(m0, m1))

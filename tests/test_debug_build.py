@@ -1,0 +1,91 @@
+"""The debug build (-DGBATTN_DEBUG_CHECKS, libgbattn_debug.so): the same entry points, with
+every kernel checking the index of each global store against its buffer (a failed check
+records word 8 in the device error word and skips the access; nothing traps).
+
+On CPU: the debug library builds and exports every declared entry point.  On the GPU:
+ordinary calls of every kernel path run through the debug library in a fresh process,
+match the fp64 oracle within the parity bars, and leave the error word clear."""
+import ctypes
+import os
+import subprocess
+import sys
+import textwrap
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import streaming_attention_flashattention_gb300 as gb  # noqa: E402
+from streaming_attention_flashattention_gb300 import build  # noqa: E402
+
+
+def test_debug_library_exports_every_entry_point():
+    path = build.build(debug=True)
+    assert path.endswith("libgbattn_debug.so")
+    lib = ctypes.CDLL(path)
+    for name in gb.EXPORTS:
+        assert hasattr(lib, name), name
+
+
+SCRIPT = textwrap.dedent(r"""
+    import sys
+    sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+    import numpy as np, torch
+    import attn_workloads as wl, oracle
+    import streaming_attention_flashattention_gb300 as gb
+    from streaming_attention_flashattention_gb300 import build
+    from _parity import compare
+    gb.load_library(build.build(debug=True))
+
+    def prefill(B, Hq, Hkv, S, d, causal, dtype="bf16", seed=1, Skv=None):
+        w = wl.Workload("dbg", "prefill", B=B, Hq=Hq, Hkv=Hkv, d=d, dtype=dtype, Sq=S,
+                        Skv=Skv or S, causal=causal, seed=seed)
+        q, k, v = wl.prefill_inputs(w)
+        o, lse = gb.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=w.scale)
+        torch.cuda.synchronize()
+        rows = np.random.default_rng(seed).integers(0, B * Hq * S, 300)
+        o_ref, l_ref = oracle.attention(wl.to_oracle(q), wl.to_oracle(k), wl.to_oracle(v),
+                                        w.scale, causal, rows=rows)
+        compare(o.float().cpu().numpy().reshape(-1, d)[rows], lse.cpu().numpy().reshape(-1)[rows],
+                o_ref, l_ref, dtype, "prefill")
+
+    def decode(B, Hq, Hkv, L, ns, Tq=1, seed=2):
+        w = wl.Workload("dbg-dec", "decode", B=B, Hq=Hq, Hkv=Hkv, d=128, dtype="bf16", Skv=L,
+                        num_splits=ns, len_lo=L // 3, len_hi=L, Sq=Tq, seed=seed)
+        if Tq == 1:
+            q, kc, vc, kl = wl.decode_inputs(w)
+            o, lse = gb.attn_decode_splitkv(q.cuda(), kc.cuda(), vc.cuda(), kl.cuda(),
+                                            num_splits=ns, scale=w.scale)
+        else:
+            q, kc, vc, kl = wl.multitoken_inputs(w)
+            o, lse = gb.attn_decode_multitoken(q.cuda(), kc.cuda(), vc.cuda(), kl.cuda(),
+                                               num_splits=ns, scale=w.scale)
+        torch.cuda.synchronize()
+        o_ref, l_ref = oracle.attention(wl.to_oracle(q), wl.to_oracle(kc), wl.to_oracle(vc),
+                                        w.scale, Tq > 1, kv_len=kl.numpy())
+        compare(o.float().cpu().numpy().reshape(o_ref.shape), lse.cpu().numpy().reshape(l_ref.shape),
+                o_ref, l_ref, "bf16", "decode")
+
+    prefill(1, 32, 8, 2560, 128, True)            # pairs of Q tiles
+    prefill(1, 32, 8, 4096, 128, False, seed=3)   # pairs plus the KV-split tail launch
+    prefill(2, 8, 2, 2048, 128, True, seed=4)     # persistent KV-split tiles
+    prefill(1, 4, 2, 300, 64, True, seed=5, Skv=700)
+    prefill(1, 2, 1, 128, 64, False, dtype="fp32", seed=6)
+    decode(4, 64, 8, 32768, 16)                   # pieces, per-group combine
+    decode(1, 64, 8, 4096, 0)                     # single launch
+    decode(2, 64, 8, 6000, 3, Tq=4)               # tcgen05 multi-token kernel + combine
+    decode(1, 32, 8, 4096, 0, Tq=3)               # 12 rows on the warp-level kernel
+    st, word = gb.attn_last_device_error()
+    assert st == 0 and word == 0, f"error word {{word}}"
+    print("debug build ok")
+""")
+
+
+@pytest.mark.gpu
+def test_debug_build_runs_every_path_with_the_error_word_clear():
+    script = SCRIPT.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
+    r = subprocess.run([sys.executable, "-c", script], capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
+    assert "debug build ok" in r.stdout
