@@ -27,12 +27,12 @@
  *  - LSE is the natural log of sum_j exp(scale * q . k_j) over the visible keys, fp32.
  *  - A row that sees no key (a decode sequence of length 0) gets O = 0, LSE = -inf.
  *  - Causal masking is bottom-right aligned: query i sits at key position i + Skv - Sq and
- *    sees keys j <= i + Skv - Sq.
+ *    sees keys j <= i + Skv - Sq (attn_fwd_positions takes the positions explicitly).
  *  - Numerics: bf16 inputs, fp32 scores / running state / accumulators, P rounded to
  *    bf16 for the P.V product, O stored in the input dtype.
  *  - Each compute call is an NVTX range named after it (attn_fwd, attn_fwd_counted,
- *    attn_fwd_host, attn_prefill_kvcache, attn_decode), visible to a profiler and free
- *    without one.
+ *    attn_fwd_positions, attn_merge, attn_fwd_host, attn_prefill_kvcache, attn_decode),
+ *    visible to a profiler and free without one.
  */
 #ifndef GBATTN_H
 #define GBATTN_H
@@ -162,6 +162,53 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
 int attn_prefill_kvcache(const void* q, const void* kcache, const void* vcache, void* o,
                          float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int Lmax, int d,
                          float scale, int causal, void* stream);
+
+/*
+ * attn_fwd_positions -- causal attention with explicit positions: query i of the call sits
+ * at position q_pos0 + i and key j at position k_pos0 + j, and a query sees exactly the keys
+ * whose position is not after its own.  "ADR-0060" section 5.4 states the tile classes on
+ * such absolute positions (query block [qs, qe) against KV tile [ks, ke)), and section 5.5
+ * folds the KV slice of each ring step of a sequence-parallel prefill this way.  attn_fwd's
+ * bottom-right causal call is the case q_pos0 = Skv - Sq, k_pos0 = 0.
+ *
+ *   q, k, v, o, lse   as for attn_fwd, bf16 only (lse may be NULL)
+ *   q_pos0, k_pos0    positions of query row 0 and key row 0, each within [-2^40, 2^40];
+ *                     only their difference matters
+ *
+ * A query that sees no key (its position is before k_pos0) gets O = 0 and LSE = -inf, the
+ * neutral element of attn_merge.  Those rows (a prefix of the call's rows) are written by a
+ * fill kernel; the other rows run on attn_fwd's kernels and numerics.  Requirements and
+ * status codes as attn_fwd with dtype GBATTN_BF16, except that Sq > Skv is allowed.
+ */
+int attn_fwd_positions(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int Sq, int Skv, int d, float scale, long long q_pos0,
+                       long long k_pos0, void* stream);
+
+/*
+ * attn_merge -- log-sum-exp merge of two partial attention results over disjoint key sets,
+ * row by row ("ADR-0060" section 4: the merge is associative and commutative, so partials
+ * can be folded in any order, by a chain or by a tree).  With L the rows' log-sum-exp:
+ *     M = max(L_a, L_b),  w_x = e^(L_x - M),
+ *     O = (w_a O_a + w_b O_b) / (w_a + w_b),  L = M + ln(w_a + w_b);
+ * a partial with L = -inf (no key) contributes nothing and its O is not read; if both are
+ * -inf the row is O = 0, L = -inf.
+ *
+ *   o_a, lse_a, dtype_a         first partial: rows x d elements (GBATTN_BF16 or GBATTN_FP32)
+ *                               and rows fp32 LSE values, device
+ *   o_b, lse_b, dtype_b         second partial, likewise
+ *   o_out, lse_out, dtype_out   the merged result (lse_out may be NULL); o_out is o_a, o_b or
+ *                               a buffer disjoint from both, and lse_out likewise, so that a
+ *                               running accumulator can be merged in place
+ *   rows, d                     rows >= 0 (0 launches nothing, and the pointers may then
+ *                               be NULL), d in {64, 128}
+ *
+ * O pointers 16-byte aligned, LSE pointers 4-byte aligned.  An fp32 accumulator keeps a
+ * chain of merges at fp32 precision; a bf16 result rounds once.  Returns GBATTN_OK or a
+ * negative status (nothing launched on error).
+ */
+int attn_merge(const void* o_a, const float* lse_a, int dtype_a, const void* o_b,
+               const float* lse_b, int dtype_b, void* o_out, float* lse_out, int dtype_out,
+               long long rows, int d, void* stream);
 
 /*
  * attn_decode_workspace_size -- bytes of device workspace attn_decode_splitkv needs on the

@@ -23,6 +23,9 @@ Functions:
   attention(...)            plain definition, two-pass stable softmax, fp64 (C, OpenMP)
   attention_probs(...)      the probability matrix P of the same definition (numpy)
   online_attention(...)     the streaming recurrence of [AttnRegion] s.6 / [ADR-0060] s.3
+  attention_at_positions(...)  causal attention with explicit query / key positions
+                            ([ADR-0060] s.5.4 tile classes on absolute positions, s.5.5 ring
+                            steps), via online_attention on one tile per head pair
   merge(...)                [ADR-0060] s.4 merge of two partial states
   split_bounds(...)         contiguous split chunks (reading: [ADR-0060] s.2.1 blocks)
   splitkv_decode(...)       per-split partial states folded with merge()
@@ -229,6 +232,31 @@ def finalize(m, l, O):
     with np.errstate(divide="ignore"):
         lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
     return out, lse
+
+
+def attention_at_positions(q, k, v, scale: float, q_pos0: int, k_pos0: int):
+    """Causal attention with explicit positions: query i sits at q_pos0 + i, key j at
+    k_pos0 + j, and a query sees the keys whose position is not after its own ([ADR-0060]
+    s.5.4 states its tile classes on such absolute positions; s.5.5 folds each ring step's
+    KV slice this way).  Per head pair (GQA: query head h reads KV head h // G) the plain
+    definition in fp64: the whole key range as one tile of online_attention, then finalize;
+    rows that see no key give O = 0, LSE = -inf.
+
+    q [B, Hq, Sq, d], k / v [B, Hkv, Skv, d] stored values (float32 or bf16 bits as uint16).
+    Returns (O float64 [B, Hq, Sq, d], LSE float64 [B, Hq, Sq]).
+    """
+    qf, kf, vf = widen(q), widen(k), widen(v)
+    B, Hq, Sq, d = qf.shape
+    Hkv, Skv = kf.shape[1], kf.shape[2]
+    G = Hq // Hkv
+    O = np.zeros((B, Hq, Sq, d))
+    L = np.zeros((B, Hq, Sq))
+    for b in range(B):
+        for h in range(Hq):
+            st = online_attention(qf[b, h], kf[b, h // G], vf[b, h // G], scale, True,
+                                  max(Skv, 1), key_offset=k_pos0, q_pos0=q_pos0)
+            O[b, h], L[b, h] = finalize(*st)
+    return O, L
 
 
 def merge(m_a, l_a, O_a, m_b, l_b, O_b):

@@ -8,6 +8,8 @@ or was not built for this machine, loading raises.
 Entry points (same names as the C ABI in include/gbattn.h):
   attn_fwd(q, k, v, causal, scale=None, out=None, lse=None)
   attn_fwd_counted(q, k, v, causal, s_tiles, ...)   attn_fwd plus the S tile products issued
+  attn_fwd_positions(q, k, v, q_pos0, k_pos0, ...)  causal attention at explicit positions
+  attn_merge(o_a, lse_a, o_b, lse_b, ...)           log-sum-exp merge of two partials
   attn_decode_splitkv(q, kcache, vcache, kv_lens, num_splits=0, scale=None, ...)
   attn_decode_workspace_size(B, Hq, Hkv, Lmax, d, num_splits)
   attn_last_device_error(stream=None)
@@ -38,9 +40,12 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
 _SZ = ctypes.c_size_t
+_LL = ctypes.c_longlong
 EXPORTS = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "attn_fwd_counted": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P]),
+    "attn_fwd_positions": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _P]),
+    "attn_merge": (_I, [_P, _P, _I, _P, _P, _I, _P, _P, _I, _LL, _I, _P]),
     "attn_fwd_host_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "attn_prefill_kvcache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
@@ -174,6 +179,79 @@ def attn_fwd_counted(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: 
                               1 if causal else 0, s_tiles.data_ptr(), _stream_ptr(stream))
     _check("attn_fwd_counted", st)
     return out, lse
+
+
+def attn_fwd_positions(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_pos0: int,
+                       k_pos0: int, scale: float | None = None, out: torch.Tensor | None = None,
+                       lse: torch.Tensor | None = None, stream=None):
+    """Causal attention with query i at position q_pos0 + i and key j at k_pos0 + j (a query
+    sees the keys not after it); bf16 BHSD tensors.  Rows that see no key get O = 0 and
+    LSE = -inf.  Returns (out, lse)."""
+    lib = load_library()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _dev_tensor(n, t, (torch.bfloat16,))
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("expected q [B,Hq,Sq,d] and k, v [B,Hkv,Skv,d]")
+    B, Hq, Sq, d = q.shape
+    _, Hkv, Skv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _dev_tensor("out", out, (torch.bfloat16,))
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    else:
+        _dev_tensor("lse", lse, (torch.float32,))
+        if tuple(lse.shape) != (B, Hq, Sq):
+            raise ValueError("lse must be [B, Hq, Sq]")
+    st = lib.attn_fwd_positions(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                lse.data_ptr(), B, Hq, Hkv, Sq, Skv, d, float(scale),
+                                int(q_pos0), int(k_pos0), _stream_ptr(stream))
+    _check("attn_fwd_positions", st)
+    return out, lse
+
+
+_DT = {torch.bfloat16: GBATTN_BF16, torch.float32: GBATTN_FP32}
+
+
+def attn_merge(o_a: torch.Tensor, lse_a: torch.Tensor, o_b: torch.Tensor, lse_b: torch.Tensor,
+               out: torch.Tensor | None = None, lse_out: torch.Tensor | None = None,
+               out_dtype: torch.dtype = torch.float32, stream=None):
+    """Log-sum-exp merge of two partial results over disjoint key sets, row by row.
+
+    o_a, o_b [..., d] (bf16 or fp32), lse_a, lse_b [...] fp32.  out (dtype out_dtype, or
+    out.dtype when given) and lse_out may be o_a / lse_a or o_b / lse_b for an in-place
+    accumulator.  Returns (out, lse_out)."""
+    lib = load_library()
+    for n, t in (("o_a", o_a), ("o_b", o_b)):
+        _dev_tensor(n, t, tuple(_DT))
+    for n, t in (("lse_a", lse_a), ("lse_b", lse_b)):
+        _dev_tensor(n, t, (torch.float32,))
+    if o_a.shape != o_b.shape or lse_a.shape != lse_b.shape or o_a.shape[:-1] != lse_a.shape:
+        raise ValueError("o_a, o_b must be [..., d] and lse_a, lse_b [...] of the same rows")
+    d = o_a.shape[-1]
+    rows = lse_a.numel()
+    if out is None:
+        out = torch.empty(o_a.shape, dtype=out_dtype, device=o_a.device)
+    else:
+        _dev_tensor("out", out, tuple(_DT))
+        if out.shape != o_a.shape:
+            raise ValueError("out must have o_a's shape")
+    if lse_out is None:
+        lse_out = torch.empty(lse_a.shape, dtype=torch.float32, device=o_a.device)
+    else:
+        _dev_tensor("lse_out", lse_out, (torch.float32,))
+        if lse_out.shape != lse_a.shape:
+            raise ValueError("lse_out must have lse_a's shape")
+    st = lib.attn_merge(o_a.data_ptr(), lse_a.data_ptr(), _DT[o_a.dtype], o_b.data_ptr(),
+                        lse_b.data_ptr(), _DT[o_b.dtype], out.data_ptr(), lse_out.data_ptr(),
+                        _DT[out.dtype], rows, d, _stream_ptr(stream))
+    _check("attn_merge", st)
+    return out, lse_out
 
 
 def _host_tensor(name: str, t: torch.Tensor, dtypes):

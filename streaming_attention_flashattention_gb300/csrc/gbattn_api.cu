@@ -121,10 +121,13 @@ struct PrefillPlan {
     long long tail;          // pairs run as KV-split tiles in a second launch
 };
 
-PrefillPlan prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int nsm) {
+// diag: causal diagonal (key j visible to query row i iff j <= i + diag); row0: the first
+// query row the Q tiles cover (every row from row0 on sees at least one key).
+PrefillPlan prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int nsm,
+                         int diag, int row0) {
     PrefillPlan pl{};
     const int G = Hq / Hkv;
-    pl.n_qblk = (Sq + 127) / 128;
+    pl.n_qblk = (Sq - row0 + 127) / 128;
     const long long per_group = ((long long)pl.n_qblk * G + 1) / 2;
     pl.n_pairs = per_group * B * Hkv;
     pl.n_tiles = (long long)pl.n_qblk * B * Hq;
@@ -143,10 +146,11 @@ PrefillPlan prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, in
         auto kv_tiles = [&](long long q0) {
             if (!causal) return ((long long)Skv + 127) / 128;
             const long long last = std::min<long long>(q0 + 128, Sq) - 1;
-            const long long keys = std::min<long long>(Skv, last + (Skv - Sq) + 1);
+            const long long keys = std::min<long long>(Skv, last + diag + 1);
             return (keys + 127) / 128;
         };
-        const long long lo = kv_tiles(0), hi = kv_tiles((long long)(pl.n_qblk - 1) * 128);
+        const long long lo = kv_tiles(row0),
+                        hi = kv_tiles(row0 + (long long)(pl.n_qblk - 1) * 128);
         const long long rem = pl.n_pairs % nsm;
         if (lo > 0 && 4 * hi <= 5 * lo && rem > 0 && rem <= nsm / 2) pl.tail = rem;
     }
@@ -155,10 +159,12 @@ PrefillPlan prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, in
 }
 
 // bf16 tcgen05 prefill; K/V rows of one head are `kv_stride` rows apart (>= Skv).
+// diag, row0: as for prefill_plan (bottom-right causal: Skv - Sq and 0).
 // tiles: null, or a device counter that receives the S tile products the kernels issue.
 int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int Hq, int Hkv, int Sq, int Skv, int kv_stride, int d, float scale,
-                        int causal, cudaStream_t st, int* tiles = nullptr) {
+                        int causal, int diag, int row0, cudaStream_t st,
+                        int* tiles = nullptr) {
     PrefillParams p{};
     if (!make_map_bf16_3d(&p.tmap_q, q, d, Sq, (uint64_t)B * Hq, 128) ||
         !make_map_bf16_3d(&p.tmap_k, k, d, Skv, (uint64_t)B * Hkv, 128, kv_stride) ||
@@ -171,13 +177,15 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, fl
     p.G = Hq / Hkv;
     const int nsm = sm_count();
     if (nsm <= 0) return GBATTN_ERR_CUDA;
-    const PrefillPlan pl = prefill_plan(B, Hq, Hkv, Sq, Skv, causal, nsm);
+    const PrefillPlan pl = prefill_plan(B, Hq, Hkv, Sq, Skv, causal, nsm, diag, row0);
     if (pl.n_pairs > kIntMax || pl.n_tiles > kIntMax) return GBATTN_ERR_TOO_LARGE;
     p.n_qblk = pl.n_qblk;
     p.kv_split = pl.kv_split ? 1 : 0;
     p.n_pairs = (int)(pl.kv_split ? pl.n_tiles : pl.first);
     p.tail0 = -1;
     p.causal = causal;
+    p.diag = diag;
+    p.row0 = row0;
     p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = device_error_word();
@@ -410,7 +418,7 @@ int attn_fwd_counted(const void* q, const void* k, const void* v, void* o, float
         (long long)B * Hkv * Skv > kIntMax)
         return GBATTN_ERR_TOO_LARGE;
     return launch_prefill_bf16(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, Skv, d, scale, causal,
-                               static_cast<cudaStream_t>(stream), s_tiles);
+                               Skv - Sq, 0, static_cast<cudaStream_t>(stream), s_tiles);
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
@@ -445,7 +453,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
         return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
     }
 
-    return launch_prefill_bf16(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, Skv, d, scale, causal, st);
+    return launch_prefill_bf16(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, Skv, d, scale, causal,
+                               Skv - Sq, 0, st);
 }
 
 size_t attn_fwd_host_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int d, int dtype) {
@@ -519,7 +528,8 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
                      ? GBATTN_OK : GBATTN_ERR_CUDA;
         } else {
             rc = launch_prefill_bf16(base + h.q_off, base + h.k_off, base + h.v_off, base + h.o_off,
-                                     lse_d, 1, gn * G, gn, Sq, Skv, Skv, d, scale, causal, st);
+                                     lse_d, 1, gn * G, gn, Sq, Skv, Skv, d, scale, causal,
+                                     Skv - Sq, 0, st);
         }
         if (rc != GBATTN_OK) return rc;
         ok = chk(cudaEventRecord(hp->ev_comp[bset], st)) &&
@@ -551,7 +561,68 @@ int attn_prefill_kvcache(const void* q, const void* kcache, const void* vcache, 
     if ((long long)B * Hq * Sq > kIntMax || (long long)B * Hkv * Lmax > kIntMax)
         return GBATTN_ERR_TOO_LARGE;
     return launch_prefill_bf16(q, kcache, vcache, o, lse, B, Hq, Hkv, Sq, Skv, Lmax, d, scale,
-                               causal, static_cast<cudaStream_t>(stream));
+                               causal, Skv - Sq, 0, static_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_positions(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int Sq, int Skv, int d, float scale, long long q_pos0,
+                       long long k_pos0, void* stream) {
+    CallRange range("attn_fwd_positions");
+    if (!q || !k || !v || !o) return GBATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || d <= 0)
+        return GBATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return GBATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || scale != scale) return GBATTN_ERR_INVALID_ARG;
+    constexpr long long kPosMax = 1LL << 40;
+    if (q_pos0 < -kPosMax || q_pos0 > kPosMax || k_pos0 < -kPosMax || k_pos0 > kPosMax)
+        return GBATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return GBATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (lse && !aligned16(lse)))
+        return GBATTN_ERR_MISALIGNED;
+    if ((long long)B * Hq > 65535LL * 65535LL || (long long)B * Hq * Sq > kIntMax ||
+        (long long)B * Hkv * Skv > kIntMax)
+        return GBATTN_ERR_TOO_LARGE;
+    // query row i sees key j iff j <= i + diag; beyond [-Sq, Skv] the clamp changes nothing
+    // (every row sees all keys, or none)
+    const int diag = (int)std::max<long long>(-(long long)Sq,
+                                              std::min<long long>(Skv, q_pos0 - k_pos0));
+    const int row0 = std::min(Sq, std::max(0, -diag));   // rows [0, row0) see no key
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int nsm = sm_count();
+    if (nsm <= 0) return GBATTN_ERR_CUDA;
+    if (row0 > 0 &&
+        launch_fill_empty_rows(static_cast<__nv_bfloat16*>(o), lse, (long long)B * Hq, Sq, row0,
+                               d, nsm, st) != cudaSuccess)
+        return GBATTN_ERR_CUDA;
+    if (row0 == Sq) return GBATTN_OK;
+    return launch_prefill_bf16(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, Skv, d, scale, 1, diag, row0,
+                               st);
+}
+
+int attn_merge(const void* o_a, const float* lse_a, int dtype_a, const void* o_b,
+               const float* lse_b, int dtype_b, void* o_out, float* lse_out, int dtype_out,
+               long long rows, int d, void* stream) {
+    CallRange range("attn_merge");
+    auto dtype_ok = [](int t) { return t == GBATTN_BF16 || t == GBATTN_FP32; };
+    if (!dtype_ok(dtype_a) || !dtype_ok(dtype_b) || !dtype_ok(dtype_out))
+        return GBATTN_ERR_INVALID_ARG;
+    if (rows < 0 || d <= 0) return GBATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return GBATTN_ERR_UNSUPPORTED;
+    if (rows == 0) return GBATTN_OK;             // nothing to read or write
+    if (!o_a || !lse_a || !o_b || !lse_b || !o_out) return GBATTN_ERR_INVALID_ARG;
+    if (!aligned16(o_a) || !aligned16(o_b) || !aligned16(o_out) ||
+        (reinterpret_cast<uintptr_t>(lse_a) & 3u) || (reinterpret_cast<uintptr_t>(lse_b) & 3u) ||
+        (reinterpret_cast<uintptr_t>(lse_out) & 3u))
+        return GBATTN_ERR_MISALIGNED;
+    if (rows > (1LL << 40)) return GBATTN_ERR_TOO_LARGE;
+    const int nsm = sm_count();
+    if (nsm <= 0) return GBATTN_ERR_CUDA;
+    return launch_attn_merge(o_a, lse_a, dtype_a == GBATTN_FP32, o_b, lse_b,
+                             dtype_b == GBATTN_FP32, o_out, lse_out, dtype_out == GBATTN_FP32,
+                             rows, d, nsm, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GBATTN_OK
+               : GBATTN_ERR_CUDA;
 }
 
 size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Tq, int Lmax, int d,
@@ -714,7 +785,7 @@ int attn_prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int n
         return GBATTN_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return GBATTN_ERR_INVALID_ARG;
     if (causal && Sq > Skv) return GBATTN_ERR_UNSUPPORTED;
-    const PrefillPlan pl = prefill_plan(B, Hq, Hkv, Sq, Skv, causal, num_sms);
+    const PrefillPlan pl = prefill_plan(B, Hq, Hkv, Sq, Skv, causal, num_sms, Skv - Sq, 0);
     if (pl.n_pairs > kIntMax || pl.n_tiles > kIntMax) return GBATTN_ERR_TOO_LARGE;
     plan[0] = pl.kv_split ? 1 : 0;
     plan[1] = (int)pl.first;

@@ -34,6 +34,10 @@ struct PrefillParams {
     int tail0;            // KV split: -1, or the first pair whose two Q tiles the CTAs take
                           // (the last, partly filled wave of a pair-mode call)
     int causal;
+    int diag;             // causal: key j is visible to query row i iff j <= i + diag
+                          // (bottom-right alignment: diag = Skv - Sq)
+    int row0;             // first query row the Q tiles cover (tile q0 = row0 + 128 * block);
+                          // rows [0, row0) see no key and are written by the row-fill kernel
     int o_align32;        // o is 32-byte aligned: the epilogue may use 32-byte stores
     float scale_log2;     // scale * log2(e)
     int* err;             // device error word of bounded waits
@@ -50,6 +54,16 @@ cudaError_t launch_attn_fwd_bf16_tail(const PrefillParams& p, int d, cudaStream_
 // min(p.n_pairs, nsm) persistent CTAs; each tile's KV range is split over a CTA's two slots.
 cudaError_t launch_attn_fwd_bf16_persistent(const PrefillParams& p, int d, int nsm,
                                             cudaStream_t stream);
+
+// ---- log-sum-exp merge and empty-row fill (attn_merge.cu) -------------------------------
+// (O_out, L_out) = merge((O_a, L_a), (O_b, L_b)) row by row; each O is rows x d, fp32 or bf16
+// as flagged; lo may be null; oo may alias oa or ob, lo may alias la or lb.  d in {64, 128}.
+cudaError_t launch_attn_merge(const void* oa, const float* la, bool a_f32, const void* ob,
+                              const float* lb, bool b_f32, void* oo, float* lo, bool out_f32,
+                              long long rows, int d, int nsm, cudaStream_t st);
+// Rows [0, row0) of each of the bh (batch, head) blocks of Sq rows: O = 0, LSE = -inf.
+cudaError_t launch_fill_empty_rows(__nv_bfloat16* o, float* lse, long long bh, int Sq, int row0,
+                                   int d, int nsm, cudaStream_t st);
 
 // ---- bf16 split-KV decode path (decode_splitkv.cu) --------------------------------------
 struct DecodeParams {

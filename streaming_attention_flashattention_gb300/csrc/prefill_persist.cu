@@ -85,12 +85,12 @@ struct QTile {
     int b, h, q0, n;
 };
 
-// KV tiles a Q tile starting at q0 visits: all of them, or (causal, bottom-right) those up
-// to the last row's position.
+// KV tiles a Q tile starting at q0 visits: all of them, or (causal) those up to the last
+// row's diagonal (row + diag).
 __device__ __forceinline__ int kv_tiles(const PrefillParams& p, int q0) {
     if (!p.causal) return (p.Skv + kBlockN - 1) / kBlockN;
     const int last_row = min(q0 + kBlockM, p.Sq) - 1;
-    const int keys = min(p.Skv, last_row + (p.Skv - p.Sq) + 1);
+    const int keys = min(p.Skv, last_row + p.diag + 1);
     return (keys + kBlockN - 1) / kBlockN;
 }
 
@@ -106,7 +106,7 @@ __device__ __forceinline__ bool tile_of(const PrefillParams& p, int k, QTile& t)
     const int bh = rank % bh_count;
     t.b = bh / p.Hq;
     t.h = bh % p.Hq;
-    t.q0 = qb * kBlockM;
+    t.q0 = p.row0 + qb * kBlockM;
     t.n = kv_tiles(p, t.q0);
     return true;
 }
@@ -339,7 +339,7 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
             const int kv0 = t == 0 ? 0 : n0;
             const int row = it.q0 + r;                  // query index
             int lim = p.Skv;                            // keys [0, lim) visible
-            if (p.causal) lim = min(lim, row + (p.Skv - p.Sq) + 1);
+            if (p.causal) lim = min(lim, row + p.diag + 1);
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < n_t; ++j) {
                 if (!mbar_wait(&s_full[t], (cs + j) & 1, kErrWaitSoftmax, p.err)) { ok = false; break; }

@@ -79,7 +79,7 @@ struct TileDesc {
 __device__ __forceinline__ int kv_tiles_of(const PrefillParams& p, int q0) {
     if (!p.causal) return (p.Skv + kBlockN - 1) / kBlockN;
     const int last_row = min(q0 + kBlockM, p.Sq) - 1;
-    const int keys = min(p.Skv, last_row + (p.Skv - p.Sq) + 1);
+    const int keys = min(p.Skv, last_row + p.diag + 1);
     return (keys + kBlockN - 1) / kBlockN;
 }
 
@@ -114,7 +114,7 @@ __device__ __forceinline__ void pair_tiles(const PrefillParams& p, int rank, int
         t[i].present = u < cnt;
         const int qb = u / p.G, gi = u % p.G;
         t[i].h = kvh * p.G + gi;
-        t[i].q0 = qb * kBlockM;
+        t[i].q0 = p.row0 + qb * kBlockM;
         t[i].n_kv = t[i].present ? kv_tiles_of(p, t[i].q0) : 0;
         t[i].kv0 = 0;
     }
@@ -372,7 +372,7 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
             const int row = me.q0 + r;                  // query index
             const float c = p.scale_log2;
             int lim = p.Skv;                            // keys [0, lim) visible
-            if (p.causal) lim = min(lim, row + (p.Skv - p.Sq) + 1);
+            if (p.causal) lim = min(lim, row + p.diag + 1);
             const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
             const uint32_t t_s = tmem + lane_off + (t == 0 ? L::kColS0 : L::kColS1);
             const uint32_t t_o = tmem + lane_off + (t == 0 ? L::kColO0 : L::kColO1);

@@ -181,3 +181,37 @@ def test_host_workspace_size_rejects_invalid_sizes(lib):
     assert f(1, 8, 3, 128, 128, 128) == 0          # Hq % Hkv != 0
     assert f(1, 8, 2, 128, 128, 96) == 0           # d not 64 / 128
     assert f(1, 8, 2, 128, 128, 128, 7) == 0       # dtype
+
+
+def test_positions_argument_validation(lib):
+    def pos(q=A, k=A, v=A, o=B_, lse=None, B=1, Hq=2, Hkv=1, Sq=128, Skv=128, d=128, scale=0.1,
+            qp=0, kp=0):
+        return lib.attn_fwd_positions(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, d, scale, qp, kp,
+                                      None)
+    assert pos(q=None) == -1
+    assert pos(Sq=0) == -1
+    assert pos(Hq=3, Hkv=2) == -1
+    assert pos(scale=-1.0) == -1
+    assert pos(qp=1 << 41) == -1
+    assert pos(kp=-(1 << 41)) == -1
+    assert pos(d=96) == -2
+    assert pos(o=MIS) == -3
+    assert pos(B=70000, Hq=70000, Hkv=70000) == -7
+
+
+def test_merge_argument_validation(lib):
+    def mg(oa=A, la=A, ta=0, ob=A, lb=A, tb=0, oo=B_, lo=None, to=1, rows=10, d=128):
+        return lib.attn_merge(oa, la, ta, ob, lb, tb, oo, lo, to, rows, d, None)
+    assert mg(oa=None) == -1
+    assert mg(lb=None) == -1
+    assert mg(oo=None) == -1
+    assert mg(ta=7) == -1
+    assert mg(to=-1) == -1
+    assert mg(rows=-1) == -1
+    assert mg(d=0) == -1
+    assert mg(d=32) == -2
+    assert mg(ob=MIS) == -3
+    assert mg(la=A + 2) == -3
+    assert mg(rows=1 << 41) == -7
+    assert mg(rows=0) == 0            # nothing to do, nothing launched
+    assert mg(oa=None, ob=None, la=None, lb=None, oo=None, rows=0) == 0

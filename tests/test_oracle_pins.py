@@ -11,7 +11,11 @@ a wrong index or a transposed operand):
   * the streaming recurrence of "AttentionRegion Transformation" section 6 / "ADR-0060"
     section 3 equals the two-pass definition for several tile sizes;
   * split-KV partial states merged with the log-sum-exp merge of "ADR-0060" section 4
-    equal the unsplit result, empty splits included.
+    equal the unsplit result, empty splits included;
+  * attention at explicit positions: the bottom-right case equals the C definition, all
+    keys visible equals torch SDPA, brute force with positions on tiny shapes, a common
+    shift of both positions changes nothing, and two key ranges at their positions merged
+    equal the whole range.
 """
 import math
 import os
@@ -400,3 +404,92 @@ def test_planted_transposed_operand_is_caught():
     k = mat(vals["k"])[None, None]
     o_bad, _ = oracle.attention(q, k, k, 0.5, False)
     assert np.max(np.abs(o_bad[0, 0, 0] - ev(vals["noncausal.O0"]))) > 1e-2
+
+
+# ---------------------------------------------------------------------------------------
+# attention at explicit positions
+# ---------------------------------------------------------------------------------------
+
+def brute_positions(q, k, v, scale, q_pos0, k_pos0):
+    B, Hq, Sq, d = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    O = np.zeros((B, Hq, Sq, d))
+    L = np.full((B, Hq, Sq), -math.inf)
+    for b in range(B):
+        for h in range(Hq):
+            for i in range(Sq):
+                ws = [(j, scale * sum(float(q[b, h, i, c]) * float(k[b, h // G, j, c])
+                                      for c in range(d)))
+                      for j in range(Skv) if k_pos0 + j <= q_pos0 + i]
+                if not ws:
+                    continue
+                mx = max(s for _, s in ws)
+                z = sum(math.exp(s - mx) for _, s in ws)
+                for c in range(d):
+                    O[b, h, i, c] = sum(math.exp(s - mx) / z * float(v[b, h // G, j, c])
+                                        for j, s in ws)
+                L[b, h, i] = mx + math.log(z)
+    return O, L
+
+
+@pytest.mark.parametrize("q_pos0,k_pos0", [(0, 0), (4, 0), (0, 3), (2, 5), (-3, -1),
+                                           (10, 0), (0, 10), (7, 7)])
+def test_positions_brute_force_tiny(q_pos0, k_pos0):
+    q = rnd((1, 4, 5, 3), 90)
+    k = rnd((1, 2, 6, 3), 91)
+    v = rnd((1, 2, 6, 3), 92)
+    o, lse = oracle.attention_at_positions(q, k, v, 0.6, q_pos0, k_pos0)
+    o_b, lse_b = brute_positions(q, k, v, 0.6, q_pos0, k_pos0)
+    np.testing.assert_allclose(o, o_b, rtol=0, atol=1e-12)
+    assert np.array_equal(np.isinf(lse), np.isinf(lse_b))
+    fin = np.isfinite(lse_b)
+    np.testing.assert_allclose(lse[fin], lse_b[fin], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("Sq,Skv", [(37, 80), (80, 80), (1, 9)])
+def test_positions_bottom_right_equals_c_definition(Sq, Skv):
+    q = rnd((2, 4, Sq, 16), 93)
+    k = rnd((2, 2, Skv, 16), 94)
+    v = rnd((2, 2, Skv, 16), 95)
+    o, lse = oracle.attention(q, k, v, 0.3, True)
+    for shift in (0, 1000):
+        o2, lse2 = oracle.attention_at_positions(q, k, v, 0.3, Skv - Sq + shift, shift)
+        np.testing.assert_allclose(o2, o, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-12)
+
+
+def test_positions_all_visible_equals_sdpa_noncausal():
+    q = rnd((1, 4, 33, 16), 96)
+    k = rnd((1, 2, 50, 16), 97)
+    v = rnd((1, 2, 50, 16), 98)
+    o_ref, lse_ref = sdpa_ref(q, k, v, 0.25, False)
+    o, lse = oracle.attention_at_positions(q, k, v, 0.25, 49, 0)     # row 0 already sees all
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def test_positions_no_visible_key():
+    q = rnd((1, 2, 10, 8), 99)
+    k = rnd((1, 1, 12, 8), 100)
+    v = rnd((1, 1, 12, 8), 101)
+    o, lse = oracle.attention_at_positions(q, k, v, 0.5, 0, 10)      # keys start after row 9
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+
+
+@pytest.mark.parametrize("cut", [1, 40, 64, 99])
+def test_positions_key_ranges_merge_to_whole(cut):
+    """Keys [0, cut) and [cut, n) at their own positions, merged with the section-4 merge,
+    equal the whole range: what a ring step and attn_merge compute."""
+    Sq, n, d = 30, 100, 16
+    q = rnd((1, 2, Sq, d), 102)
+    k = rnd((1, 1, n, d), 103)
+    v = rnd((1, 1, n, d), 104)
+    qp = 70                                   # queries at positions 70 .. 99
+    o, lse = oracle.attention_at_positions(q, k, v, 0.2, qp, 0)
+    oa, la = oracle.attention_at_positions(q, k[:, :, :cut], v[:, :, :cut], 0.2, qp, 0)
+    ob, lb = oracle.attention_at_positions(q, k[:, :, cut:], v[:, :, cut:], 0.2, qp, cut)
+    m, l, om = oracle.merge(la, np.ones_like(la), oa, lb, np.ones_like(lb), ob)
+    o2, lse2 = oracle.finalize(m, l, om)
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-12)
