@@ -48,7 +48,7 @@ template <> struct Vec4<__nv_bfloat16> {
 template <typename TA, typename TB, typename TO>
 __global__ void __launch_bounds__(256)
 merge_kernel(const TA* oa, const float* la, const TB* ob, const float* lb, TO* oo, float* lo,
-             long long rows, int d) {
+             long long rows, int d, int* err) {
     const int lane = threadIdx.x & 31;
     const int lpr = d >> 2;                          // lanes per row
     const int rpw = 32 / lpr;                        // rows per warp
@@ -81,34 +81,38 @@ merge_kernel(const TA* oa, const float* la, const TB* ob, const float* lb, TO* o
         if (w_b > 0.f) Vec4<TB>::load(ob + row * d + col, vb);
         #pragma unroll
         for (int e = 0; e < 4; ++e) r[e] = (w_a * va[e] + w_b * vb[e]) * inv;
-        Vec4<TO>::store(oo + row * d + col, r);
-        if (lo != nullptr && lane % lpr == 0) lo[row] = s > 0.f ? M + logf(s) : -INFINITY;
+        if (GBATTN_IN_BOUNDS(row * d + col + 3, rows * d, err)) Vec4<TO>::store(oo + row * d + col, r);
+        if (lo != nullptr && lane % lpr == 0 && GBATTN_IN_BOUNDS(row, rows, err))
+            lo[row] = s > 0.f ? M + logf(s) : -INFINITY;
     }
 }
 
 template <typename TA, typename TB, typename TO>
 cudaError_t launch_merge_t(const void* oa, const float* la, const void* ob, const float* lb,
-                           void* oo, float* lo, long long rows, int d, int nsm, cudaStream_t st) {
+                           void* oo, float* lo, long long rows, int d, int nsm, int* err,
+                           cudaStream_t st) {
     constexpr int kThreads = 256;
     const long long units = (rows + (128 / d) - 1) / (128 / d);
     const long long blocks = std::min<long long>((units + 7) / 8, (long long)nsm * 8);
     merge_kernel<TA, TB, TO><<<(unsigned)std::max<long long>(blocks, 1), kThreads, 0, st>>>(
         static_cast<const TA*>(oa), la, static_cast<const TB*>(ob), lb, static_cast<TO*>(oo), lo,
-        rows, d);
+        rows, d, err);
     return cudaGetLastError();
 }
 
 template <typename TA, typename TB>
 cudaError_t launch_merge_ab(const void* oa, const float* la, const void* ob, const float* lb,
                             void* oo, float* lo, bool out_f32, long long rows, int d, int nsm,
-                            cudaStream_t st) {
-    return out_f32 ? launch_merge_t<TA, TB, float>(oa, la, ob, lb, oo, lo, rows, d, nsm, st)
-                   : launch_merge_t<TA, TB, __nv_bfloat16>(oa, la, ob, lb, oo, lo, rows, d, nsm, st);
+                            int* err, cudaStream_t st) {
+    return out_f32 ? launch_merge_t<TA, TB, float>(oa, la, ob, lb, oo, lo, rows, d, nsm, err, st)
+                   : launch_merge_t<TA, TB, __nv_bfloat16>(oa, la, ob, lb, oo, lo, rows, d, nsm, err,
+                                                          st);
 }
 
 // Rows [0, row0) of every (batch, head): O = 0, L = -inf.  One thread per 16 bytes of O.
 __global__ void __launch_bounds__(256)
-fill_empty_rows_kernel(__nv_bfloat16* o, float* lse, long long bh, int Sq, int row0, int d) {
+fill_empty_rows_kernel(__nv_bfloat16* o, float* lse, long long bh, int Sq, int row0, int d,
+                       int* err) {
     const int chunks = d / 8;                        // 16-byte chunks per row
     const long long total = bh * row0 * chunks;
     const long long stride = (long long)gridDim.x * blockDim.x;
@@ -117,8 +121,9 @@ fill_empty_rows_kernel(__nv_bfloat16* o, float* lse, long long bh, int Sq, int r
         const int c = (int)(i % chunks);
         const long long head = r / row0, row = r % row0;
         const long long g = head * Sq + row;
-        *reinterpret_cast<uint4*>(o + g * d + c * 8) = make_uint4(0u, 0u, 0u, 0u);
-        if (lse != nullptr && c == 0) lse[g] = -INFINITY;
+        if (GBATTN_IN_BOUNDS(g * d + c * 8 + 7, bh * Sq * d, err))
+            *reinterpret_cast<uint4*>(o + g * d + c * 8) = make_uint4(0u, 0u, 0u, 0u);
+        if (lse != nullptr && c == 0 && GBATTN_IN_BOUNDS(g, bh * Sq, err)) lse[g] = -INFINITY;
     }
 }
 
@@ -126,24 +131,24 @@ fill_empty_rows_kernel(__nv_bfloat16* o, float* lse, long long bh, int Sq, int r
 
 cudaError_t launch_attn_merge(const void* oa, const float* la, bool a_f32, const void* ob,
                               const float* lb, bool b_f32, void* oo, float* lo, bool out_f32,
-                              long long rows, int d, int nsm, cudaStream_t st) {
+                              long long rows, int d, int nsm, int* err, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
+    using bf = __nv_bfloat16;
     if (a_f32)
-        return b_f32 ? launch_merge_ab<float, float>(oa, la, ob, lb, oo, lo, out_f32, rows, d, nsm, st)
-                     : launch_merge_ab<float, __nv_bfloat16>(oa, la, ob, lb, oo, lo, out_f32, rows, d,
-                                                             nsm, st);
-    return b_f32 ? launch_merge_ab<__nv_bfloat16, float>(oa, la, ob, lb, oo, lo, out_f32, rows, d,
-                                                         nsm, st)
-                 : launch_merge_ab<__nv_bfloat16, __nv_bfloat16>(oa, la, ob, lb, oo, lo, out_f32,
-                                                                 rows, d, nsm, st);
+        return b_f32 ? launch_merge_ab<float, float>(oa, la, ob, lb, oo, lo, out_f32, rows, d, nsm,
+                                                     err, st)
+                     : launch_merge_ab<float, bf>(oa, la, ob, lb, oo, lo, out_f32, rows, d, nsm,
+                                                  err, st);
+    return b_f32 ? launch_merge_ab<bf, float>(oa, la, ob, lb, oo, lo, out_f32, rows, d, nsm, err, st)
+                 : launch_merge_ab<bf, bf>(oa, la, ob, lb, oo, lo, out_f32, rows, d, nsm, err, st);
 }
 
 cudaError_t launch_fill_empty_rows(__nv_bfloat16* o, float* lse, long long bh, int Sq, int row0,
-                                   int d, int nsm, cudaStream_t st) {
+                                   int d, int nsm, int* err, cudaStream_t st) {
     if (bh <= 0 || row0 <= 0) return cudaSuccess;
     const long long total = bh * row0 * (d / 8);
     const long long blocks = std::min<long long>((total + 255) / 256, (long long)nsm * 8);
-    fill_empty_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(o, lse, bh, Sq, row0, d);
+    fill_empty_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(o, lse, bh, Sq, row0, d, err);
     return cudaGetLastError();
 }
 

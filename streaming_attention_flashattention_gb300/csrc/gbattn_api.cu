@@ -591,9 +591,11 @@ int attn_fwd_positions(const void* q, const void* k, const void* v, void* o, flo
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int nsm = sm_count();
     if (nsm <= 0) return GBATTN_ERR_CUDA;
+    int* err = device_error_word();
+    if (!err) return GBATTN_ERR_CUDA;
     if (row0 > 0 &&
         launch_fill_empty_rows(static_cast<__nv_bfloat16*>(o), lse, (long long)B * Hq, Sq, row0,
-                               d, nsm, st) != cudaSuccess)
+                               d, nsm, err, st) != cudaSuccess)
         return GBATTN_ERR_CUDA;
     if (row0 == Sq) return GBATTN_OK;
     return launch_prefill_bf16(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, Skv, d, scale, 1, diag, row0,
@@ -618,9 +620,11 @@ int attn_merge(const void* o_a, const float* lse_a, int dtype_a, const void* o_b
     if (rows > (1LL << 40)) return GBATTN_ERR_TOO_LARGE;
     const int nsm = sm_count();
     if (nsm <= 0) return GBATTN_ERR_CUDA;
+    int* err = device_error_word();
+    if (!err) return GBATTN_ERR_CUDA;
     return launch_attn_merge(o_a, lse_a, dtype_a == GBATTN_FP32, o_b, lse_b,
                              dtype_b == GBATTN_FP32, o_out, lse_out, dtype_out == GBATTN_FP32,
-                             rows, d, nsm, static_cast<cudaStream_t>(stream)) == cudaSuccess
+                             rows, d, nsm, err, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? GBATTN_OK
                : GBATTN_ERR_CUDA;
 }

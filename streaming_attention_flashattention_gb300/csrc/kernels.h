@@ -58,12 +58,13 @@ cudaError_t launch_attn_fwd_bf16_persistent(const PrefillParams& p, int d, int n
 // ---- log-sum-exp merge and empty-row fill (attn_merge.cu) -------------------------------
 // (O_out, L_out) = merge((O_a, L_a), (O_b, L_b)) row by row; each O is rows x d, fp32 or bf16
 // as flagged; lo may be null; oo may alias oa or ob, lo may alias la or lb.  d in {64, 128}.
+// err: the device error word (debug builds record failed store bounds checks there).
 cudaError_t launch_attn_merge(const void* oa, const float* la, bool a_f32, const void* ob,
                               const float* lb, bool b_f32, void* oo, float* lo, bool out_f32,
-                              long long rows, int d, int nsm, cudaStream_t st);
+                              long long rows, int d, int nsm, int* err, cudaStream_t st);
 // Rows [0, row0) of each of the bh (batch, head) blocks of Sq rows: O = 0, LSE = -inf.
 cudaError_t launch_fill_empty_rows(__nv_bfloat16* o, float* lse, long long bh, int Sq, int row0,
-                                   int d, int nsm, cudaStream_t st);
+                                   int d, int nsm, int* err, cudaStream_t st);
 
 // ---- bf16 split-KV decode path (decode_splitkv.cu) --------------------------------------
 struct DecodeParams {

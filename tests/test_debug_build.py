@@ -76,6 +76,19 @@ SCRIPT = textwrap.dedent(r"""
     decode(1, 64, 8, 4096, 0)                     # single launch
     decode(2, 64, 8, 6000, 3, Tq=4)               # tcgen05 multi-token kernel + combine
     decode(1, 32, 8, 4096, 0, Tq=3)               # 12 rows on the warp-level kernel
+    # attn_fwd_positions (rows 0..99 filled, the rest from row 100 on) and attn_merge
+    g = np.random.default_rng(9)
+    bf = lambda *s: torch.from_numpy(g.standard_normal(s).astype(np.float32)).to(torch.bfloat16)
+    q, k, v = bf(1, 4, 300, 128), bf(1, 2, 400, 128), bf(1, 2, 400, 128)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    pa = gb.attn_fwd_positions(qd, kd[:, :, :300].contiguous(), vd[:, :, :300].contiguous(), 0, 100)
+    pb = gb.attn_fwd_positions(qd, kd[:, :, 300:].contiguous(), vd[:, :, 300:].contiguous(), 0, 400)
+    o, lse = gb.attn_merge(pa[0], pa[1], pb[0], pb[1], out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    kk = k[:, :, :300].contiguous(); vv = v[:, :, :300].contiguous()
+    o_ref, l_ref = oracle.attention_at_positions(wl.to_oracle(q), wl.to_oracle(kk), wl.to_oracle(vv),
+                                                 1 / 128 ** 0.5, 0, 100)
+    compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "bf16", "positions+merge")
     st, word = gb.attn_last_device_error()
     assert st == 0 and word == 0, f"error word {{word}}"
     print("debug build ok")
