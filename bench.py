@@ -11,9 +11,10 @@ Printed JSON line (rank 0):
   configs    every one of the five workloads timed on its own (L2 flushed before each
              call, CUDA events): 1 tiny fp32, 2 small causal GQA prefill, 3 and 4 (the
              step's two calls), 5 ragged decode, each with its fraction of the roofline
-  e2e        the same metric through attn_fwd_host: pinned-host inputs copied in and
-             outputs copied out by the call (chunked, overlapped with the kernel)
-             inside the timed region, every step
+  e2e        the same metric through attn_fwd_host (and the decode half through
+             attn_decode_host): pinned-host inputs copied in and outputs copied out by
+             the call (chunked, overlapped with the kernels) inside the timed region,
+             every step
   cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload; the same
              leg compares sampled rows of every timed output with the oracle and fails the
              run on a mismatch
@@ -486,6 +487,9 @@ def run_gpu(args, rank, world, local_rank):
         hdlse = torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()
         hws = torch.empty(gb.attn_fwd_host_workspace_size(
             PREFILL.B, PREFILL.Hq, PREFILL.Hkv, PREFILL.Sq, PREFILL.Skv, PREFILL.d), dtype=torch.uint8, device=dev)
+        hdws = torch.empty(gb.attn_decode_host_workspace_size(
+            DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.Skv, DECODE.d, DECODE.num_splits),
+            dtype=torch.uint8, device=dev)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdq, hdk, hdv, hdl))
         d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdo, hdlse))
 
@@ -499,11 +503,8 @@ def run_gpu(args, rank, world, local_rank):
                              lse=hlse, workspace=hws)
             if ev is not None:
                 ev[1].record(stream)
-            dq.copy_(hdq, non_blocking=True); dk.copy_(hdk, non_blocking=True)
-            dv.copy_(hdv, non_blocking=True); dl.copy_(hdl, non_blocking=True)
-            gb.attn_decode_splitkv(dq, dk, dv, dl, num_splits=DECODE.num_splits,
-                                   scale=DECODE.scale, out=do, lse=dlse, workspace=ws)
-            hdo.copy_(do, non_blocking=True); hdlse.copy_(dlse, non_blocking=True)
+            gb.attn_decode_host(hdq, hdk, hdv, hdl, num_splits=DECODE.num_splits,
+                                scale=DECODE.scale, out=hdo, lse=hdlse, workspace=hdws)
             if ev is not None:
                 ev[2].record(stream)
 

@@ -31,8 +31,8 @@
  *  - Numerics: bf16 inputs, fp32 scores / running state / accumulators, P rounded to
  *    bf16 for the P.V product, O stored in the input dtype.
  *  - Each compute call is an NVTX range named after it (attn_fwd, attn_fwd_counted,
- *    attn_fwd_positions, attn_merge, attn_fwd_host, attn_prefill_kvcache, attn_decode),
- *    visible to a profiler and free without one.
+ *    attn_fwd_positions, attn_merge, attn_fwd_host, attn_prefill_kvcache, attn_decode,
+ *    attn_decode_host), visible to a profiler and free without one.
  */
 #ifndef GBATTN_H
 #define GBATTN_H
@@ -305,6 +305,36 @@ int attn_decode_multitoken(const void* q, const void* kcache, const void* vcache
                            const int* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
                            int Tq, int Lmax, int d, float scale, int num_splits,
                            void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * attn_decode_host_workspace_size -- device bytes attn_decode_host needs for these sizes on
+ * the current device (staging buffers and a decode workspace); 0 for invalid sizes.
+ */
+size_t attn_decode_host_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int num_splits);
+
+/*
+ * attn_decode_host -- attn_decode_splitkv on HOST buffers: the same operation and kernels,
+ * with the inputs copied to the device and the outputs back as part of the call.  Not in
+ * the pages (their accelerator has no host link); the decode counterpart of attn_fwd_host.
+ *
+ *   q, kcache, vcache, o, lse   HOST pointers, layouts as for attn_decode_splitkv (lse may
+ *                               be NULL); page-locked memory gives asynchronous copies
+ *   kv_lens                     HOST int32 [B], each within [0, Lmax] (checked on the host:
+ *                               GBATTN_ERR_INVALID_ARG otherwise, nothing launched)
+ *   num_splits                  as for attn_decode_splitkv, applied to each chunk
+ *   workspace, ws_bytes         DEVICE scratch of at least attn_decode_host_workspace_size(...)
+ *                               bytes, owned by the caller
+ *   stream                      ordered after the earlier work on `stream`; work queued on
+ *                               `stream` afterwards runs after the last copy has landed
+ *
+ * The sequences are cut into up to 4 chunks of consecutive sequences, staged through two
+ * device buffer sets on internal copy streams: chunk i+1 is copied in and chunk i-1 copied
+ * out while chunk i decodes.  Calls on one device are serialised on the host.  Status codes
+ * as attn_decode_splitkv.
+ */
+int attn_decode_host(const void* q, const void* kcache, const void* vcache, const int* kv_lens,
+                     void* o, float* lse, int B, int Hq, int Hkv, int Lmax, int d, float scale,
+                     int num_splits, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * attn_decode_splitkv_noalloc -- attn_decode_splitkv for callers that cannot allocate

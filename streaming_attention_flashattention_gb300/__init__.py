@@ -30,7 +30,13 @@ LIBRARY_PATH = os.path.join(_PKG, "libgbattn.so")
 GBATTN_BF16 = 0
 GBATTN_FP32 = 1
 GBATTN_OK = 0
+GBATTN_ERR_INVALID_ARG = -1
+GBATTN_ERR_UNSUPPORTED = -2
+GBATTN_ERR_MISALIGNED = -3
+GBATTN_ERR_CUDA = -4
 GBATTN_ERR_TIMEOUT = -5
+GBATTN_ERR_WORKSPACE = -6
+GBATTN_ERR_TOO_LARGE = -7
 
 _lock = threading.Lock()
 _lib = None
@@ -47,6 +53,8 @@ EXPORTS = {
     "attn_fwd_positions": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _LL, _LL, _P]),
     "attn_merge": (_I, [_P, _P, _I, _P, _P, _I, _P, _P, _I, _LL, _I, _P]),
     "attn_fwd_host_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "attn_decode_host_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "attn_decode_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "attn_prefill_kvcache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
@@ -317,6 +325,54 @@ def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: boo
                            B, Hq, Hkv, Sq, Skv, d, float(scale), 1 if causal else 0, dtype,
                            workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
     _check("attn_fwd_host", st)
+    return out, lse
+
+
+def attn_decode_host_workspace_size(B: int, Hq: int, Hkv: int, Lmax: int, d: int,
+                                    num_splits: int = 0) -> int:
+    return int(load_library().attn_decode_host_workspace_size(B, Hq, Hkv, Lmax, d, num_splits))
+
+
+def attn_decode_host(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor,
+                     kv_lens: torch.Tensor, num_splits: int = 0, scale: float | None = None,
+                     out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None, stream=None):
+    """attn_decode_splitkv on host (CPU) tensors: q [B,Hq,1,d], caches [B,Hkv,Lmax,d] bf16,
+    kv_lens int32 [B], all on the host; inputs copied in and outputs copied back by the
+    call.  Returns (out [B,Hq,1,d], lse [B,Hq]) on the host, complete once `stream` (default:
+    the current stream) has been synchronised."""
+    lib = load_library()
+    for n, t in (("q", q), ("kcache", kcache), ("vcache", vcache)):
+        _host_tensor(n, t, (torch.bfloat16,))
+    _host_tensor("kv_lens", kv_lens, (torch.int32,))
+    B, Hq, one, d = q.shape
+    _, Hkv, Lmax, _ = kcache.shape
+    if one != 1 or vcache.shape != kcache.shape or tuple(kv_lens.shape) != (B,):
+        raise ValueError("expected q [B,Hq,1,d], caches [B,Hkv,Lmax,d], kv_lens [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    else:
+        _host_tensor("out", out, (torch.bfloat16,))
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32).pin_memory()
+    else:
+        _host_tensor("lse", lse, (torch.float32,))
+    need = attn_decode_host_workspace_size(B, Hq, Hkv, Lmax, d, num_splits)
+    if need == 0:
+        raise GbAttnError("attn_decode_host", GBATTN_ERR_INVALID_ARG)
+    if workspace is None:
+        key = ("decode_host", torch.cuda.current_device(), need)
+        workspace = _host_ws.get(key)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+            _host_ws[key] = workspace
+    st = lib.attn_decode_host(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
+                              kv_lens.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Hq, Hkv,
+                              Lmax, d, float(scale), int(num_splits), workspace.data_ptr(),
+                              workspace.numel(), _stream_ptr(stream))
+    _check("attn_decode_host", st)
     return out, lse
 
 

@@ -760,6 +760,110 @@ int attn_decode_splitkv(const void* q, const void* kcache, const void* vcache,
                                   scale, num_splits, workspace, ws_bytes, stream);
 }
 
+// ---- host-buffer decode: the sequences in up to 4 chunks, copies overlapped -------------
+// Each chunk is a run of consecutive sequences -- contiguous slabs of q / o ([Hq, d]), the
+// caches ([Hkv, Lmax, d]), kv_lens and LSE -- staged through two device buffer sets as in
+// attn_fwd_host, and decoded by attn_decode_splitkv on the staged copies with a decode
+// workspace shared by the chunks (their decodes run in order on the caller's stream).
+struct DecodeHostPlan {
+    int cb, n_chunks, n_bufs;
+    size_t q_off, k_off, v_off, n_off, o_off, l_off, set_bytes, dec_off, dec_bytes;
+};
+
+bool decode_host_plan(int B, int Hq, int Hkv, int Lmax, int d, int num_splits,
+                      DecodeHostPlan& h) {
+    h.cb = (B + 3) / 4;
+    h.n_chunks = (B + h.cb - 1) / h.cb;
+    h.n_bufs = h.n_chunks > 1 ? 2 : 1;
+    const size_t qb = (size_t)h.cb * Hq * d * 2, kb = (size_t)h.cb * Hkv * Lmax * d * 2;
+    h.q_off = 0;
+    h.k_off = align256(qb);
+    h.v_off = h.k_off + align256(kb);
+    h.n_off = h.v_off + align256(kb);
+    h.o_off = h.n_off + align256((size_t)h.cb * 4);
+    h.l_off = h.o_off + align256(qb);
+    h.set_bytes = h.l_off + align256((size_t)h.cb * Hq * 4);
+    h.dec_off = h.set_bytes * h.n_bufs;
+    const int last = B - (h.n_chunks - 1) * h.cb;
+    const size_t w0 = attn_decode_workspace_size(h.cb, Hq, Hkv, Lmax, d, num_splits);
+    const size_t w1 = attn_decode_workspace_size(last, Hq, Hkv, Lmax, d, num_splits);
+    if (w0 == 0 || w1 == 0) return false;
+    h.dec_bytes = std::max(w0, w1);
+    return true;
+}
+
+size_t attn_decode_host_workspace_size(int B, int Hq, int Hkv, int Lmax, int d, int num_splits) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lmax <= 0 || Hq % Hkv != 0) return 0;
+    if ((d != 64 && d != 128) || num_splits < 0 || num_splits > kMaxSplits) return 0;
+    DecodeHostPlan h{};
+    if (!decode_host_plan(B, Hq, Hkv, Lmax, d, num_splits, h)) return 0;
+    return h.dec_off + h.dec_bytes;
+}
+
+int attn_decode_host(const void* q, const void* kcache, const void* vcache, const int* kv_lens,
+                     void* o, float* lse, int B, int Hq, int Hkv, int Lmax, int d, float scale,
+                     int num_splits, void* workspace, size_t ws_bytes, void* stream) {
+    CallRange range("attn_decode_host");
+    if (!q || !kcache || !vcache || !kv_lens || !o) return GBATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lmax <= 0 || d <= 0) return GBATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return GBATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || scale != scale) return GBATTN_ERR_INVALID_ARG;
+    if (num_splits < 0 || num_splits > kMaxSplits) return GBATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return GBATTN_ERR_UNSUPPORTED;
+    for (int b = 0; b < B; ++b)                  // the lengths are on the host: check them here
+        if (kv_lens[b] < 0 || kv_lens[b] > Lmax) return GBATTN_ERR_INVALID_ARG;
+    if ((long long)B * Hq > kIntMax / 8 || (long long)B * Hkv * Lmax > kIntMax)
+        return GBATTN_ERR_TOO_LARGE;
+    const size_t need = attn_decode_host_workspace_size(B, Hq, Hkv, Lmax, d, num_splits);
+    if (need == 0) return GBATTN_ERR_CUDA;
+    if (!workspace || ws_bytes < need) return GBATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return GBATTN_ERR_MISALIGNED;
+    HostPipe* hp = host_pipe();
+    if (!hp) return GBATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(hp->mu);
+
+    DecodeHostPlan h{};
+    if (!decode_host_plan(B, Hq, Hkv, Lmax, d, num_splits, h)) return GBATTN_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const char* qh = static_cast<const char*>(q);
+    const char* kh = static_cast<const char*>(kcache);
+    const char* vh = static_cast<const char*>(vcache);
+    const char* nh = reinterpret_cast<const char*>(kv_lens);
+    char* oh = static_cast<char*>(o);
+    char* lh = reinterpret_cast<char*>(lse);
+    char* ws = static_cast<char*>(workspace);
+    const size_t qs = (size_t)Hq * d * 2, ks = (size_t)Hkv * Lmax * d * 2, ls = (size_t)Hq * 4;
+    auto chk = [](cudaError_t e) { return e == cudaSuccess; };
+    bool ok = chk(cudaEventRecord(hp->entry, st));   // the caller's earlier work comes first
+    for (int i = 0; ok && i < h.n_chunks; ++i) {
+        const int bset = i % h.n_bufs;
+        const int b0 = i * h.cb, bn = std::min(h.cb, B - b0);
+        char* base = ws + (size_t)bset * h.set_bytes;
+        ok = chk(cudaStreamWaitEvent(hp->in, i >= h.n_bufs ? hp->ev_out[bset] : hp->entry, 0)) &&
+             chk(cudaMemcpyAsync(base + h.q_off, qh + b0 * qs, bn * qs, cudaMemcpyHostToDevice, hp->in)) &&
+             chk(cudaMemcpyAsync(base + h.k_off, kh + b0 * ks, bn * ks, cudaMemcpyHostToDevice, hp->in)) &&
+             chk(cudaMemcpyAsync(base + h.v_off, vh + b0 * ks, bn * ks, cudaMemcpyHostToDevice, hp->in)) &&
+             chk(cudaMemcpyAsync(base + h.n_off, nh + b0 * 4, bn * 4, cudaMemcpyHostToDevice, hp->in)) &&
+             chk(cudaEventRecord(hp->ev_in[bset], hp->in)) &&
+             chk(cudaStreamWaitEvent(st, hp->ev_in[bset], 0));
+        if (!ok) break;
+        const int rc = attn_decode_splitkv(
+            base + h.q_off, base + h.k_off, base + h.v_off,
+            reinterpret_cast<const int*>(base + h.n_off), base + h.o_off,
+            lh ? reinterpret_cast<float*>(base + h.l_off) : nullptr, bn, Hq, Hkv, Lmax, d, scale,
+            num_splits, ws + h.dec_off, h.dec_bytes, stream);
+        if (rc != GBATTN_OK) return rc;
+        ok = chk(cudaEventRecord(hp->ev_comp[bset], st)) &&
+             chk(cudaStreamWaitEvent(hp->out, hp->ev_comp[bset], 0)) &&
+             chk(cudaMemcpyAsync(oh + b0 * qs, base + h.o_off, bn * qs, cudaMemcpyDeviceToHost, hp->out)) &&
+             (!lh || chk(cudaMemcpyAsync(lh + b0 * ls, base + h.l_off, bn * ls, cudaMemcpyDeviceToHost, hp->out))) &&
+             chk(cudaEventRecord(hp->ev_out[bset], hp->out));
+    }
+    // the caller's stream completes after the last copy out
+    ok = ok && chk(cudaEventRecord(hp->done, hp->out)) && chk(cudaStreamWaitEvent(st, hp->done, 0));
+    return ok ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
 int attn_decode_plan(int B, int Hq, int Hkv, int Tq, int Lmax, int d, int num_splits,
                      int num_sms, int* plan) {
     if (!plan) return GBATTN_ERR_INVALID_ARG;

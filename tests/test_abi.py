@@ -215,3 +215,30 @@ def test_merge_argument_validation(lib):
     assert mg(rows=1 << 41) == -7
     assert mg(rows=0) == 0            # nothing to do, nothing launched
     assert mg(oa=None, ob=None, la=None, lb=None, oo=None, rows=0) == 0
+
+
+def test_binding_status_constants_match_the_header():
+    text = open(HEADER).read()
+    enum = dict((n, int(v)) for n, v in re.findall(r"(GBATTN_(?:OK|ERR_\w+))\s*=\s*(-?\d+)", text))
+    assert len(enum) == 8
+    for name, value in enum.items():
+        assert getattr(gb, name) == value, name
+
+
+def test_decode_host_argument_validation(lib):
+    lens_ok = (ctypes.c_int * 2)(5, 7)
+    lens_bad = (ctypes.c_int * 2)(5, 9000)
+
+    def dh(q=A, kc=A, vc=A, lens=None, o=B_, B=2, Hq=8, Hkv=1, Lmax=4096, d=128, scale=0.1,
+           ns=0, ws=A, wsb=1 << 30):
+        lens = lens_ok if lens is None else lens
+        return lib.attn_decode_host(q, kc, vc, lens, o, None, B, Hq, Hkv, Lmax, d, scale, ns, ws,
+                                    wsb, None)
+    assert dh(q=None) == -1
+    assert dh(B=0) == -1
+    assert dh(Hq=6, Hkv=4) == -1
+    assert dh(scale=0.0) == -1
+    assert dh(ns=300) == -1
+    assert dh(d=80) == -2
+    assert dh(lens=lens_bad) == -1            # a length beyond Lmax, seen on the host
+    assert gb.load_library().attn_decode_host_workspace_size(0, 8, 1, 4096, 128, 0) == 0

@@ -66,3 +66,33 @@ def test_host_pipeline_rejects_small_workspace():
     ws = torch.empty(64, dtype=torch.uint8, device="cuda")
     with pytest.raises(gb.GbAttnError):
         gb.attn_fwd_host(q, k, v, causal=True, workspace=ws)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L,ns", [(4, 64, 8, 32768, 16),   # workload 4's shape: 4 chunks
+                                           (7, 32, 8, 5000, 0),     # chunks of 2, the last of 1
+                                           (1, 8, 1, 300, 0)])      # one chunk, one buffer set
+def test_decode_host_matches_oracle_and_device_call(B, Hq, Hkv, L, ns):
+    w = wl.Workload(f"dhost-b{B}-h{Hq}/{Hkv}-l{L}", "decode", B=B, Hq=Hq, Hkv=Hkv, d=128,
+                    dtype="bf16", Skv=L, num_splits=ns, len_lo=L // 4, len_hi=L, Sq=1, seed=61)
+    q, kc, vc, kl = wl.decode_inputs(w)
+    o, lse = gb.attn_decode_host(q.pin_memory(), kc.pin_memory(), vc.pin_memory(),
+                                 kl.pin_memory(), num_splits=ns, scale=w.scale)
+    torch.cuda.synchronize()
+    assert not o.is_cuda and not lse.is_cuda
+    o_ref, l_ref = oracle.attention(wl.to_oracle(q), wl.to_oracle(kc), wl.to_oracle(vc), w.scale,
+                                    False, kv_len=kl.numpy())
+    compare(o.float().numpy(), lse.numpy(), o_ref, l_ref[..., 0] if l_ref.ndim == 3 else l_ref,
+            "bf16", w.name)
+    # one chunk holds all sequences: the same kernels and split decisions as the device call
+    if B == 1:
+        od, ld = gb.attn_decode_splitkv(q.cuda(), kc.cuda(), vc.cuda(), kl.cuda(),
+                                        num_splits=ns, scale=w.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(od.cpu(), o) and torch.equal(ld.cpu(), lse)
+
+
+def test_decode_host_rejects_a_length_beyond_the_cache():
+    q = torch.zeros((2, 8, 1, 128), dtype=torch.bfloat16)
+    kc = torch.zeros((2, 1, 256, 128), dtype=torch.bfloat16)
+    with pytest.raises(gb.GbAttnError):
+        gb.attn_decode_host(q, kc, kc, torch.tensor([10, 300], dtype=torch.int32))
