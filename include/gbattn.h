@@ -259,9 +259,10 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Tq, int Lmax, int
  * of the splits are merged ("ADR-0060" section 4; a sequence with one split is written
  * directly).  When the (split, KV head) work items of the warp-level kernel would leave the
  * GPU's last wave mostly idle, each split is processed as up to 4 contiguous pieces (at
- * least 512 keys each),
- * each with a partial of its own in the same merge: the result is the same up to fp32
- * rounding, and attn_decode_plan reports the piece count.  When every work item fits in one wave of the GPU, or the call has at most
+ * least 512 keys per piece on average; piece k starts at the fraction 1 - 4^-k of the split,
+ * and every split's first piece is handed out before the smaller ones), each with a partial
+ * of its own in the same merge: the result is the same up to fp32 rounding, and
+ * attn_decode_plan reports the piece count.  When every work item fits in one wave of the GPU, or the call has at most
  * 16 (sequence, KV head) groups with splits of at least 1024 keys (Lmax / splits), the
  * merge is done by the CTA that finishes a group's last split (one launch, "ADR-0060"
  * section 4.3); otherwise a combine kernel, launched dependent on the split kernel, merges.  With G >= 16 query

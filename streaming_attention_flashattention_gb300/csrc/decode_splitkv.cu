@@ -355,15 +355,23 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
             // more (a static round-robin measured slower even for equal-size splits).
             for (int item = atomicAdd(p.counter, 1); ok && item < p.n_items;
                  item = atomicAdd(p.counter, 1)) {
-                // order: row chunk innermost, then piece, then split, then KV head, then
-                // sequence.  The row chunks of one split (several when G * Tq > 8) read the
-                // same K/V tiles and run side by side, so all but the first pass hit L2.
+                // order: row chunk innermost, then split, then KV head, then sequence,
+                // then piece (guided pieces: every split's large first piece before the
+                // small ones).  The row chunks of one split (several when G * Tq > 8) read
+                // the same K/V tiles and run side by side, so all but the first pass hit L2.
                 int rem = item;
                 const int hc = rem % p.n_hg; rem /= p.n_hg;         // chunk group
+#if GBATTN_GUIDED_PIECES
+                const int s = rem % p.n_slots; rem /= p.n_slots;
+                const int kvh = rem % p.Hkv; rem /= p.Hkv;
+                const int b = rem % p.B;
+                const int pc = rem / p.B;                           // piece of the split
+#else
                 const int pc = rem % p.pieces; rem /= p.pieces;     // piece of the split
                 const int s = rem % p.n_slots; rem /= p.n_slots;
                 const int kvh = rem % p.Hkv; rem /= p.Hkv;
                 const int b = rem;
+#endif
                 int len = __ldg(&p.kv_lens[b]);
                 len = max(0, min(len, p.Lmax));
                 const int nb = splits_for(len, p.fixed_splits, p.auto_floor);
@@ -388,7 +396,11 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                 }
                 int t0, t1;
                 split_range(len, nb, s, t0, t1);
+#if GBATTN_GUIDED_PIECES
+                piece_range_guided(t0, t1, p.pieces, pc, t0, t1);
+#else
                 piece_range(t0, t1, p.pieces, pc, t0, t1);
+#endif
                 const int part = s * p.pieces + pc;
                 if (t0 >= t1) {
                     // an empty piece of a non-empty split: a partial that weighs nothing

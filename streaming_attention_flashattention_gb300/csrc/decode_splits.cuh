@@ -53,4 +53,26 @@ __host__ __device__ __forceinline__ int splits_for(int len, int fixed_splits, in
 }
 
 
+// Guided pieces (the layout the split kernel uses): piece pc of P starts at the fraction
+// 1 - 4^-pc of the split (3/4 + 1/4 for two pieces), cut points rounded up to kSplitAlign,
+// and the work queue hands out piece 0 of every split before any piece 1.  Large items go
+// first and small ones last, so the persistent CTAs run out of work within a small item of
+// one another instead of a whole one.  Still contiguous blocks, folded by the same merge.
+#ifndef GBATTN_GUIDED_PIECES
+#define GBATTN_GUIDED_PIECES 1
+#endif
+__device__ __forceinline__ void piece_range_guided(int t0, int t1, int P, int pc, int& a,
+                                                   int& b) {
+    const int n = t1 - t0;
+    auto cut = [&](int k) -> int {                 // keys of the split before piece k
+        if (k <= 0) return 0;
+        if (k >= P) return n;
+        long long c = (long long)n - ((long long)n >> (2 * k));
+        c = ((c + kSplitAlign - 1) / kSplitAlign) * kSplitAlign;
+        return (int)min((long long)n, c);
+    };
+    a = t0 + cut(pc);
+    b = t0 + cut(pc + 1);
+}
+
 }  // namespace gbattn
