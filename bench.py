@@ -464,6 +464,36 @@ def run_gpu(args, rank, world, local_rank):
         mtok = {"workload": wm.name, "ms": mm, "value": mbytes / (mm * 1e-3) / 1e9, "unit": "GB/s"}
         del mq, mkc, mvc, mkl, mo, mlse, mws
 
+    # sequence-parallel pieces: one ring step of the Llama3-70B prefill over 8 ranks (a rank's
+    # 8 query heads, all 8192 positions, against KV slice 3 of 8: keys 3072..4095 of its KV
+    # head) and the merge of that step into an fp32 accumulator (in place)
+    spar = None
+    if not args.no_chunk:
+        Sr, Lr, kp = PREFILL.Sq, PREFILL.Skv // 8, 3 * (PREFILL.Skv // 8)
+        g = torch.Generator().manual_seed(97)
+        rq = torch.randn((1, 8, Sr, PREFILL.d), generator=g).to(torch.bfloat16).to(dev)
+        rk = torch.randn((1, 1, Lr, PREFILL.d), generator=g).to(torch.bfloat16).to(dev)
+        rv = torch.randn((1, 1, Lr, PREFILL.d), generator=g).to(torch.bfloat16).to(dev)
+        ro = torch.empty_like(rq)
+        rl = torch.empty((1, 8, Sr), dtype=torch.float32, device=dev)
+        acc_o = torch.zeros((1, 8, Sr, PREFILL.d), dtype=torch.float32, device=dev)
+        acc_l = torch.full((1, 8, Sr), float("-inf"), device=dev)
+        run_r = lambda: gb.attn_fwd_positions(rq, rk, rv, 0, kp, scale=PREFILL.scale, out=ro, lse=rl)
+        run_g = lambda: gb.attn_merge(acc_o, acc_l, ro, rl, out=acc_o, lse_out=acc_l)
+        for _ in range(3):
+            run_r(); run_g()
+        rm = max_over_ranks([time_calls(run_r, 10)], dev)[0]
+        gm = max_over_ranks([time_calls(run_g, 10)], dev)[0]
+        vis = sum(min(Lr, max(0, i - kp + 1)) for i in range(Sr))       # visible keys, all rows
+        rflops = 4.0 * PREFILL.d * vis * 8
+        rows = 8 * Sr
+        gbytes = rows * (PREFILL.d * (4 + 2 + 4) + 12)                   # acc in, part in, acc out
+        spar = {"ring_step": {"shape": f"q 1x8x{Sr}x{PREFILL.d}, kv slice 1x1x{Lr} at {kp}",
+                              "ms": rm, "value": rflops / (rm * 1e-3) / 1e12, "unit": "TFLOP/s"},
+                "merge": {"rows": rows, "ms": gm, "value": gbytes / (gm * 1e-3) / 1e9,
+                          "unit": "GB/s", "bound": "hbm"}}
+        del rq, rk, rv, ro, rl, acc_o, acc_l
+
     st, word = gb.attn_last_device_error()
     if st != 0:
         raise RuntimeError(f"device error word {word} during the timed steps")
@@ -530,6 +560,10 @@ def run_gpu(args, rank, world, local_rank):
     dec_gbs = dbytes / (dec_avg * 1e-3) / 1e9 * world
     peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    if spar is not None:
+        spar["merge"]["peak"] = peak_bw
+        spar["merge"]["frac"] = spar["merge"]["value"] / peak_bw
+        spar["ring_step"]["frac"] = spar["ring_step"]["value"] / peak_tf
     per_gpu_tf = flops / (pre_avg * 1e-3) / 1e12
     per_gpu_bw = dbytes / (dec_avg * 1e-3) / 1e9
     if chunk is not None:
@@ -597,6 +631,7 @@ def run_gpu(args, rank, world, local_rank):
         "gpu_launches": launches * args.steps,
         "chunked_prefill": chunk,
         "multitoken_decode": mtok,
+        "sequence_parallel": spar,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:

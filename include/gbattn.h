@@ -190,7 +190,7 @@ int attn_fwd_positions(const void* q, const void* k, const void* v, void* o, flo
  * can be folded in any order, by a chain or by a tree).  With L the rows' log-sum-exp:
  *     M = max(L_a, L_b),  w_x = e^(L_x - M),
  *     O = (w_a O_a + w_b O_b) / (w_a + w_b),  L = M + ln(w_a + w_b);
- * a partial with L = -inf (no key) contributes nothing and its O is not read; if both are
+ * a partial with L = -inf (no key) contributes nothing, whatever its O holds; if both are
  * -inf the row is O = 0, L = -inf.
  *
  *   o_a, lse_a, dtype_a         first partial: rows x d elements (GBATTN_BF16 or GBATTN_FP32)

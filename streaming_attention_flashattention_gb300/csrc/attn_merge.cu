@@ -11,9 +11,8 @@
 // A partial over no key has L = -inf (w = 0) and adds nothing; if both have none the row is
 // O = 0, L = -inf.
 //
-// Layout: rows of d contiguous elements; one warp handles 128 / d rows (d / 4 lanes per row,
-// 4 elements per lane), so a row's lanes read its two LSE values and one of them writes the
-// merged one after the warp has exchanged them -- out may alias either input.
+// Layout: rows of d contiguous elements; one warp handles 128 / d rows at a time (d / 4 lanes
+// per row, 4 elements per lane).  Out may alias either input (see merge_kernel).
 #include <algorithm>
 
 #include "common.cuh"
@@ -45,45 +44,65 @@ template <> struct Vec4<__nv_bfloat16> {
     }
 };
 
+// Each warp takes kUnroll units (rows-per-warp groups) per pass and issues all their loads --
+// both LSE values and both O vectors of every lane -- before any arithmetic, so that one pass
+// waits for one memory latency; a partial whose weight is 0 is then ignored by selection
+// (never multiplied, so whatever its O holds cannot leak in).  Every lane reads its row's LSE
+// values itself; the warp synchronises before the stores, so the merged LSE may overwrite an
+// input that other lanes of the row have read.
+constexpr int kUnroll = 2;
+
 template <typename TA, typename TB, typename TO>
 __global__ void __launch_bounds__(256)
 merge_kernel(const TA* oa, const float* la, const TB* ob, const float* lb, TO* oo, float* lo,
              long long rows, int d, int* err) {
     const int lane = threadIdx.x & 31;
     const int lpr = d >> 2;                          // lanes per row
-    const int rpw = 32 / lpr;                        // rows per warp
+    const int rpw = 32 / lpr;                        // rows per warp unit
     const int sub = lane / lpr, col = (lane % lpr) * 4;
     const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
     const long long units = (rows + rpw - 1) / rpw;
-    for (long long u = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units;
-         u += warps) {
-        const long long row = u * rpw + sub;
-        const bool live = row < rows;
-        float lsa = -INFINITY, lsb = -INFINITY;
-        if (live && lane % lpr == 0) {
-            lsa = la[row];
-            lsb = lb[row];
-        }
-        const int leader = sub * lpr;
-        lsa = __shfl_sync(0xffffffffu, lsa, leader);
-        lsb = __shfl_sync(0xffffffffu, lsb, leader);
-        if (!live) continue;
-        const float M = fmaxf(lsa, lsb);
-        float w_a = 0.f, w_b = 0.f;
-        if (M != -INFINITY) {
-            w_a = expf(lsa - M);                     // e^-inf = 0 for an empty partial
-            w_b = expf(lsb - M);
-        }
-        const float s = w_a + w_b;
-        const float inv = s > 0.f ? 1.f / s : 0.f;
-        float va[4] = {0.f, 0.f, 0.f, 0.f}, vb[4] = {0.f, 0.f, 0.f, 0.f}, r[4];
-        if (w_a > 0.f) Vec4<TA>::load(oa + row * d + col, va);
-        if (w_b > 0.f) Vec4<TB>::load(ob + row * d + col, vb);
+    const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    for (long long u0 = wid; u0 < units; u0 += warps * kUnroll) {
+        long long row[kUnroll];
+        float lsa[kUnroll], lsb[kUnroll], va[kUnroll][4], vb[kUnroll][4];
         #pragma unroll
-        for (int e = 0; e < 4; ++e) r[e] = (w_a * va[e] + w_b * vb[e]) * inv;
-        if (GBATTN_IN_BOUNDS(row * d + col + 3, rows * d, err)) Vec4<TO>::store(oo + row * d + col, r);
-        if (lo != nullptr && lane % lpr == 0 && GBATTN_IN_BOUNDS(row, rows, err))
-            lo[row] = s > 0.f ? M + logf(s) : -INFINITY;
+        for (int x = 0; x < kUnroll; ++x) {
+            row[x] = (u0 + x * warps) * rpw + sub;
+            lsa[x] = lsb[x] = -INFINITY;
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) va[x][e] = vb[x][e] = 0.f;
+            if (u0 + x * warps < units && row[x] < rows) {
+                lsa[x] = la[row[x]];
+                lsb[x] = lb[row[x]];
+                Vec4<TA>::load(oa + row[x] * d + col, va[x]);
+                Vec4<TB>::load(ob + row[x] * d + col, vb[x]);
+            }
+        }
+        __syncwarp();
+        #pragma unroll
+        for (int x = 0; x < kUnroll; ++x) {
+            if (!(u0 + x * warps < units && row[x] < rows)) continue;
+            const float M = fmaxf(lsa[x], lsb[x]);
+            float w_a = 0.f, w_b = 0.f;
+            if (M != -INFINITY) {
+                w_a = expf(lsa[x] - M);              // e^-inf = 0 for an empty partial
+                w_b = expf(lsb[x] - M);
+            }
+            const float s = w_a + w_b;
+            const float inv = s > 0.f ? 1.f / s : 0.f;
+            float r[4];
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float ta = w_a > 0.f ? w_a * va[x][e] : 0.f;
+                const float tb = w_b > 0.f ? w_b * vb[x][e] : 0.f;
+                r[e] = (ta + tb) * inv;
+            }
+            if (GBATTN_IN_BOUNDS(row[x] * d + col + 3, rows * d, err))
+                Vec4<TO>::store(oo + row[x] * d + col, r);
+            if (lo != nullptr && lane % lpr == 0 && GBATTN_IN_BOUNDS(row[x], rows, err))
+                lo[row[x]] = s > 0.f ? M + logf(s) : -INFINITY;
+        }
     }
 }
 
@@ -93,7 +112,8 @@ cudaError_t launch_merge_t(const void* oa, const float* la, const void* ob, cons
                            cudaStream_t st) {
     constexpr int kThreads = 256;
     const long long units = (rows + (128 / d) - 1) / (128 / d);
-    const long long blocks = std::min<long long>((units + 7) / 8, (long long)nsm * 8);
+    const long long blocks = std::min<long long>((units + 8 * kUnroll - 1) / (8 * kUnroll),
+                                                 (long long)nsm * 8);
     merge_kernel<TA, TB, TO><<<(unsigned)std::max<long long>(blocks, 1), kThreads, 0, st>>>(
         static_cast<const TA*>(oa), la, static_cast<const TB*>(ob), lb, static_cast<TO*>(oo), lo,
         rows, d, err);

@@ -140,6 +140,11 @@ def test_merge_in_place_accumulator_and_empty_partials():
     compare(acc_o.cpu().numpy(), acc_l.cpu().numpy(), o_ref, l_ref, "bf16", "merge in place")
     assert torch.isneginf(lb).all().item()                 # the second half saw no key
     assert torch.equal(acc_o, oa.float()) and torch.equal(acc_l, la)
+    # an empty partial is dropped whatever its O holds (NaN here)
+    nan_o = torch.full_like(acc_o, float("nan"))
+    o2, l2 = gb.attn_merge(acc_o, acc_l, nan_o, lb)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, acc_o) and torch.equal(l2, acc_l)
     # both partials empty: O = 0, LSE = -inf
     e_o = torch.full_like(acc_o, float("nan"))
     e_l = torch.full_like(acc_l, float("-inf"))
