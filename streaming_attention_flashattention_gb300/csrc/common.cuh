@@ -118,6 +118,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int er
     }
 }
 
+// Wait for the phase of a copy this thread issued, at exit: unlike mbar_wait it does not give
+// up when another part of the grid has recorded an error -- a CTA must not exit with its own
+// TMA copies still writing into its shared memory -- only after kWaitLimitCycles (recording
+// kErrWaitDrain).
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, int* err_word) {
+    if (mbar_try_wait(bar, parity)) return;
+    const long long t0 = clock64();
+    uint32_t spins = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if ((++spins & 1023u) == 0 && clock64() - t0 > kWaitLimitCycles) {
+            record_error(err_word, kErrWaitDrain);
+            return;
+        }
+    }
+}
+
 // Add `v` to a device-scope counter with release semantics: every write that this thread has
 // observed -- its own, and those of threads that synchronised with it before (a CTA barrier or
 // an mbarrier phase) -- is visible to a thread that reads the new count with acquire

@@ -473,7 +473,7 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
             asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             // drain: never leave the CTA with a TMA copy still writing its shared memory
             for (int i = 0; i < kStages; ++i)
-                if (filled & (1u << i)) mbar_wait(&full[i], (fill_parity >> i) & 1u, kErrWaitDrain, p.err);
+                if (filled & (1u << i)) mbar_wait_drain(&full[i], (fill_parity >> i) & 1u, p.err);
         }
     } else if (warp == kConsumerWarps + 1) {
         // ============================= publisher warp ==============================

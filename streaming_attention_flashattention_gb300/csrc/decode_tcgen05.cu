@@ -245,9 +245,9 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
             // this CTA takes no more work: the combine grid may start being scheduled
             asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             // drain: the last fills of Q and of each K slot must land before the CTA exits
-            if (k > 0) mbar_wait(q_full, (k - 1) & 1, kErrWaitDrain, p.err);
+            if (k > 0) mbar_wait_drain(q_full, (k - 1) & 1, p.err);
             for (uint32_t f = nf >= (uint32_t)KS ? nf - KS : 0; f < nf; ++f)
-                mbar_wait(&k_full[f % KS], (f / KS) & 1, kErrWaitDrain, p.err);
+                mbar_wait_drain(&k_full[f % KS], (f / KS) & 1, p.err);
         }
     } else if (warp == 2) {
         // ================================== V producer ==================================
@@ -313,7 +313,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
         // drain: the last fill of each V slot must land before the CTA exits
         if (lane == 0)
             for (uint32_t f = nf >= (uint32_t)VS ? nf - VS : 0; f < nf; ++f)
-                mbar_wait(&v_full[f % VS], (f / VS) & 1, kErrWaitDrain, p.err);
+                mbar_wait_drain(&v_full[f % VS], (f / VS) & 1, p.err);
     } else if (warp == 1) {
         // ================================= MMA issuer =================================
         // Per step j: PV0(j), S0(j+1), PV1(j), S1(j+1) -- the ping-pong order of the

@@ -232,11 +232,11 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
                 }
             }
             // drain: the last fills of each slot must land before the CTA can exit
-            mbar_wait(q_full, 0, kErrWaitDrain, p.err);
+            mbar_wait_drain(q_full, 0, p.err);
             for (uint32_t f = nf >= (uint32_t)KS ? nf - KS : 0; f < nf; ++f)
-                mbar_wait(&k_full[f % KS], (f / KS) & 1, kErrWaitDrain, p.err);
+                mbar_wait_drain(&k_full[f % KS], (f / KS) & 1, p.err);
             for (uint32_t f = nfv >= 2 ? nfv - 2 : 0; f < nfv; ++f)
-                mbar_wait(&v_full[f & 1], (f >> 1) & 1, kErrWaitDrain, p.err);
+                mbar_wait_drain(&v_full[f & 1], (f >> 1) & 1, p.err);
         }
     } else if (warp == 1) {
         // ================================= MMA issuer =================================
