@@ -98,18 +98,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Returns false (after
-// recording `err`) if the wait runs past kWaitLimitCycles or another part of the grid
-// already recorded an error.
+// recording `err`) if the wait runs past kWaitLimitCycles or, unless abort_on_error is
+// false, another part of the grid already recorded an error.  The exit drains of copies a
+// CTA issued pass false: a CTA must not leave with its own TMA copies still writing into its
+// shared memory, whatever happened elsewhere.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int err,
                                           int* err_word,
-                                          long long limit_cycles = kWaitLimitCycles) {
+                                          long long limit_cycles = kWaitLimitCycles,
+                                          bool abort_on_error = true) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     uint32_t spins = 0;
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((++spins & 1023u) == 0) {
-            if (device_error_set(err_word)) return false;
+            if (abort_on_error && device_error_set(err_word)) return false;
             if (clock64() - t0 > limit_cycles) {
                 record_error(err_word, err);
                 return false;
@@ -118,20 +121,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int er
     }
 }
 
-// Wait for the phase of a copy this thread issued, at exit: unlike mbar_wait it does not give
-// up when another part of the grid has recorded an error -- a CTA must not exit with its own
-// TMA copies still writing into its shared memory -- only after kWaitLimitCycles (recording
-// kErrWaitDrain).
-__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, int* err_word) {
-    if (mbar_try_wait(bar, parity)) return;
-    const long long t0 = clock64();
-    uint32_t spins = 0;
-    while (!mbar_try_wait(bar, parity)) {
-        if ((++spins & 1023u) == 0 && clock64() - t0 > kWaitLimitCycles) {
-            record_error(err_word, kErrWaitDrain);
-            return;
-        }
-    }
+// The exit drain of a copy this thread issued: mbar_wait that does not give up when another
+// part of the grid has recorded an error.  Kept out of line: inlined at the producers' exits
+// it measurably slowed the prefill kernel's steady state (code layout).
+static __device__ __noinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity,
+                                                    int* err_word) {
+    mbar_wait(bar, parity, kErrWaitDrain, err_word, kWaitLimitCycles, false);
 }
 
 // Add `v` to a device-scope counter with release semantics: every write that this thread has

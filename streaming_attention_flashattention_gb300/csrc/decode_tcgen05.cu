@@ -578,6 +578,10 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
         }
     }
 
+    // TMEM is released only when no tensor-core work of the CTA can still be running: on
+    // success the softmax warps have waited for the last P.V of each slot (the issuer's
+    // products complete in issue order); a role that gave up did so after a wait of
+    // kWaitLimitCycles, long after the products issued before it had completed.
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

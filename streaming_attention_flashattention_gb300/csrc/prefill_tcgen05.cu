@@ -547,6 +547,10 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
         }
     }
 
+    // TMEM is released only when no tensor-core work of the CTA can still be running: on
+    // success the softmax warps have waited for the last P.V of each slot (the issuer's
+    // products complete in issue order); a role that gave up did so after a wait of
+    // kWaitLimitCycles, long after the products issued before it had completed.
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
