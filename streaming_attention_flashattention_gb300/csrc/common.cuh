@@ -129,6 +129,14 @@ static __device__ __noinline__ void mbar_wait_drain(uint64_t* bar, uint32_t pari
     mbar_wait(bar, parity, kErrWaitDrain, err_word, kWaitLimitCycles, false);
 }
 
+// After a failed wait: make `bar` track every tcgen05 operation this thread issued and wait
+// (time limit only) until they have completed, so that TMEM is not released under them.
+static __device__ __noinline__ void mma_drain(uint64_t* bar, int* err_word) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_u32(bar)) : "memory");
+    mbar_wait(bar, 0, kErrWaitDrain, err_word, kWaitLimitCycles, false);
+}
+
 // Add `v` to a device-scope counter with release semantics: every write that this thread has
 // observed -- its own, and those of threads that synchronised with it before (a CTA barrier or
 // an mbarrier phase) -- is visible to a thread that reads the new count with acquire

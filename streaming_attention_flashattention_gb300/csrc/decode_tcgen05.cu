@@ -71,7 +71,7 @@ struct Layout {
     static constexpr int kV0 = kK0 + KS * kTileBytes;        // VS V slots
     static constexpr int kBar = kV0 + VS * kTileBytes;
     static constexpr int kNumBars = 32;
-    static_assert(2 + 2 * KS + 3 * VS + 6 + 2 + 4 <= kNumBars, "barrier block");
+    static_assert(2 + 2 * KS + 3 * VS + 6 + 2 + 4 + 1 <= kNumBars, "barrier block");
     static constexpr int kXm = kBar + kNumBars * 8;          // merge: m, l [2 slot][128]
     static constexpr int kInfo = kXm + 4 * 128 * 4;          // MtItem [2]
     static constexpr int kTmemSlot = kInfo + 2 * (int)sizeof(MtItem);
@@ -105,6 +105,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
     uint64_t* o_free = v_fix + VS;         // the merge has read both O accumulators
     uint64_t* item_full = o_free + 1;      // [2] item ring
     uint64_t* item_empty = item_full + 2;  // [2]
+    uint64_t* mma_idle = item_empty + 2;   // error exit: the issuer's products have completed
     float* xm = reinterpret_cast<float*>(smem + L::kXm);
     MtItem* info = reinterpret_cast<MtItem*>(smem + L::kInfo);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
@@ -132,6 +133,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
         }
         mbar_init(merge_bar, 8);
         mbar_init(o_free, 8);
+        mbar_init(mma_idle, 1);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, L::kTmemCols);
@@ -580,12 +582,14 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
 
     // TMEM is released only when no tensor-core work of the CTA can still be running: on
     // success the softmax warps have waited for the last P.V of each slot (the issuer's
-    // products complete in issue order); a role that gave up did so after a wait of
-    // kWaitLimitCycles, long after the products issued before it had completed.
+    // products complete in issue order); after an error the issuer has drained its
+    // products (mma_drain).
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
+        if (lane == 0 && device_error_set(p.err)) mma_drain(mma_idle, p.err);  // the issuer
+        __syncwarp();
         tmem_dealloc(tmem, L::kTmemCols);
     }
 }

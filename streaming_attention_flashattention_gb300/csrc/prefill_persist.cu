@@ -70,7 +70,7 @@ struct Layout {
     static constexpr int kOst = kV0 + VS * kTileBytes;       // O tile staged for its TMA store
     static constexpr int kBar = kOst + kTileBytes;
     static constexpr int kNumBars = 24;
-    static_assert(2 + 2 * KS + 2 * VS + 6 + 2 <= kNumBars, "barrier block");
+    static_assert(2 + 2 * KS + 2 * VS + 6 + 3 <= kNumBars, "barrier block");
     static constexpr int kXm = kBar + kNumBars * 8;          // merge: m, l [2 slot][128]
     static constexpr int kTmemSlot = kXm + 4 * 128 * 4;
     static constexpr int kBytes = kTmemSlot + 16;
@@ -131,6 +131,7 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
     uint64_t* o_done = p_ready + 2;        // [2] per slot
     uint64_t* merge_bar = o_done + 2;      // the two softmax warpgroups meet
     uint64_t* o_free = merge_bar + 1;      // the merge has read both O accumulators
+    uint64_t* mma_idle = o_free + 1;       // error exit: the issuer's products have completed
     float* xm = reinterpret_cast<float*>(smem + L::kXm);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -153,6 +154,7 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
         }
         mbar_init(merge_bar, 8);
         mbar_init(o_free, 8);
+        mbar_init(mma_idle, 1);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, L::kTmemCols);
@@ -505,12 +507,14 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
 
     // TMEM is released only when no tensor-core work of the CTA can still be running: on
     // success the softmax warps have waited for the last P.V of each slot (the issuer's
-    // products complete in issue order); a role that gave up did so after a wait of
-    // kWaitLimitCycles, long after the products issued before it had completed.
+    // products complete in issue order); after an error the issuer has drained its
+    // products (mma_drain).
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
+        if (lane == 0 && device_error_set(p.err)) mma_drain(mma_idle, p.err);  // the issuer
+        __syncwarp();
         tmem_dealloc(tmem, L::kTmemCols);
     }
 }

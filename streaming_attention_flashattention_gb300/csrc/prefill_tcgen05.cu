@@ -141,6 +141,7 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
     uint64_t* merge_bar = bars + 17; // KV-split mode: the two softmax warpgroups meet
     float* xm = reinterpret_cast<float*>(smem + L::kXm);   // [2][128] m, then [2][128] l
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+    uint64_t* mma_idle = reinterpret_cast<uint64_t*>(smem + L::kTmemSlot + 8);  // error exit
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -170,6 +171,7 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
             mbar_init(&k_empty[i], 1);
         }
         mbar_init(merge_bar, 8);
+        mbar_init(mma_idle, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
@@ -549,12 +551,14 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
 
     // TMEM is released only when no tensor-core work of the CTA can still be running: on
     // success the softmax warps have waited for the last P.V of each slot (the issuer's
-    // products complete in issue order); a role that gave up did so after a wait of
-    // kWaitLimitCycles, long after the products issued before it had completed.
+    // products complete in issue order); after an error the issuer has drained its
+    // products (mma_drain).
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
+        if (lane == 0 && device_error_set(p.err)) mma_drain(mma_idle, p.err);  // the issuer
+        __syncwarp();
         tmem_dealloc(tmem, L::kTmemCols);
     }
     // a tail launch finishes only after the pair-mode grid it overlaps
