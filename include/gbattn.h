@@ -79,7 +79,7 @@ enum {
  * Tile classes follow "ADR-0060" section 5.4: KV tiles entirely in a query tile's future
  * are skipped, tiles crossing the diagonal are masked, the rest run unmasked.
  * bf16 work items are pairs of Q tiles (one CTA each), or -- when pairs would not fill the
- * GPU twice over -- single Q tiles with their KV range split over a CTA's two slots, run by
+ * GPU once -- single Q tiles with their KV range split over a CTA's two slots, run by
  * at most one persistent CTA per SM that takes its tiles heaviest first.  When the pairs
  * weigh nearly the same (non-causal calls, or a chunk at the end of a long context) and
  * their last wave is at most half full, that wave's Q tiles run split in a second launch,

@@ -131,11 +131,12 @@ PrefillPlan prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, in
     const long long per_group = ((long long)pl.n_qblk * G + 1) / 2;
     pl.n_pairs = per_group * B * Hkv;
     pl.n_tiles = (long long)pl.n_qblk * B * Hq;
-    // Pairs of Q tiles keep both ping-pong slots busy with independent work; when they
-    // would not fill the SMs twice over, splitting each tile's KV range over the two slots
-    // halves the longest item instead, and the tiles run on persistent CTAs (one per SM,
-    // heaviest tiles dealt first) so that each SM pays the start-up once.
-    pl.kv_split = pl.n_pairs < 2LL * nsm;
+    // Pairs of Q tiles keep both ping-pong slots busy with independent work; when there are
+    // fewer pairs than SMs, splitting each tile's KV range over the two slots halves the
+    // longest item instead, and the tiles run on persistent CTAs (one per SM, heaviest
+    // tiles dealt first) so that each SM pays the start-up once.  (Between one and two
+    // pairs per SM the pair kernel measured 10-19% faster than the split.)
+    pl.kv_split = pl.n_pairs < (long long)nsm;
     // Pairs of nearly equal weight (non-causal, or a chunk at the end of a long context)
     // whose last wave is at most half full: those last pairs run as single Q tiles in
     // KV-split mode, launched behind the pair grid as a programmatic dependent so that they

@@ -169,6 +169,12 @@ def test_bf16_pair_mode_full_compare():
     check(small(1, 32, 8, 2560, 2560, 128, True, seed=17))
 
 
+def test_bf16_pair_mode_between_one_and_two_pairs_per_sm():
+    # 256 pairs on 152 SMs (1.7 per SM): pair mode since at least one pair per SM, one wave
+    # of 152 CTAs then 104 more (causal, so no KV-split tail)
+    check(small(1, 32, 8, 2048, 2048, 128, True, seed=37))
+
+
 def test_bf16_pair_mode_g1_causal_ragged_odd_tiles():
     # pair mode with G = 1: a CTA's two Q tiles are consecutive q blocks of one head with
     # different causal extents; 9 q blocks per head leave a last CTA with one tile, and

@@ -111,10 +111,15 @@ def test_prefill_pairs_and_kv_split_mode():
     # Llama3-70B causal prefill: 2048 pairs, heaviest first, one launch
     assert pre(1, 64, 8, 8192, 8192, True) == {"mode": "pairs", "first_launch_ctas": 2048,
                                                "tail_pairs": 0, "q_tiles": 4096}
-    # fewer than two pairs per SM: single Q tiles with their KV range split over a CTA's
+    # fewer pairs than SMs (128): single Q tiles with their KV range split over a CTA's
     # two slots, on one persistent CTA per SM
     assert pre(2, 8, 2, 2048, 2048, True) == {"mode": "kv_split", "first_launch_ctas": 152,
                                               "tail_pairs": 0, "q_tiles": 256}
+    # one pair per SM or more (256): pairs
+    assert pre(1, 32, 8, 2048, 2048, True) == {"mode": "pairs", "first_launch_ctas": 256,
+                                               "tail_pairs": 0, "q_tiles": 512}
+    assert pre(1, 4, 1, 9728, 9728, True)["mode"] == "pairs"        # exactly 152 pairs
+    assert pre(1, 4, 1, 9600, 9600, True)["mode"] == "kv_split"     # 150 pairs
     # fewer Q tiles than SMs: one CTA per tile
     assert pre(1, 8, 2, 1024, 1024, True)["first_launch_ctas"] == 64
 
