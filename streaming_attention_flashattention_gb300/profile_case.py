@@ -7,6 +7,11 @@ calls the library `--reps` times with nothing else on the GPU.  Examples:
     python -m streaming_attention_flashattention_gb300.profile_case prefill --workload 3
     python -m streaming_attention_flashattention_gb300.profile_case decode --workload 4
     python -m streaming_attention_flashattention_gb300.profile_case multitoken --keys 16384 --splits 4
+    python -m streaming_attention_flashattention_gb300.profile_case ringstep
+
+`ringstep` is one rank's step of an 8-rank ring-KV prefill of the Llama3-70B shape (8 query
+heads x 8192 positions against KV slice 3 of 8, attn_fwd_positions) followed by the merge of
+its result into an fp32 accumulator (attn_merge), each call `--reps` times.
 
 `--keys` / `--splits` shrink a decode or multi-token workload (cache length and split count)
 so that a full-metric capture stays small.
@@ -22,9 +27,30 @@ import streaming_attention_flashattention_gb300 as gb
 from streaming_attention_flashattention_gb300 import build
 
 
+def ring_step(reps: int) -> None:
+    w = wl.WORKLOADS[3]
+    S, L = w.Sq, w.Skv // 8
+    g = torch.Generator().manual_seed(97)
+    q = torch.randn((1, 8, S, w.d), generator=g).to(torch.bfloat16).cuda()
+    k = torch.randn((1, 1, L, w.d), generator=g).to(torch.bfloat16).cuda()
+    v = torch.randn((1, 1, L, w.d), generator=g).to(torch.bfloat16).cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty((1, 8, S), dtype=torch.float32, device="cuda")
+    acc_o = torch.zeros((1, 8, S, w.d), dtype=torch.float32, device="cuda")
+    acc_l = torch.full((1, 8, S), float("-inf"), device="cuda")
+    for _ in range(reps):
+        gb.attn_fwd_positions(q, k, v, 0, 3 * L, scale=w.scale, out=o, lse=lse)
+        gb.attn_merge(acc_o, acc_l, o, lse, out=acc_o, lse_out=acc_l)
+    torch.cuda.synchronize()
+    st, word = gb.attn_last_device_error()
+    if st != 0 or not torch.isfinite(acc_o).all():
+        raise SystemExit(f"ring step failed: status {st}, word {word}")
+    print(f"ok ringstep reps={reps}")
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill", "decode", "chunk", "multitoken"])
+    ap.add_argument("case", choices=["prefill", "decode", "chunk", "multitoken", "ringstep"])
     ap.add_argument("--workload", type=int, default=None, help="workload index (default per case)")
     ap.add_argument("--keys", type=int, default=0, help="decode / multi-token: cache length override")
     ap.add_argument("--splits", type=int, default=-1, help="decode / multi-token: split count override")
@@ -32,6 +58,9 @@ def main() -> None:
     args = ap.parse_args()
     build.build()
     gb.load_library()
+    if args.case == "ringstep":
+        ring_step(args.reps)
+        return
     default = {"prefill": 3, "decode": 4, "chunk": 6, "multitoken": 7}[args.case]
     idx = args.workload if args.workload is not None else default
     w = wl.WORKLOADS.get(idx) or wl.EXTRA_WORKLOADS[idx]
