@@ -274,3 +274,34 @@ def test_decode_reduce_threads_equal_single_device(world, root):
         assert o.dtype == torch.bfloat16
         compare(o.float().cpu().numpy(), l.cpu().numpy(), o_ref[:, :, 0], l_ref[:, :, 0],
                 "bf16", f"decode P{world} root {root}")
+
+
+@pytest.mark.parametrize("Sq", [1, 5, 128, 129])
+@pytest.mark.parametrize("Skv", [1, 5, 128, 129])
+@pytest.mark.parametrize("shift", [-200, -3, 0, 2, 300])
+def test_positions_grid_against_oracle(Sq, Skv, shift):
+    # query i at position shift + i, key j at position j: every mix of rows that see no key,
+    # some keys and all keys across the tile edges (d = 64, G = 2)
+    q, k, v = bf16((1, 2, Sq, 64), 50 + Sq), bf16((1, 1, Skv, 64), 60 + Skv), bf16((1, 1, Skv, 64), 70 + Skv)
+    o, lse = gb.attn_fwd_positions(q.cuda(), k.cuda(), v.cuda(), shift, 0, scale=0.125)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.attention_at_positions(wl.to_oracle(q), wl.to_oracle(k), wl.to_oracle(v),
+                                                 0.125, shift, 0)
+    compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "bf16",
+            f"positions grid {Sq}x{Skv} shift {shift}")
+
+
+def test_ring_prefill_threads_noncausal():
+    world, Hq, Hkv, L, d = 2, 8, 2, 256, 128
+    n = L * world
+    q, k, v = bf16((1, Hq, n, d), 81), bf16((1, Hkv, n, d), 82), bf16((1, Hkv, n, d), 83)
+    hr = Hq // world
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    res = run_ranks(world, lambda r, comm: sp.ring_prefill(
+        qd[:, r * hr:(r + 1) * hr].contiguous(), kd[:, :, r * L:(r + 1) * L].contiguous(),
+        vd[:, :, r * L:(r + 1) * L].contiguous(), group_size=Hq // Hkv, causal=False, comm=comm))
+    o_ref, l_ref = oracle.attention(wl.to_oracle(q), wl.to_oracle(k), wl.to_oracle(v),
+                                    1.0 / math.sqrt(d), False)
+    for r, (o, l) in enumerate(res):
+        compare(o.float().cpu().numpy(), l.cpu().numpy(), o_ref[:, r * hr:(r + 1) * hr],
+                l_ref[:, r * hr:(r + 1) * hr], "bf16", f"ring non-causal rank {r}")
