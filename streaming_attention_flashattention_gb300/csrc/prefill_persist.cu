@@ -70,7 +70,7 @@ struct Layout {
     static constexpr int kOst = kV0 + VS * kTileBytes;       // O tile staged for its TMA store
     static constexpr int kBar = kOst + kTileBytes;
     static constexpr int kNumBars = 24;
-    static_assert(2 + 2 * KS + 2 * VS + 6 + 3 <= kNumBars, "barrier block");
+    static_assert(2 + 2 * KS + 2 * VS + 6 + 4 <= kNumBars, "barrier block");
     static constexpr int kXm = kBar + kNumBars * 8;          // merge: m, l [2 slot][128]
     static constexpr int kTmemSlot = kXm + 4 * 128 * 4;
     static constexpr int kBytes = kTmemSlot + 16;
@@ -132,6 +132,7 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
     uint64_t* merge_bar = o_done + 2;      // the two softmax warpgroups meet
     uint64_t* o_free = merge_bar + 1;      // the merge has read both O accumulators
     uint64_t* mma_idle = o_free + 1;       // error exit: the issuer's products have completed
+    uint64_t* staged = mma_idle + 1;       // every merge warp has written its rows of the staging tile
     float* xm = reinterpret_cast<float*>(smem + L::kXm);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -155,6 +156,7 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
         mbar_init(merge_bar, 8);
         mbar_init(o_free, 8);
         mbar_init(mma_idle, 1);
+        mbar_init(staged, 8);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, L::kTmemCols);
@@ -483,10 +485,16 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
                     p.lse[((long long)it.b * p.Hq + it.h) * p.Sq + row] =
                         lt > 0.f ? (M + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
             }
-            // the staged tile is complete once all 256 merge threads pass the barrier
+            // the staged tile is complete once all 8 merge warps have arrived; only the store
+            // thread waits (bounded), so a warp that left the loop after an error cannot hold
+            // the others at a hardware barrier. A warp arrives for tile k + 1 only after the
+            // meet of tile k + 1, which the store thread reaches after this wait: the phases
+            // cannot overtake one another.
             fence_proxy_async_smem();
-            named_barrier_sync(1, 256);
-            if (threadIdx.x == kStoreThread && GBATTN_IN_BOUNDS(it.b * p.Hq + it.h, p.B * p.Hq, p.err) &&
+            __syncwarp();
+            if (lane == 0) mbar_arrive(staged);
+            if (threadIdx.x == kStoreThread && mbar_wait(staged, k & 1, kErrWaitSoftmax, p.err) &&
+                GBATTN_IN_BOUNDS(it.b * p.Hq + it.h, p.B * p.Hq, p.err) &&
                 GBATTN_IN_BOUNDS(it.q0, p.Sq, p.err)) {
                 #pragma unroll
                 for (int bx = 0; bx < L::kBoxes; ++bx)
