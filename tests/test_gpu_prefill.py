@@ -99,6 +99,40 @@ def test_bf16_sharp_softmax_rescale_path():
     check(small(1, 2, 1, 256, 1024, 128, True, q_scale=6.0, seed=11))
 
 
+@pytest.mark.parametrize("causal,Hq,Hkv,Sq", [
+    (False, 2, 1, 128),      # KV-split mode (persistent CTAs)
+    (True, 64, 8, 1024),     # pair mode: 256 pairs of Q tiles
+    (False, 64, 8, 1024),
+])
+def test_bf16_max_moves_in_some_rows_of_a_warp(causal, Hq, Hkv, Sq):
+    # Keys 512 + (r mod 128) are aligned with query row r of head 0 for every third row r,
+    # so those rows' running max jumps by far more than 2^8 in a later KV tile while most
+    # other rows of the same warps keep theirs: within one warp some rows rescale their O
+    # accumulator and row sum and the others do not.
+    w = small(1, Hq, Hkv, Sq, 1024, 128, causal, seed=13)
+    q, k, v = wl.prefill_inputs(w)
+    qf = q.float()
+    for r in range(0, Sq, 3):
+        if causal and 512 + r % 128 > r + (w.Skv - w.Sq):
+            continue
+        u = qf[0, 0, r] / qf[0, 0, r].norm()
+        k[0, 0, 512 + r % 128] = (21.0 * u).to(k.dtype)
+    # precondition, in fp32 on the stored values: within one warp of head 0, some rows' max
+    # after their first KV tile is exceeded by more than 2^8 later on and some rows' is not
+    c = w.scale / math.log(2.0)
+    s = (qf[0, 0] @ k[0, 0].float().T) * c
+    if causal:
+        s = s.masked_fill(torch.ones(w.Sq, w.Skv, dtype=torch.bool).triu(w.Skv - w.Sq + 1), -math.inf)
+    first = s[:, :128].max(dim=1).values
+    moves = (s[:, 128:].max(dim=1).values > first + 8.0).numpy()
+    warps = moves[: Sq // 32 * 32].reshape(-1, 32)
+    assert (warps.any(axis=1) & ~warps.all(axis=1)).any()
+    o, lse = run_gpu(q, k, v, w.causal, w.scale)
+    o_ref, lse_ref = oracle.attention(wl.to_oracle(q), wl.to_oracle(k), wl.to_oracle(v),
+                                      w.scale, w.causal)
+    compare(o, lse, o_ref, lse_ref, w.dtype, w.name)
+
+
 def test_workload2_causal_gqa_prefill_full():
     check(wl.WORKLOADS[2])
 
