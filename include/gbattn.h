@@ -113,7 +113,7 @@ int attn_fwd_counted(const void* q, const void* k, const void* v, void* o, float
 
 /*
  * attn_fwd_host_workspace_size -- device bytes attn_fwd_host needs for these sizes on the
- * current device (two staging buffer sets); 0 for invalid sizes.
+ * current device (up to three staging buffer sets); 0 for invalid sizes.
  */
 size_t attn_fwd_host_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int d, int dtype);
 
@@ -132,9 +132,10 @@ size_t attn_fwd_host_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int
  *                        queued on `stream` afterwards runs after its last copy has landed
  *                        in host memory (synchronise on it before reading o / lse)
  *
- * The (batch, KV head) groups are cut into up to 4 chunks, each large enough for the
- * kernel's pair mode, and staged through two device buffer sets on internal copy streams:
- * chunk i+1 is copied in and chunk i-1 copied out while chunk i computes.  Calls on one
+ * The (batch, KV head) groups are cut into chunks, each the smallest that keeps the
+ * kernel's pair mode (a pair of Q tiles per SM), and staged through up to three device
+ * buffer sets on internal copy streams: chunks i+1 and i+2 are copied in and chunk i-1
+ * copied out while chunk i computes.  Calls on one
  * device are serialised on the host; calls sharing a workspace must be ordered on one
  * stream.  Requirements and status codes as attn_fwd, plus GBATTN_ERR_WORKSPACE.
  */

@@ -206,14 +206,18 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, fl
 
 // ---- host-buffer prefill: chunked copies in and out overlapped with the kernel ----------
 // The work is cut into chunks of consecutive (batch, KV head) groups -- each a contiguous
-// slab of Q/O ([G, Sq, d]), K and V ([Skv, d]) and LSE ([G, Sq]) -- staged through two
-// device buffer sets.  Chunk i's copy in waits for chunk i-2's copy out (the same buffers),
-// its kernel for its copy in, its copy out for its kernel, so chunk i+1 comes in and chunk
-// i-1 goes out while chunk i computes.
+// slab of Q/O ([G, Sq, d]), K and V ([Skv, d]) and LSE ([G, Sq]) -- staged through up to
+// three device buffer sets.  Chunk i's copy in waits for chunk i-3's copy out (the same
+// buffers), its kernel for its copy in, its copy out for its kernel, so chunks i+1 and i+2
+// come in and chunk i-1 goes out while chunk i computes.  (With two sets, chunk i's copy in
+// waited for chunk i-2's copy out, which itself waits for chunk i-2's kernel: the link sat
+// idle in between.)
+constexpr int kHostSets = 3;
+
 struct HostPlan {
     int cg;                  // groups per chunk
     int n_chunks;
-    int n_bufs;              // buffer sets (2 when there are several chunks)
+    int n_bufs;              // buffer sets: min(n_chunks, kHostSets)
     size_t q_off, k_off, v_off, o_off, l_off, set_bytes;   // one buffer set
 };
 
@@ -224,14 +228,13 @@ HostPlan host_plan(int B, int Hq, int Hkv, int Sq, int Skv, int d, size_t esize,
     const int G = Hq / Hkv;
     const long long ng = (long long)B * Hkv;
     const long long pairs_per_group = ((long long)((Sq + 127) / 128) * G + 1) / 2;
-    // the smallest chunk that keeps the kernel's pair mode (>= 2 Q-tile pairs per SM), and
-    // no more than 4 chunks
-    long long cg = (2LL * nsm + pairs_per_group - 1) / pairs_per_group;
-    cg = std::max(cg, (ng + 3) / 4);
+    // the smallest chunk that keeps the kernel's pair mode (a Q-tile pair per SM): small
+    // chunks shorten the first copy in and the last kernel and copy out, which nothing hides
+    long long cg = ((long long)nsm + pairs_per_group - 1) / pairs_per_group;
     cg = std::min(std::max(cg, 1LL), ng);
     h.cg = (int)cg;
     h.n_chunks = (int)((ng + cg - 1) / cg);
-    h.n_bufs = h.n_chunks > 1 ? 2 : 1;
+    h.n_bufs = std::min(h.n_chunks, kHostSets);
     const size_t qb = (size_t)cg * G * Sq * d * esize;
     const size_t kb = (size_t)cg * Skv * d * esize;
     const size_t lb = (size_t)cg * G * Sq * 4;
@@ -248,7 +251,7 @@ HostPlan host_plan(int B, int Hq, int Hkv, int Sq, int Skv, int d, size_t esize,
 struct HostPipe {
     cudaStream_t in = nullptr, out = nullptr;
     cudaEvent_t entry = nullptr, done = nullptr;
-    cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_comp[2] = {nullptr, nullptr}, ev_out[2] = {nullptr, nullptr};
+    cudaEvent_t ev_in[kHostSets] = {}, ev_comp[kHostSets] = {}, ev_out[kHostSets] = {};
     std::mutex mu;           // one host-buffer call at a time per device
 };
 
@@ -264,13 +267,13 @@ HostPipe* host_pipe() {
              cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) == cudaSuccess &&
              cudaEventCreateWithFlags(&h.entry, cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&h.done, cudaEventDisableTiming) == cudaSuccess;
-        for (int i = 0; i < 2 && ok; ++i)
+        for (int i = 0; i < kHostSets && ok; ++i)
             ok = cudaEventCreateWithFlags(&h.ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
                  cudaEventCreateWithFlags(&h.ev_comp[i], cudaEventDisableTiming) == cudaSuccess &&
                  cudaEventCreateWithFlags(&h.ev_out[i], cudaEventDisableTiming) == cudaSuccess;
     });
     HostPipe& h = pipes[dev];
-    return (h.in && h.out && h.done && h.ev_out[1]) ? &h : nullptr;
+    return (h.in && h.out && h.done && h.ev_out[kHostSets - 1]) ? &h : nullptr;
 }
 
 // Query rows of a decode call per KV head (G * Tq, chunks of 8) and how work items group

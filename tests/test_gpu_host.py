@@ -28,8 +28,9 @@ def _w(B, Hq, Hkv, S, d, causal, dtype="bf16", seed=41):
 
 
 def test_host_pipeline_matches_oracle_several_chunks():
-    # 8 (b, KV head) groups of 64 Q-tile pairs: chunks of 5 groups, the last one partial
-    w = _w(1, 64, 8, 2048, 128, True)
+    # 16 (b, KV head) groups of 64 Q-tile pairs: chunks of 3 groups (one pair per SM), the
+    # last of 1, so 6 chunks go through the 3 staging sets and every set is reused
+    w = _w(2, 64, 8, 2048, 128, True)
     q, k, v = wl.prefill_inputs(w)
     o, lse = gb.attn_fwd_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), causal=True)
     torch.cuda.synchronize()
