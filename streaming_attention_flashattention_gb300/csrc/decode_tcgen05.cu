@@ -50,6 +50,7 @@ constexpr int kSoftmaxWarp0 = 4;
 constexpr int KS = 2;                     // K ring slots
 constexpr int VS = 3;                     // V ring slots
 constexpr float kRescaleThreshold = 8.0f; // log2 units: move the running max only by > 2^8
+constexpr int kPubSlots = 4;              // publisher ring entries (finished partials)
 static_assert(kKeysT == 128, "the softmax row reductions assume 128 columns");
 
 // One work item as the producer hands it to the MMA and softmax warps.
@@ -70,12 +71,13 @@ struct Layout {
     static constexpr int kK0 = kTileBytes;                   // KS K slots
     static constexpr int kV0 = kK0 + KS * kTileBytes;        // VS V slots
     static constexpr int kBar = kV0 + VS * kTileBytes;
-    static constexpr int kNumBars = 32;
-    static_assert(2 + 2 * KS + 3 * VS + 6 + 2 + 4 + 1 <= kNumBars, "barrier block");
+    static constexpr int kNumBars = 40;
+    static_assert(2 + 2 * KS + 3 * VS + 6 + 2 + 4 + 1 + 2 * kPubSlots <= kNumBars, "barrier block");
     static constexpr int kXm = kBar + kNumBars * 8;          // merge: m, l [2 slot][128]
     static constexpr int kInfo = kXm + 4 * 128 * 4;          // MtItem [2]
     static constexpr int kTmemSlot = kInfo + 2 * (int)sizeof(MtItem);
-    static constexpr int kBytes = kTmemSlot + 16;
+    static constexpr int kPubGroup = kTmemSlot + 16;         // publisher ring: group per entry
+    static constexpr int kBytes = kPubGroup + kPubSlots * 4;
     static constexpr int kAlloc = kBytes + 1024;
     static constexpr uint32_t kColS0 = 0, kColS1 = 128;
     static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
@@ -106,6 +108,9 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
     uint64_t* item_full = o_free + 1;      // [2] item ring
     uint64_t* item_empty = item_full + 2;  // [2]
     uint64_t* mma_idle = item_empty + 2;   // error exit: the issuer's products have completed
+    uint64_t* pub_full = mma_idle + 1;     // [kPubSlots] softmax warps -> publisher (partial written)
+    uint64_t* pub_empty = pub_full + kPubSlots;   // [kPubSlots] publisher -> softmax warps
+    int* pub_group = reinterpret_cast<int*>(smem + L::kPubGroup);   // [kPubSlots]
     float* xm = reinterpret_cast<float*>(smem + L::kXm);
     MtItem* info = reinterpret_cast<MtItem*>(smem + L::kInfo);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
@@ -134,6 +139,10 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
         mbar_init(merge_bar, 8);
         mbar_init(o_free, 8);
         mbar_init(mma_idle, 1);
+        for (int i = 0; i < kPubSlots; ++i) {
+            mbar_init(&pub_full[i], 8);
+            mbar_init(&pub_empty[i], 1);
+        }
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, L::kTmemCols);
@@ -186,11 +195,17 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
             piece_range(t0, t1, p.pieces, pc, t0, t1);
             const int part = s * p.pieces + pc;
             if (t0 >= t1) {
-                // an empty piece of a non-empty split: a partial that weighs nothing
-                const int nrows = min(kRowsT, p.R - rt * kRowsT);
-                for (int i = lane; i < nrows; i += 32)
-                    if (GBATTN_IN_BOUNDS((row0 + i) * p.n_parts + part, (long long)p.B * p.Hq * p.Tq * p.n_parts, p.err))
-                        p.ws_lse[(row0 + i) * p.n_parts + part] = -INFINITY;
+                // an empty piece of a non-empty split: a partial that weighs nothing (written
+                // by one lane, which then counts it with a release covering its writes)
+                if (lane == 0) {
+                    const int nrows = min(kRowsT, p.R - rt * kRowsT);
+                    for (int i = 0; i < nrows; ++i)
+                        if (GBATTN_IN_BOUNDS((row0 + i) * p.n_parts + part, (long long)p.B * p.Hq * p.Tq * p.n_parts, p.err))
+                            p.ws_lse[(row0 + i) * p.n_parts + part] = -INFINITY;
+                    if (p.counted && GBATTN_IN_BOUNDS((long long)b * p.Hkv + kvh, (long long)p.B * p.Hkv, p.err))
+                        counter_add_release(p.group_cnt + (long long)b * p.Hkv + kvh, 1);
+                }
+                __syncwarp();
                 continue;
             }
             const int nt = (t1 - t0 + kKeysT - 1) / kKeysT;
@@ -407,6 +422,24 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                 ++k;
             }
         }
+    } else if (warp == 3) {
+        // ================================ publisher =================================
+        // Counts each finished partial into its (sequence, KV head) group with a device-scope
+        // release, so that the combine, which reads the count with acquire, can merge the group
+        // while the grid is still running.  The softmax warps' writes of the partial happen
+        // before their arrivals here (CTA-scope mbarrier release / acquire), so the release
+        // covers them; it waits for those writes to land, on this otherwise idle warp.
+        if (lane == 0 && p.counted) {
+            for (uint32_t k = 0;; ++k) {
+                const uint32_t ps = k % kPubSlots;
+                if (!mbar_wait(&pub_full[ps], (k / kPubSlots) & 1, kErrWaitConsumer, p.err)) break;
+                const int g = pub_group[ps];
+                if (g < 0) break;                    // the softmax warps are done
+                if (GBATTN_IN_BOUNDS(g, (long long)p.B * p.Hkv, p.err))
+                    counter_add_release(p.group_cnt + g, 1);
+                mbar_arrive(&pub_empty[ps]);
+            }
+        }
     } else if (warp >= kSoftmaxWarp0) {
         // =============================== softmax warps ================================
         const int t = (warp - kSoftmaxWarp0) >> 2;     // slot of this warpgroup
@@ -426,7 +459,15 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
             if (!mbar_wait(&item_full[k & 1], (k >> 1) & 1, kErrWaitSoftmax, p.err)) break;
             // read from shared memory where used (few registers); released after the merge
             const MtItem& it = info[k & 1];
-            if (it.done) break;
+            if (it.done) {
+                // tell the publisher (all eight arrivals from one thread)
+                if (p.counted && warp == kSoftmaxWarp0 && lane == 0 &&
+                    mbar_wait(&pub_empty[k % kPubSlots], ((k / kPubSlots) & 1) ^ 1u, kErrWaitSoftmax, p.err)) {
+                    pub_group[k % kPubSlots] = -1;
+                    for (int i = 0; i < 8; ++i) mbar_arrive(&pub_full[k % kPubSlots]);
+                }
+                break;
+            }
             const int nt = (it.t1 - it.t0 + kKeysT - 1) / kKeysT;
             const int n0 = (nt + 1) / 2, n1 = nt - n0;
             const int n_t = t == 0 ? n0 : n1;           // this slot's key tiles
@@ -511,7 +552,15 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                 ls[t * 128 + r] = l;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(merge_bar);
+            if (lane == 0) {
+                // the publisher entry of this item: free once the item kPubSlots back has been
+                // counted; claimed before the meet, so no warp arrives on it earlier
+                if (p.counted && warp == kSoftmaxWarp0) {
+                    if (mbar_wait(&pub_empty[k % kPubSlots], ((k / kPubSlots) & 1) ^ 1u, kErrWaitSoftmax, p.err))
+                        pub_group[k % kPubSlots] = it.b * p.Hkv + it.kvh;
+                }
+                mbar_arrive(merge_bar);
+            }
             if (!mbar_wait(merge_bar, k & 1, kErrWaitSoftmax, p.err)) break;
             // the other slot's last completion, already seen by its warpgroup
             const int u = 1 - t;
@@ -572,6 +621,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(o_free);
+                if (p.counted) mbar_arrive(&pub_full[k % kPubSlots]);   // this warp's rows are written
                 mbar_arrive(&item_empty[k & 1]);
             }
             cs0 += (uint32_t)n0;
@@ -601,7 +651,7 @@ cudaError_t launch_mt(const DecodeTcParams& p, int nsm, cudaStream_t stream) {
     cudaError_t err = cudaFuncSetAttribute(decode_mt_kernel<D>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    err = cudaMemsetAsync(p.counter, 0, sizeof(int), stream);
+    err = cudaMemsetAsync(p.counter, 0, (p.counted ? 1 + (size_t)p.B * p.Hkv : 1) * sizeof(int), stream);
     if (err != cudaSuccess) return err;
     decode_mt_kernel<D><<<min(p.n_items, nsm), kThreads, smem, stream>>>(p);
     return cudaGetLastError();

@@ -83,15 +83,17 @@ def prefill_shapes(nsm: int):
 
 DECODE_DRAWS = 6
 DECODE_KINDS = ("single_launch", "combine_per_group", "combine_per_group+pieces",
-                "mt:single_launch", "mt:combine", "mt:tcgen05")
+                "mt:single_launch", "mt:combine", "mt:tcgen05+combine_per_group",
+                "mt:tcgen05+combine")
 
 
 def decode_kind(Tq: int, plan: dict) -> str:
     """Single-token calls merge in the split kernel (single launch) or per group (with or
     without pieces); multi-token calls (mt:) run the warp kernel with either merge, or the
-    tcgen05 kernel with the combine kernel."""
+    tcgen05 kernel with the per-group combine (one 128-row tile per KV head) or the combine
+    that waits for the grid (more rows)."""
     if plan["kernel"] == "tcgen05":
-        k = "tcgen05"
+        k = "tcgen05+" + plan["merge"]
     else:
         k = plan["merge"] + ("+pieces" if plan["pieces"] > 1 else "")
     return ("mt:" + k) if Tq > 1 else k
@@ -110,7 +112,7 @@ def decode_shapes(nsm: int):
         B = int(rng.integers(1, 7))
         Hkv = int(rng.choice([1, 2, 4, 8]))
         G = int(rng.choice([1, 2, 4, 8]))
-        Tq = int(rng.integers(2, 13)) if multi else 1
+        Tq = int(rng.choice(list(range(2, 13)) + [17, 20, 33])) if multi else 1
         d = int(rng.choice([64, 128]))
         hi = int(rng.choice([600, 5000, 40000]))
         lens = [int(rng.choice(special)) if rng.random() < 0.25 else int(rng.integers(1, hi + 1))
