@@ -51,6 +51,13 @@ constexpr int KS = 2;                     // K ring slots
 constexpr int VS = 3;                     // V ring slots
 constexpr float kRescaleThreshold = 8.0f; // log2 units: move the running max only by > 2^8
 constexpr int kPubSlots = 4;              // publisher ring entries (finished partials)
+#ifdef GBATTN_DEBUG_CHECKS
+// Test hook of the debug build: CTA 0 of the grid does not issue the K fill with this index
+// (counted over the CTA's fills; -1: none).  The fill's barrier then never completes, the wait
+// for it runs out after its time limit and records its code in the error word, and every role
+// of every CTA leaves through its give-up exit.  Set by attn_debug_skip_fill.
+__device__ int g_skip_k_fill = -1;
+#endif
 static_assert(kKeysT == 128, "the softmax row reductions assume 128 columns");
 
 // One work item as the producer hands it to the MMA and softmax warps.
@@ -160,7 +167,11 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
         }
         uint32_t nf = 0;         // K fills so far (all items)
         uint32_t k = 0;          // items handed over so far
+        uint32_t nq = 0;         // Q fills issued (lane 0)
         bool ok = true;
+#ifdef GBATTN_DEBUG_CHECKS
+        uint32_t skipped = 0xffffffffu;   // the fill the test hook left out
+#endif
         while (ok) {
             int item = 0;
             if (lane == 0) item = atomicAdd(p.counter, 1);
@@ -228,6 +239,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                     #pragma unroll
                     for (int bx = 0; bx < L::kBoxes; ++bx)
                         tma_load_3d(smem + L::kQ0 + bx * L::kBoxBytes, &p.tmap_q, bx * 64, (int)row0, 0, q_full);
+                    ++nq;
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -240,6 +252,11 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                     const uint32_t ks = nf % KS, kph = (nf / KS) & 1;
                     if (lane == 0) {
                         ok = mbar_wait(&k_empty[ks], kph ^ 1u, kErrWaitProducer, p.err);
+#ifdef GBATTN_DEBUG_CHECKS
+                        if (ok && blockIdx.x == 0 && (int)nf == g_skip_k_fill) {
+                            skipped = nf;
+                        } else
+#endif
                         if (ok) {
                             mbar_arrive_expect_tx(&k_full[ks], L::kTileBytes);
                             #pragma unroll
@@ -249,7 +266,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                         }
                     }
                     ok = __shfl_sync(0xffffffffu, ok, 0);
-                    ++nf;
+                    nf += ok ? 1u : 0u;   // (a fill not issued is not drained)
                 }
             }
         }
@@ -262,9 +279,13 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
             // this CTA takes no more work: the combine grid may start being scheduled
             asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             // drain: the last fills of Q and of each K slot must land before the CTA exits
-            if (k > 0) mbar_wait_drain(q_full, (k - 1) & 1, p.err);
-            for (uint32_t f = nf >= (uint32_t)KS ? nf - KS : 0; f < nf; ++f)
+            if (nq > 0) mbar_wait_drain(q_full, (nq - 1) & 1, p.err);
+            for (uint32_t f = nf >= (uint32_t)KS ? nf - KS : 0; f < nf; ++f) {
+#ifdef GBATTN_DEBUG_CHECKS
+                if (f == skipped) continue;
+#endif
                 mbar_wait_drain(&k_full[f % KS], (f / KS) & 1, p.err);
+            }
         }
     } else if (warp == 2) {
         // ================================== V producer ==================================
@@ -303,6 +324,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                         }
                     }
                     ok = __shfl_sync(0xffffffffu, ok, 0);
+                    const uint32_t issued = ok ? 1u : 0u;   // (a fill not issued is not drained)
                     if (ok && key0 + kKeysT > it.len) {
                         // the tile crossing len (at most one per split): zero its rows past len
                         bool landed = true;
@@ -323,7 +345,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                             ok = false;
                         }
                     }
-                    ++nf;
+                    nf += issued;
                 }
             }
         }
@@ -663,5 +685,11 @@ cudaError_t launch_decode_multitoken_tc(const DecodeTcParams& p, int d, int nsm,
     if (p.n_items <= 0) return cudaSuccess;
     return d == 128 ? launch_mt<128>(p, nsm, stream) : launch_mt<64>(p, nsm, stream);
 }
+
+#ifdef GBATTN_DEBUG_CHECKS
+cudaError_t debug_skip_fill_multitoken(int fill) {
+    return cudaMemcpyToSymbol(g_skip_k_fill, &fill, sizeof(int));
+}
+#endif
 
 }  // namespace gbattn

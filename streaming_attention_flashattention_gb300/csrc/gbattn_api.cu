@@ -14,6 +14,9 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#ifdef GBATTN_DEBUG_CHECKS
+#include "gbattn_debug.h"
+#endif
 
 namespace gbattn {
 
@@ -909,6 +912,27 @@ int attn_prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int n
     plan[3] = (int)pl.n_tiles;
     return GBATTN_OK;
 }
+
+#ifdef GBATTN_DEBUG_CHECKS
+}  // extern "C"
+namespace gbattn {
+cudaError_t debug_skip_fill_persist(int fill);
+cudaError_t debug_skip_fill_multitoken(int fill);
+}  // namespace gbattn
+extern "C" {
+
+int attn_debug_skip_fill(int kernel, int fill) {
+    if (fill < -1) return GBATTN_ERR_INVALID_ARG;
+    cudaError_t e;
+    if (kernel == GBATTN_DEBUG_PERSISTENT_PREFILL)
+        e = debug_skip_fill_persist(fill);
+    else if (kernel == GBATTN_DEBUG_MULTITOKEN_DECODE)
+        e = debug_skip_fill_multitoken(fill);
+    else
+        return GBATTN_ERR_INVALID_ARG;
+    return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+#endif
 
 int attn_selftest_bounded_wait(void* stream) {
     int* err = device_error_word();

@@ -57,6 +57,13 @@ constexpr int KS = 2;                     // K ring slots
 constexpr int VS = 2;                     // V ring slots
 constexpr float kRescaleThreshold = 8.0f; // log2 units: move the running max only by > 2^8
 constexpr int kStoreThread = kSoftmaxWarp0 * 32;   // issues the O tiles' TMA stores
+#ifdef GBATTN_DEBUG_CHECKS
+// Test hook of the debug build: CTA 0 of the grid does not issue the K fill with this index
+// (counted over the CTA's fills; -1: none).  The fill's barrier then never completes, the wait
+// for it runs out after its time limit and records its code in the error word, and every role
+// of every CTA leaves through its give-up exit.  Set by attn_debug_skip_fill.
+__device__ int g_skip_k_fill = -1;
+#endif
 static_assert(kBlockN == 128, "the softmax row reductions assume 128 columns");
 
 template <int D>
@@ -173,6 +180,9 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
             uint32_t nf = 0;         // K fills so far (all tiles)
             int k = 0;               // Q tiles so far
             bool ok = true;
+#ifdef GBATTN_DEBUG_CHECKS
+            uint32_t skipped = 0xffffffffu;   // the fill the test hook left out
+#endif
             QTile it;
             for (; ok && tile_of(p, k, it); ++k) {
                 // Q once the previous tile's last S product has read the buffer
@@ -190,6 +200,12 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
                         const int tile = t == 0 ? j : n0 + j;
                         const uint32_t ks = nf % KS, kph = (nf / KS) & 1;
                         if (!(ok = mbar_wait(&k_empty[ks], kph ^ 1u, kErrWaitProducer, p.err))) break;
+#ifdef GBATTN_DEBUG_CHECKS
+                        if (blockIdx.x == 0 && (int)nf == g_skip_k_fill) {
+                            skipped = nf++;
+                            continue;
+                        }
+#endif
                         mbar_arrive_expect_tx(&k_full[ks], L::kTileBytes);
                         #pragma unroll
                         for (int bx = 0; bx < L::kBoxes; ++bx)
@@ -201,8 +217,12 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
             }
             // drain: the last fills of Q and of each K slot must land before the CTA exits
             if (k > 0) mbar_wait_drain(q_full, (k - 1) & 1, p.err);
-            for (uint32_t f = nf >= (uint32_t)KS ? nf - KS : 0; f < nf; ++f)
+            for (uint32_t f = nf >= (uint32_t)KS ? nf - KS : 0; f < nf; ++f) {
+#ifdef GBATTN_DEBUG_CHECKS
+                if (f == skipped) continue;
+#endif
                 mbar_wait_drain(&k_full[f % KS], (f / KS) & 1, p.err);
+            }
         }
     } else if (warp == 2) {
         // ================================ V producer =================================
@@ -545,5 +565,11 @@ cudaError_t launch_attn_fwd_bf16_persistent(const PrefillParams& p, int d, int n
     if (p.n_pairs <= 0) return cudaSuccess;
     return d == 128 ? launch_persist<128>(p, nsm, stream) : launch_persist<64>(p, nsm, stream);
 }
+
+#ifdef GBATTN_DEBUG_CHECKS
+cudaError_t debug_skip_fill_persist(int fill) {
+    return cudaMemcpyToSymbol(g_skip_k_fill, &fill, sizeof(int));
+}
+#endif
 
 }  // namespace gbattn

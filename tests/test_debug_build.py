@@ -102,3 +102,99 @@ def test_debug_build_runs_every_path_with_the_error_word_clear():
                        timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
     assert "debug build ok" in r.stdout
+
+
+# ---------------------------------------------------------------------------------------
+# the debug build's test hook: a wait that runs out inside a real attention kernel
+# ---------------------------------------------------------------------------------------
+
+def test_debug_hook_is_in_the_debug_library_only():
+    dbg = ctypes.CDLL(build.build(debug=True))
+    assert hasattr(dbg, "attn_debug_skip_fill")
+    rel = ctypes.CDLL(build.build())
+    assert not hasattr(rel, "attn_debug_skip_fill")
+
+
+def test_debug_header_compiles_as_c99(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "gbattn_debug.h"\nint main(void) { return GBATTN_DEBUG_MULTITOKEN_DECODE - 1; }\n')
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-I",
+                        os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+TIMEOUT_SCRIPT = textwrap.dedent(r"""
+    import ctypes, sys, time
+    sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+    import numpy as np, torch
+    import attn_workloads as wl, oracle
+    import streaming_attention_flashattention_gb300 as gb
+    from streaming_attention_flashattention_gb300 import build
+    from _parity import compare
+    lib = gb.load_library(build.build(debug=True))
+    skip = lib.attn_debug_skip_fill
+    skip.argtypes = [ctypes.c_int, ctypes.c_int]
+    skip.restype = ctypes.c_int
+    PERSISTENT_PREFILL, MULTITOKEN_DECODE = 0, 1
+    assert skip(7, 0) == gb.GBATTN_ERR_INVALID_ARG and skip(0, -2) == gb.GBATTN_ERR_INVALID_ARG
+
+    def prefill():
+        w = wl.Workload("dbg-to", "prefill", B=1, Hq=8, Hkv=2, d=128, dtype="bf16", Sq=1024,
+                        Skv=1024, causal=True, seed=21)
+        assert gb.attn_prefill_plan(1, 8, 2, 1024, 1024, True, 152)["mode"] == "kv_split"
+        q, k, v = wl.prefill_inputs(w)
+        o, lse = gb.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=w.scale)
+        return w, (q, k, v), o, lse
+
+    def decode():
+        w = wl.Workload("dbg-to-mt", "decode", B=2, Hq=16, Hkv=2, d=128, dtype="bf16", Skv=3000,
+                        num_splits=2, len_lo=2500, len_hi=3000, Sq=4, seed=22)
+        assert gb.attn_decode_plan(2, 16, 2, 4, 3000, 128, 2, 152)["kernel"] == "tcgen05"
+        q, kc, vc, kl = wl.multitoken_inputs(w)
+        o, lse = gb.attn_decode_multitoken(q.cuda(), kc.cuda(), vc.cuda(), kl.cuda(),
+                                           num_splits=2, scale=w.scale)
+        return w, (q, kc, vc, kl), o, lse
+
+    for kernel, call in ((PERSISTENT_PREFILL, prefill), (MULTITOKEN_DECODE, decode)):
+        # the wait for the unissued K tile runs out; every role of every CTA gives up and the
+        # kernel returns: the host sees GBATTN_ERR_TIMEOUT with the code of a wait
+        assert skip(kernel, 3) == 0
+        t0 = time.time()
+        call()
+        st, word = gb.attn_last_device_error()
+        elapsed = time.time() - t0
+        assert st == gb.GBATTN_ERR_TIMEOUT and word in (1, 2, 3, 4, 7), (kernel, st, word)
+        assert elapsed < 60, elapsed
+        assert gb.attn_last_device_error() == (0, 0)          # read and cleared
+        # the context is still usable: the same call without the hook matches the oracle
+        assert skip(kernel, -1) == 0
+        w, ins, o, lse = call()
+        torch.cuda.synchronize()
+        if kernel == PERSISTENT_PREFILL:
+            q, k, v = ins
+            o_ref, l_ref = oracle.attention(wl.to_oracle(q), wl.to_oracle(k), wl.to_oracle(v),
+                                            w.scale, True)
+        else:
+            q, kc, vc, kl = ins
+            o_ref, l_ref = oracle.attention(wl.to_oracle(q), wl.to_oracle(kc), wl.to_oracle(vc),
+                                            w.scale, True, kv_len=kl.numpy())
+        compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "bf16", f"after {{kernel}}")
+        assert gb.attn_last_device_error() == (0, 0)
+        print(f"kernel {{kernel}}: gave up with word {{word}} after {{elapsed:.2f}} s, then ran clean")
+    print("timeouts ok")
+""")
+
+
+@pytest.mark.gpu
+def test_wait_runs_out_inside_real_kernels_and_every_role_exits():
+    # A K tile copy that is never issued (debug-build hook) makes the wait for it run out
+    # inside the persistent prefill kernel and the tcgen05 decode kernel: the producers drain
+    # their copies, the MMA issuer drains its products, TMEM is released, the error word
+    # carries the wait's code, and the next call on the same context is correct.  No fault,
+    # no trap: the copy is simply not started.
+    script = TIMEOUT_SCRIPT.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
+    r = subprocess.run([sys.executable, "-c", script], capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
+    assert "timeouts ok" in r.stdout
+    print(r.stdout.strip())
