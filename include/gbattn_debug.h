@@ -19,12 +19,15 @@ extern "C" {
 /* kernels the hook can target */
 #define GBATTN_DEBUG_PERSISTENT_PREFILL 0  /* persistent KV-split prefill (small attn_fwd calls) */
 #define GBATTN_DEBUG_MULTITOKEN_DECODE 1   /* tcgen05 multi-token decode (16+ rows per KV head) */
+#define GBATTN_DEBUG_PAIR_PREFILL 2        /* prefill on pairs of Q tiles (and its tail launch) */
+#define GBATTN_DEBUG_SPLIT_DECODE 3        /* warp-level split decode (a stage: 64 keys of K, V) */
 
 /*
  * attn_debug_skip_fill -- from the next launch of `kernel` on the current device, CTA 0 does
- * not issue its K tile copy number `fill` (0-based, counted over the CTA's copies), until
- * called again with fill = -1.  The launch then ends after the bounded wait for that tile
- * has run out (about 2e9 cycles, one second), and attn_last_device_error() reports
+ * not issue its K tile copy number `fill` (0-based, counted over the CTA's copies; for the
+ * split decode kernel a copy is a ring stage of K and V), until called again with fill = -1.
+ * The launch then ends after the bounded wait for that tile has run out (about 2e9 cycles,
+ * one second), and attn_last_device_error() reports
  * GBATTN_ERR_TIMEOUT with the code of the wait that gave up first (1 producer, 2 consumer,
  * 3 tensor-core issuer, 4 softmax, 7 a combine block).  The outputs of that call are
  * undefined; later calls are not affected once the hook is cleared.

@@ -66,6 +66,13 @@ struct Cfg {
 };
 constexpr int kHeads = 8;                  // query heads per work item (MMA N)
 constexpr int kPubSlots = 4;               // publisher ring entries (finished partials)
+#ifdef GBATTN_DEBUG_CHECKS
+// Test hook of the debug build: CTA 0 of the grid does not issue the stage fill (K, V and Q of 64 keys) with this index
+// (counted over the CTA's fills; -1: none).  The fill's barrier then never completes, the wait
+// for it runs out after its time limit and records its code in the error word, and every role
+// of every CTA leaves through its give-up exit.  Set by attn_debug_skip_fill.
+__device__ int g_skip_k_fill = -1;
+#endif
 
 // Single-token instances that count their partials (for the combine's per-group wait) have a
 // publisher warp after the producer: the consumers hand it each finished partial and it
@@ -351,6 +358,9 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;   // per-stage bits for the exit drain
             bool ok = true;
+#ifdef GBATTN_DEBUG_CHECKS
+            int nfill = 0;                          // stage fills so far (the test hook)
+#endif
             // Items are pulled from a device counter, so a CTA that finishes early takes
             // more (a static round-robin measured slower even for equal-size splits).
             for (int item = atomicAdd(p.counter, 1); ok && item < p.n_items;
@@ -436,25 +446,32 @@ decode_split_kernel(const __grid_constant__ DecodeParams p) {
                     // NCI chunks of it)
                     const bool with_q = tile == 0 || NCI > 1;
                     const uint32_t bytes = L::kKBytes + L::kVBytes + (with_q ? L::kQBytes : 0);
-                    mbar_arrive_expect_tx(&full[stage], bytes);
-                    #pragma unroll
-                    for (int bx = 0; bx < L::kBoxes; ++bx) {
-                        tma_load_3d(st + bx * (kKeysPerStage * 128), &p.tmap_k, bx * 64, y, zkv,
-                                    &full[stage]);
-                        tma_load_3d(st + L::kKBytes + bx * (kKeysPerStage * 128), &p.tmap_v,
-                                    bx * 64, y, zkv, &full[stage]);
-                    }
-                    if (with_q) {
+#ifdef GBATTN_DEBUG_CHECKS
+                    if (blockIdx.x == 0 && nfill++ == g_skip_k_fill) {
+                        // left out: the stage's barrier never completes (and is not drained)
+                    } else
+#endif
+                    {
+                        mbar_arrive_expect_tx(&full[stage], bytes);
                         #pragma unroll
-                        for (int cq = 0; cq < NCI; ++cq)
+                        for (int bx = 0; bx < L::kBoxes; ++bx) {
+                            tma_load_3d(st + bx * (kKeysPerStage * 128), &p.tmap_k, bx * 64, y, zkv,
+                                        &full[stage]);
+                            tma_load_3d(st + L::kKBytes + bx * (kKeysPerStage * 128), &p.tmap_v,
+                                        bx * 64, y, zkv, &full[stage]);
+                        }
+                        if (with_q) {
                             #pragma unroll
-                            for (int bx = 0; bx < L::kBoxes; ++bx)
-                                tma_load_3d(st + L::kKBytes + L::kVBytes + bx * (kHeads * NCI * 128) +
-                                                cq * (kHeads * 128),
-                                            &p.tmap_q, bx * 64, (int)row0 + cq * kHeads, 0, &full[stage]);
+                            for (int cq = 0; cq < NCI; ++cq)
+                                #pragma unroll
+                                for (int bx = 0; bx < L::kBoxes; ++bx)
+                                    tma_load_3d(st + L::kKBytes + L::kVBytes + bx * (kHeads * NCI * 128) +
+                                                    cq * (kHeads * 128),
+                                                &p.tmap_q, bx * 64, (int)row0 + cq * kHeads, 0, &full[stage]);
+                        }
+                        filled |= 1u << stage;
+                        fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     }
-                    filled |= 1u << stage;
-                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -1108,5 +1125,11 @@ cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
         return p.nci == 2 ? launch_pair<128, 2>(p, num_sms, stream) : launch_pair<128, 1>(p, num_sms, stream);
     return p.nci == 2 ? launch_pair<64, 2>(p, num_sms, stream) : launch_pair<64, 1>(p, num_sms, stream);
 }
+
+#ifdef GBATTN_DEBUG_CHECKS
+cudaError_t debug_skip_fill_split(int fill) {
+    return cudaMemcpyToSymbol(g_skip_k_fill, &fill, sizeof(int));
+}
+#endif
 
 }  // namespace gbattn

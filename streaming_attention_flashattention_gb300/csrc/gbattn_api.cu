@@ -916,7 +916,9 @@ int attn_prefill_plan(int B, int Hq, int Hkv, int Sq, int Skv, int causal, int n
 #ifdef GBATTN_DEBUG_CHECKS
 }  // extern "C"
 namespace gbattn {
+cudaError_t debug_skip_fill_pairs(int fill);
 cudaError_t debug_skip_fill_persist(int fill);
+cudaError_t debug_skip_fill_split(int fill);
 cudaError_t debug_skip_fill_multitoken(int fill);
 }  // namespace gbattn
 extern "C" {
@@ -928,6 +930,10 @@ int attn_debug_skip_fill(int kernel, int fill) {
         e = debug_skip_fill_persist(fill);
     else if (kernel == GBATTN_DEBUG_MULTITOKEN_DECODE)
         e = debug_skip_fill_multitoken(fill);
+    else if (kernel == GBATTN_DEBUG_PAIR_PREFILL)
+        e = debug_skip_fill_pairs(fill);
+    else if (kernel == GBATTN_DEBUG_SPLIT_DECODE)
+        e = debug_skip_fill_split(fill);
     else
         return GBATTN_ERR_INVALID_ARG;
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;

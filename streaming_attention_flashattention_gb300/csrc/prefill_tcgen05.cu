@@ -47,6 +47,13 @@ constexpr int kThreads = 12 * 32;
 constexpr int kSoftmaxWarp0 = 4;          // warps 4..7 -> tile 0, 8..11 -> tile 1
 constexpr float kRescaleThreshold = 8.0f; // log2 units: rescale O only if max grows > 2^8
 static_assert(kBlockN == 128, "the softmax row reductions assume 128 columns");
+#ifdef GBATTN_DEBUG_CHECKS
+// Test hook of the debug build: CTA 0 of the grid does not issue the K fill with this index
+// (counted over the CTA's fills; -1: none).  The fill's barrier then never completes, the wait
+// for it runs out after its time limit and records its code in the error word, and every role
+// of every CTA leaves through its give-up exit.  Set by attn_debug_skip_fill.
+__device__ int g_skip_k_fill = -1;
+#endif
 
 template <int D>
 struct PLayout {
@@ -209,6 +216,9 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
             const int zkv = b * p.Hkv + kvh;
             uint32_t nf = 0, nfv = 0;
             bool ok = true;
+#ifdef GBATTN_DEBUG_CHECKS
+            uint32_t skipped = 0xffffffffu;   // the fill the test hook left out
+#endif
             for (int j = 0; j < n_kv_max && ok; ++j) {
                 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
@@ -217,11 +227,18 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
                     const int tile = kSplit ? td[t].kv0 + j : j;
                     const uint32_t ks = nf % KS, kph = (nf / KS) & 1;
                     if (!mbar_wait(&k_empty[ks], kph ^ 1u, kErrWaitProducer, p.err)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&k_full[ks], L::kTileBytes);
-                    #pragma unroll
-                    for (int bx = 0; bx < L::kBoxes; ++bx)
-                        tma_load_3d(k_slot(nf) + bx * L::kBoxBytes, &p.tmap_k, bx * 64,
-                                    tile * kBlockN, zkv, &k_full[ks]);
+#ifdef GBATTN_DEBUG_CHECKS
+                    if (blockIdx.x == 0 && (int)nf == g_skip_k_fill) {
+                        skipped = nf;
+                    } else
+#endif
+                    {
+                        mbar_arrive_expect_tx(&k_full[ks], L::kTileBytes);
+                        #pragma unroll
+                        for (int bx = 0; bx < L::kBoxes; ++bx)
+                            tma_load_3d(k_slot(nf) + bx * L::kBoxBytes, &p.tmap_k, bx * 64,
+                                        tile * kBlockN, zkv, &k_full[ks]);
+                    }
                     ++nf;
                     const uint32_t vs = nfv & 1, vph = (nfv >> 1) & 1;
                     if (!mbar_wait(&v_empty[vs], vph ^ 1u, kErrWaitProducer, p.err)) { ok = false; break; }
@@ -235,8 +252,12 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
             }
             // drain: the last fills of each slot must land before the CTA can exit
             mbar_wait_drain(q_full, 0, p.err);
-            for (uint32_t f = nf >= (uint32_t)KS ? nf - KS : 0; f < nf; ++f)
+            for (uint32_t f = nf >= (uint32_t)KS ? nf - KS : 0; f < nf; ++f) {
+#ifdef GBATTN_DEBUG_CHECKS
+                if (f == skipped) continue;
+#endif
                 mbar_wait_drain(&k_full[f % KS], (f / KS) & 1, p.err);
+            }
             for (uint32_t f = nfv >= 2 ? nfv - 2 : 0; f < nfv; ++f)
                 mbar_wait_drain(&v_full[f & 1], (f >> 1) & 1, p.err);
         }
@@ -607,5 +628,11 @@ cudaError_t launch_attn_fwd_bf16(const PrefillParams& p, int d, cudaStream_t str
     if (p.kv_split) return cudaErrorInvalidValue;   // small calls run prefill_persist.cu
     return d == 128 ? launch_pairs<128>(p, stream) : launch_pairs<64>(p, stream);
 }
+
+#ifdef GBATTN_DEBUG_CHECKS
+cudaError_t debug_skip_fill_pairs(int fill) {
+    return cudaMemcpyToSymbol(g_skip_k_fill, &fill, sizeof(int));
+}
+#endif
 
 }  // namespace gbattn

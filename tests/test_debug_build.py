@@ -135,16 +135,28 @@ TIMEOUT_SCRIPT = textwrap.dedent(r"""
     skip = lib.attn_debug_skip_fill
     skip.argtypes = [ctypes.c_int, ctypes.c_int]
     skip.restype = ctypes.c_int
-    PERSISTENT_PREFILL, MULTITOKEN_DECODE = 0, 1
+    PERSISTENT_PREFILL, MULTITOKEN_DECODE, PAIR_PREFILL, SPLIT_DECODE = 0, 1, 2, 3
     assert skip(7, 0) == gb.GBATTN_ERR_INVALID_ARG and skip(0, -2) == gb.GBATTN_ERR_INVALID_ARG
 
-    def prefill():
-        w = wl.Workload("dbg-to", "prefill", B=1, Hq=8, Hkv=2, d=128, dtype="bf16", Sq=1024,
-                        Skv=1024, causal=True, seed=21)
-        assert gb.attn_prefill_plan(1, 8, 2, 1024, 1024, True, 152)["mode"] == "kv_split"
+    def prefill(Hq=8, Hkv=2, S=1024, mode="kv_split"):
+        w = wl.Workload("dbg-to", "prefill", B=1, Hq=Hq, Hkv=Hkv, d=128, dtype="bf16", Sq=S,
+                        Skv=S, causal=True, seed=21)
+        assert gb.attn_prefill_plan(1, Hq, Hkv, S, S, True, 152)["mode"] == mode
         q, k, v = wl.prefill_inputs(w)
         o, lse = gb.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=w.scale)
         return w, (q, k, v), o, lse
+
+    def pairs():
+        return prefill(Hq=32, Hkv=8, S=2560, mode="pairs")
+
+    def split_decode():
+        w = wl.Workload("dbg-to-dec", "decode", B=4, Hq=64, Hkv=8, d=128, dtype="bf16", Skv=8192,
+                        num_splits=16, len_lo=6000, len_hi=8192, seed=23)
+        assert gb.attn_decode_plan(4, 64, 8, 1, 8192, 128, 16, 152)["merge"] == "combine_per_group"
+        q, kc, vc, kl = wl.decode_inputs(w)
+        o, lse = gb.attn_decode_splitkv(q.cuda(), kc.cuda(), vc.cuda(), kl.cuda(), num_splits=16,
+                                        scale=w.scale)
+        return w, (q, kc, vc, kl), o, lse.unsqueeze(-1)
 
     def decode():
         w = wl.Workload("dbg-to-mt", "decode", B=2, Hq=16, Hkv=2, d=128, dtype="bf16", Skv=3000,
@@ -155,7 +167,8 @@ TIMEOUT_SCRIPT = textwrap.dedent(r"""
                                            num_splits=2, scale=w.scale)
         return w, (q, kc, vc, kl), o, lse
 
-    for kernel, call in ((PERSISTENT_PREFILL, prefill), (MULTITOKEN_DECODE, decode)):
+    for kernel, call in ((PERSISTENT_PREFILL, prefill), (MULTITOKEN_DECODE, decode),
+                         (PAIR_PREFILL, pairs), (SPLIT_DECODE, split_decode)):
         # the wait for the unissued K tile runs out; every role of every CTA gives up and the
         # kernel returns: the host sees GBATTN_ERR_TIMEOUT with the code of a wait
         assert skip(kernel, 3) == 0
@@ -170,15 +183,18 @@ TIMEOUT_SCRIPT = textwrap.dedent(r"""
         assert skip(kernel, -1) == 0
         w, ins, o, lse = call()
         torch.cuda.synchronize()
-        if kernel == PERSISTENT_PREFILL:
+        if kernel in (PERSISTENT_PREFILL, PAIR_PREFILL):
             q, k, v = ins
+            rows = np.random.default_rng(kernel).integers(0, q.shape[1] * q.shape[2], 2000)
             o_ref, l_ref = oracle.attention(wl.to_oracle(q), wl.to_oracle(k), wl.to_oracle(v),
-                                            w.scale, True)
+                                            w.scale, True, rows=rows)
+            o, lse = o.reshape(-1, 128)[rows], lse.reshape(-1)[rows]
         else:
             q, kc, vc, kl = ins
             o_ref, l_ref = oracle.attention(wl.to_oracle(q), wl.to_oracle(kc), wl.to_oracle(vc),
-                                            w.scale, True, kv_len=kl.numpy())
-        compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "bf16", f"after {{kernel}}")
+                                            w.scale, kernel == MULTITOKEN_DECODE, kv_len=kl.numpy())
+        compare(o.float().cpu().numpy(), lse.cpu().numpy().reshape(l_ref.shape), o_ref, l_ref,
+                "bf16", f"after {{kernel}}")
         assert gb.attn_last_device_error() == (0, 0)
         print(f"kernel {{kernel}}: gave up with word {{word}} after {{elapsed:.2f}} s, then ran clean")
     print("timeouts ok")
@@ -188,7 +204,8 @@ TIMEOUT_SCRIPT = textwrap.dedent(r"""
 @pytest.mark.gpu
 def test_wait_runs_out_inside_real_kernels_and_every_role_exits():
     # A K tile copy that is never issued (debug-build hook) makes the wait for it run out
-    # inside the persistent prefill kernel and the tcgen05 decode kernel: the producers drain
+    # inside each attention kernel (pair and persistent prefill, warp-level and tcgen05
+    # decode): the producers drain
     # their copies, the MMA issuer drains its products, TMEM is released, the error word
     # carries the wait's code, and the next call on the same context is correct.  No fault,
     # no trap: the copy is simply not started.
