@@ -191,3 +191,16 @@ def test_plan_agrees_with_workspace_size_and_invariants():
             assert p["kernel"] == "tcgen05"
         if G * Tq <= 8:
             assert p["kernel"] == "warp"
+
+
+def test_decode_work_items_do_not_grow_with_the_group_size():
+    # GQA reuse ("ADR-0060: AHBM GQA Fused Attention Kernel (Llama3-70B)", §11): a work item
+    # reads its split's K and V once for all G query heads of the KV head (all G * T_q rows on
+    # the tcgen05 kernel), so the items -- and the K/V bytes read -- are the same for every G
+    base = dec(4, 8, 8, 1, 32768, 16)["items"]
+    for G in (2, 4, 8):
+        assert dec(4, 8 * G, 8, 1, 32768, 16)["items"] == base
+    tc = dec(4, 32, 8, 4, 32768, 16)
+    assert tc["kernel"] == "tcgen05"
+    for G in (8, 16):
+        assert dec(4, 8 * G, 8, 4, 32768, 16)["items"] == tc["items"]
