@@ -57,12 +57,15 @@ constexpr int kKeysPerStage = 64;
 // items carry NCI times the math per byte of K/V: 8 consumer warps (4 key slices x 2
 // halves of the item's chunks) so that each warp holds fewer chunks' state and more warps
 // hide the MMA and shuffle latencies; the ring drops to 4 stages to make room for their
-// merge buffers.
-template <int NCI>
+// merge buffers.  Single-launch calls with more items than SMs run two CTAs per SM with
+// 2-stage rings (kTwo): while one CTA folds a finished group's partials, the other keeps
+// streaming.
+template <int NCI, bool kTwo = false>
 struct Cfg {
     static constexpr int kCW = NCI == 1 ? 4 : 8;           // consumer warps
     static constexpr int kThreads = (kCW + 1) * 32;
-    static constexpr int kStages = NCI == 1 ? 5 : 4;
+    static constexpr int kStages = kTwo ? 2 : (NCI == 1 ? 5 : 4);
+    static constexpr int kPerSM = kTwo ? 2 : 1;             // resident CTAs per SM
 };
 constexpr int kHeads = 8;                  // query heads per work item (MMA N)
 constexpr int kPubSlots = 4;               // publisher ring entries (finished partials)
@@ -89,9 +92,9 @@ struct StageInfo {
     int direct;                   // the item is the row's only partial: write O and LSE
 };
 
-template <int D, int NCI>
+template <int D, int NCI, bool kTwo = false>
 struct Layout {
-    static constexpr int kStages = Cfg<NCI>::kStages;
+    static constexpr int kStages = Cfg<NCI, kTwo>::kStages;
     static constexpr int kConsumerWarps = Cfg<NCI>::kCW;
     static constexpr int kBoxes = D / 64;                       // 64-element swizzle boxes
     static constexpr int kKBytes = kKeysPerStage * D * 2;       // K tile
@@ -301,13 +304,14 @@ __device__ __forceinline__ int row_partials(const DecodeParams& p, int b) {
     return nonempty_splits(len, splits_for(len, p.fixed_splits, p.auto_floor)) * p.pieces;
 }
 
-template <int D, int NCI, bool kFused>
-__global__ void __launch_bounds__(split_threads<NCI, kFused>(), 1)
+template <int D, int NCI, bool kFused, bool kTwo = false>
+__global__ void __launch_bounds__(split_threads<NCI, kFused>(), (Cfg<NCI, kTwo>::kPerSM))
 decode_split_kernel(const __grid_constant__ DecodeParams p) {
     static_assert(!kFused || NCI == 1, "single-launch mode is for single-token items");
-    using L = Layout<D, NCI>;
+    static_assert(!kTwo || kFused, "two CTAs per SM: single-launch calls only");
+    using L = Layout<D, NCI, kTwo>;
     constexpr int kConsumerWarps = Cfg<NCI>::kCW;
-    constexpr int kStages = Cfg<NCI>::kStages;
+    constexpr int kStages = Cfg<NCI, kTwo>::kStages;
     constexpr int W = kConsumerWarps / NCI;       // consumer warps per row chunk
     constexpr int kKeysPerWarp = kKeysPerStage / W;
     extern __shared__ uint8_t smem_raw[];
@@ -1061,16 +1065,17 @@ size_t decode_workspace_bytes(int B_rows, int Hq, int kv_groups, int n_hg, int d
 
 namespace {
 
-template <int D, int NCI, bool kFused = false>
+template <int D, int NCI, bool kFused = false, bool kTwo = false>
 cudaError_t launch_pair(const DecodeParams& p, int num_sms, cudaStream_t stream) {
-    constexpr int smem = Layout<D, NCI>::kAlloc;
-    static_assert(smem <= 227 * 1024, "shared memory budget");
-    const int grid = p.n_items < num_sms ? p.n_items : num_sms;
+    constexpr int smem = Layout<D, NCI, kTwo>::kAlloc;
+    static_assert(smem * Cfg<NCI, kTwo>::kPerSM <= 227 * 1024, "shared memory budget");
+    const int slots = num_sms * Cfg<NCI, kTwo>::kPerSM;
+    const int grid = p.n_items < slots ? p.n_items : slots;
     if (grid <= 0) return cudaSuccess;
-    cudaError_t err = cudaFuncSetAttribute(decode_split_kernel<D, NCI, kFused>,
+    cudaError_t err = cudaFuncSetAttribute(decode_split_kernel<D, NCI, kFused, kTwo>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    decode_split_kernel<D, NCI, kFused><<<grid, split_threads<NCI, kFused>(), smem, stream>>>(p);
+    decode_split_kernel<D, NCI, kFused, kTwo><<<grid, split_threads<NCI, kFused>(), smem, stream>>>(p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     if constexpr (kFused) return cudaSuccess;      // merged in the split kernel
@@ -1116,6 +1121,12 @@ cudaError_t launch_decode_splitkv(const DecodeParams& p, int d, int num_sms,
     cudaError_t err = cudaMemsetAsync(p.counter, 0, decode_counter_bytes(p.B, p.Hkv, p.n_hg), stream);
     if (err != cudaSuccess) return err;
     if (p.fused) {
+        // more items than SMs: two CTAs per SM (one folds a group while the other streams);
+        // one wave: one CTA per SM with the deep ring (measured: B1 with 131072 keys 93.9 ->
+        // 88.9 us with two per SM, B1 with 65536 keys in one wave 50.4 -> 58.2 us)
+        if (p.n_items > num_sms)
+            return d == 128 ? launch_pair<128, 1, true, true>(p, num_sms, stream)
+                            : launch_pair<64, 1, true, true>(p, num_sms, stream);
         return d == 128 ? launch_pair<128, 1, true>(p, num_sms, stream)
                         : launch_pair<64, 1, true>(p, num_sms, stream);
     }

@@ -57,6 +57,20 @@ def test_decode_shapes(B, Hq, Hkv, Lmax, d, ns, lens):
     run_decode(small(B, Hq, Hkv, Lmax, d, ns, Lmax, Lmax), lens=lens)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,Lmax,d,ns,lens", [
+    (1, 64, 8, 131072, 128, 0, [131072]),             # 8 groups x 32 splits = 256 items
+    (2, 64, 8, 65536, 128, 0, [65536, 40000]),        # 16 groups x 16 splits, ragged
+    (2, 16, 2, 70000, 64, 64, [70000, 33333]),        # d = 64: 4 groups x 64 splits
+])
+def test_single_launch_two_ctas_per_sm(B, Hq, Hkv, Lmax, d, ns, lens):
+    # single-launch merge with more work items than SMs: two CTAs per SM, 2-stage rings
+    import torch
+    p = gb.attn_decode_plan(B, Hq, Hkv, 1, Lmax, d, ns,
+                            torch.cuda.get_device_properties(0).multi_processor_count)
+    assert p["merge"] == "single_launch" and p["items"] > 152
+    run_decode(small(B, Hq, Hkv, Lmax, d, ns, Lmax, Lmax, seed=31), lens=lens)
+
+
 @pytest.mark.parametrize("ns", [1, 2, 7, 16, 64, 0])
 def test_decode_split_count_invariance(ns):
     run_decode(small(2, 64, 8, 6000, 128, ns, 5000, 6000, seed=21))

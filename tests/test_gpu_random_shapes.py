@@ -82,20 +82,23 @@ def prefill_shapes(nsm: int):
 
 
 DECODE_DRAWS = 6
-DECODE_KINDS = ("single_launch", "combine_per_group", "combine_per_group+pieces",
-                "mt:single_launch", "mt:combine", "mt:tcgen05+combine_per_group",
-                "mt:tcgen05+combine")
+DECODE_KINDS = ("single_launch", "single_launch+two_per_sm", "combine_per_group",
+                "combine_per_group+pieces", "mt:single_launch", "mt:combine",
+                "mt:tcgen05+combine_per_group", "mt:tcgen05+combine")
 
 
-def decode_kind(Tq: int, plan: dict) -> str:
-    """Single-token calls merge in the split kernel (single launch) or per group (with or
-    without pieces); multi-token calls (mt:) run the warp kernel with either merge, or the
-    tcgen05 kernel with the per-group combine (one 128-row tile per KV head) or the combine
-    that waits for the grid (more rows)."""
+def decode_kind(Tq: int, plan: dict, nsm: int) -> str:
+    """Single-token calls merge in the split kernel (single launch: one CTA per SM in one
+    wave, two per SM with more items than SMs) or per group (with or without pieces);
+    multi-token calls (mt:) run the warp kernel with either merge, or the tcgen05 kernel with
+    the per-group combine (one 128-row tile per KV head) or the combine that waits for the
+    grid (more rows)."""
     if plan["kernel"] == "tcgen05":
         k = "tcgen05+" + plan["merge"]
     else:
         k = plan["merge"] + ("+pieces" if plan["pieces"] > 1 else "")
+        if Tq == 1 and plan["merge"] == "single_launch" and plan["items"] > nsm:
+            k += "+two_per_sm"
     return ("mt:" + k) if Tq > 1 else k
 
 
@@ -121,7 +124,7 @@ def decode_shapes(nsm: int):
         ns = int(rng.choice([0, 0, 1, 2, 5, 16, 37]))
         Lmax = max(max(lens), Tq, 1) + int(rng.integers(0, 200))
         Hq = Hkv * G
-        k = decode_kind(Tq, gb.attn_decode_plan(B, Hq, Hkv, Tq, Lmax, d, ns, nsm))
+        k = decode_kind(Tq, gb.attn_decode_plan(B, Hq, Hkv, Tq, Lmax, d, ns, nsm), nsm)
         if counts.get(k, DECODE_DRAWS) >= DECODE_DRAWS:
             continue
         counts[k] += 1
