@@ -13,10 +13,12 @@ ring_prefill  -- section 5.5, prefill with the sequence split over the ranks (Ri
     ends with its own heads' final rows; there is no reduction across ranks.
 
 decode_reduce -- section 4, decode with the KV cache split along the sequence (KV-parallel):
-    every rank holds the same queries (T_q = 1) and a contiguous block of each sequence's
-    keys, sweeps it with the split-KV decode kernel into a partial (O_r, LSE_r), and the
-    partials are combined by reduce-to-root over a static binomial tree of depth
-    ceil(log2 P): a node merges its children's partials, in a fixed order, as they arrive
+    every rank holds the same queries (T_q = 1) and a share of each sequence's keys -- a
+    contiguous block (section 2.1), or every P-th token round robin (the section's
+    alternative; decode attends to every key, so any disjoint split of the positions gives
+    the same result) -- and sweeps it with the split-KV decode kernel into a partial
+    (O_r, LSE_r); the partials are combined by reduce-to-root over a static binomial tree
+    of depth ceil(log2 P): a node merges its children's partials, in a fixed order, as they arrive
     and sends the result to its parent once its own sweep and its children are done; only
     the root holds the answer (section 4: attention is needed in one place, so not an
     all-reduce).  The merge is section 4's log-sum-exp merge, attn_merge.
@@ -211,9 +213,10 @@ def decode_reduce(q, k_shard, v_shard, kv_lens, *, root: int = 0, scale: float |
     """KV-parallel decode with reduce-to-root ("ADR-0060" section 4); call on every rank.
 
     q        [B, Hq, d]          the same decode queries on every rank
-    k_shard  [B, Hkv, Lmax, d]   this rank's contiguous block of each sequence's keys
-    v_shard                      (cache layout of attn_decode_splitkv)
-    kv_lens  [B] int32           valid keys of the block per sequence (0 allowed)
+    k_shard  [B, Hkv, Lmax, d]   this rank's keys of each sequence (a contiguous block, or
+    v_shard                      round-robin tokens: any disjoint split of the positions)
+                                 in the cache layout of attn_decode_splitkv
+    kv_lens  [B] int32           valid keys of the shard per sequence (0 allowed)
     Returns (O [B, Hq, d] bf16, LSE [B, Hq]) on `root`, (None, None) on the other ranks.
     """
     backend = backend or CudaBackend()

@@ -242,8 +242,11 @@ def test_ring_prefill_threads_equal_single_device(world, B, Hq, Hkv, L, q_rows, 
                 l_ref[:, r * hr:(r + 1) * hr], "bf16", f"ring P{world} rank {r}")
 
 
+@pytest.mark.parametrize("placement", ["contiguous", "round_robin"])
 @pytest.mark.parametrize("world,root", [(3, 0), (4, 2), (5, 1)])
-def test_decode_reduce_threads_equal_single_device(world, root):
+def test_decode_reduce_threads_equal_single_device(world, root, placement):
+    # the cache split along the sequence in contiguous blocks ("ADR-0060" section 2.1), or
+    # token by token round robin (position t on rank t mod P, the section's alternative)
     B, Hq, Hkv, d = 4, 64, 8, 128
     lens = [9000, 1, 0, 6000]
     Lmax = 9000
@@ -253,14 +256,20 @@ def test_decode_reduce_threads_equal_single_device(world, root):
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
 
     def rank_fn(r, comm):
-        lo, hi = r * c, min((r + 1) * c, Lmax)
         ks = torch.zeros((B, Hkv, c, d), dtype=torch.bfloat16, device="cuda")
         vs = torch.zeros_like(ks)
-        if hi > lo:
-            ks[:, :, :hi - lo] = kd[:, :, lo:hi]
-            vs[:, :, :hi - lo] = vd[:, :, lo:hi]
-        lens_r = torch.tensor([max(0, min(n - lo, c)) for n in lens], dtype=torch.int32,
-                              device="cuda")
+        if placement == "contiguous":
+            lo, hi = r * c, min((r + 1) * c, Lmax)
+            if hi > lo:
+                ks[:, :, :hi - lo] = kd[:, :, lo:hi]
+                vs[:, :, :hi - lo] = vd[:, :, lo:hi]
+            held = [max(0, min(n - lo, c)) for n in lens]
+        else:
+            mine = kd[:, :, r::world]
+            ks[:, :, :mine.shape[2]] = mine
+            vs[:, :, :mine.shape[2]] = vd[:, :, r::world]
+            held = [max(0, -(-(n - r) // world)) for n in lens]   # positions r, r + P, ... < n
+        lens_r = torch.tensor(held, dtype=torch.int32, device="cuda")
         return sp.decode_reduce(qd, ks, vs, lens_r, root=root, comm=comm)
 
     res = run_ranks(world, rank_fn)
@@ -273,7 +282,7 @@ def test_decode_reduce_threads_equal_single_device(world, root):
             continue
         assert o.dtype == torch.bfloat16
         compare(o.float().cpu().numpy(), l.cpu().numpy(), o_ref[:, :, 0], l_ref[:, :, 0],
-                "bf16", f"decode P{world} root {root}")
+                "bf16", f"decode P{world} root {root} {placement}")
 
 
 @pytest.mark.parametrize("Sq", [1, 5, 128, 129])

@@ -187,6 +187,16 @@ def _worker(rank, world, port, out):
             o, l = spw.decode_reduce(q, ks, vs, lens_r, root=root, scale=0.3,
                                      backend=OracleBackend())
             res[("dec", ci)] = None if o is None else (o.numpy(), l.numpy())
+            # round-robin placement: position t on rank t mod P
+            ks = torch.zeros((B, Hkv, c, d))
+            vs = torch.zeros((B, Hkv, c, d))
+            mine = k[:, :, rank::world]
+            ks[:, :, :mine.shape[2]] = mine
+            vs[:, :, :mine.shape[2]] = v[:, :, rank::world]
+            lens_r = torch.tensor([max(0, -(-(n - rank) // world)) for n in lens], dtype=torch.int32)
+            o, l = spw.decode_reduce(q, ks, vs, lens_r, root=root, scale=0.3,
+                                     backend=OracleBackend())
+            res[("dec_rr", ci)] = None if o is None else (o.numpy(), l.numpy())
         out[rank] = res
     finally:
         dist.destroy_process_group()
@@ -234,13 +244,14 @@ def test_schedules_over_gloo_equal_single_device(world):
         v = _rnd((B, Hkv, Lmax, d), 12)
         o_ref, l_ref = oracle.attention(q.numpy()[:, :, None, :], k.numpy(), v.numpy(), 0.3,
                                         False, kv_len=np.array(lens, np.int32))
-        for r in range(world):
-            got = out[r][("dec", ci)]
-            if r != root:
-                assert got is None
-                continue
-            o, l = got
-            np.testing.assert_allclose(o, o_ref[:, :, 0], rtol=0, atol=1e-6)
-            fin = np.isfinite(l_ref[:, :, 0])
-            assert np.array_equal(fin, np.isfinite(l))
-            np.testing.assert_allclose(l[fin], l_ref[:, :, 0][fin], rtol=0, atol=1e-6)
+        for key in ("dec", "dec_rr"):       # contiguous blocks, round-robin tokens
+            for r in range(world):
+                got = out[r][(key, ci)]
+                if r != root:
+                    assert got is None
+                    continue
+                o, l = got
+                np.testing.assert_allclose(o, o_ref[:, :, 0], rtol=0, atol=1e-6)
+                fin = np.isfinite(l_ref[:, :, 0])
+                assert np.array_equal(fin, np.isfinite(l))
+                np.testing.assert_allclose(l[fin], l_ref[:, :, 0][fin], rtol=0, atol=1e-6)
