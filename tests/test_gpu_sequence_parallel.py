@@ -314,3 +314,37 @@ def test_ring_prefill_threads_noncausal():
     for r, (o, l) in enumerate(res):
         compare(o.float().cpu().numpy(), l.cpu().numpy(), o_ref[:, r * hr:(r + 1) * hr],
                 l_ref[:, r * hr:(r + 1) * hr], "bf16", f"ring non-causal rank {r}")
+
+
+def _positions_draws():
+    """12 seeded (B, Hq, Hkv, Sq, Skv, d, q_pos0, k_pos0): half of them large enough for the
+    pair kernel (many heads), half small (persistent KV-split tiles); the offsets mix rows
+    that see no key, some keys and every key."""
+    rng = np.random.default_rng(6060)
+    out = []
+    for i in range(12):
+        big = i % 2 == 0
+        d = int(rng.choice([64, 128]))
+        Hkv = 8 if big else int(rng.choice([1, 2]))
+        G = 8 if big else int(rng.choice([1, 2, 4]))
+        B = 1 if big else int(rng.integers(1, 3))
+        Sq = int(rng.integers(650, 800)) if big else int(rng.integers(1, 400))
+        Skv = int(rng.integers(300, 900)) if big else int(rng.integers(1, 500))
+        k_pos0 = int(rng.integers(0, 1000))
+        # (large draws: at most 100 rows before the first key, so that >= 152 tile pairs remain)
+        q_pos0 = k_pos0 + int(rng.integers(-100, 1500)) if big else int(rng.integers(-300, 1500))
+        out.append((B, Hkv * G, Hkv, Sq, Skv, d, q_pos0, k_pos0))
+    return out
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_positions_random_shapes(i):
+    B, Hq, Hkv, Sq, Skv, d, q_pos0, k_pos0 = _positions_draws()[i]
+    q, k, v = bf16((B, Hq, Sq, d), 700 + i), bf16((B, Hkv, Skv, d), 800 + i), bf16((B, Hkv, Skv, d), 900 + i)
+    scale = d ** -0.5
+    o, lse = gb.attn_fwd_positions(q.cuda(), k.cuda(), v.cuda(), q_pos0, k_pos0, scale=scale)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.attention_at_positions(wl.to_oracle(q), wl.to_oracle(k), wl.to_oracle(v),
+                                                 scale, q_pos0, k_pos0)
+    compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "bf16",
+            f"positions b{B} h{Hq}/{Hkv} s{Sq}x{Skv} d{d} q@{q_pos0} k@{k_pos0}")
