@@ -61,6 +61,7 @@ def test_graph_prefill_replays_with_new_inputs(causal):
 @pytest.mark.parametrize("B,Hq,Hkv,Lmax,ns,lens0,lens1", [
     (4, 64, 8, 9000, 16, [9000, 5000, 1, 4097], [2500, 9000, 0, 64]),   # work queue + combine
     (1, 8, 1, 4096, 8, [4096], [1500]),                               # single launch (one wave)
+    (1, 64, 8, 131072, 0, [131072], [90001]),                         # single launch, 2 CTAs per SM
 ])
 def test_graph_decode_replays_as_the_cache_grows(B, Hq, Hkv, Lmax, ns, lens0, lens1):
     d = 128
