@@ -136,12 +136,13 @@ TIMEOUT_SCRIPT = textwrap.dedent(r"""
     skip.argtypes = [ctypes.c_int, ctypes.c_int]
     skip.restype = ctypes.c_int
     PERSISTENT_PREFILL, MULTITOKEN_DECODE, PAIR_PREFILL, SPLIT_DECODE = 0, 1, 2, 3
+    NSM = torch.cuda.get_device_properties(0).multi_processor_count
     assert skip(7, 0) == gb.GBATTN_ERR_INVALID_ARG and skip(0, -2) == gb.GBATTN_ERR_INVALID_ARG
 
     def prefill(Hq=8, Hkv=2, S=1024, mode="kv_split"):
         w = wl.Workload("dbg-to", "prefill", B=1, Hq=Hq, Hkv=Hkv, d=128, dtype="bf16", Sq=S,
                         Skv=S, causal=True, seed=21)
-        assert gb.attn_prefill_plan(1, Hq, Hkv, S, S, True, 152)["mode"] == mode
+        assert gb.attn_prefill_plan(1, Hq, Hkv, S, S, True, NSM)["mode"] == mode
         q, k, v = wl.prefill_inputs(w)
         o, lse = gb.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=w.scale)
         return w, (q, k, v), o, lse
@@ -152,7 +153,7 @@ TIMEOUT_SCRIPT = textwrap.dedent(r"""
     def split_decode():
         w = wl.Workload("dbg-to-dec", "decode", B=4, Hq=64, Hkv=8, d=128, dtype="bf16", Skv=8192,
                         num_splits=16, len_lo=6000, len_hi=8192, seed=23)
-        assert gb.attn_decode_plan(4, 64, 8, 1, 8192, 128, 16, 152)["merge"] == "combine_per_group"
+        assert gb.attn_decode_plan(4, 64, 8, 1, 8192, 128, 16, NSM)["merge"] == "combine_per_group"
         q, kc, vc, kl = wl.decode_inputs(w)
         o, lse = gb.attn_decode_splitkv(q.cuda(), kc.cuda(), vc.cuda(), kl.cuda(), num_splits=16,
                                         scale=w.scale)
@@ -161,7 +162,7 @@ TIMEOUT_SCRIPT = textwrap.dedent(r"""
     def decode():
         w = wl.Workload("dbg-to-mt", "decode", B=2, Hq=16, Hkv=2, d=128, dtype="bf16", Skv=3000,
                         num_splits=2, len_lo=2500, len_hi=3000, Sq=4, seed=22)
-        assert gb.attn_decode_plan(2, 16, 2, 4, 3000, 128, 2, 152)["kernel"] == "tcgen05"
+        assert gb.attn_decode_plan(2, 16, 2, 4, 3000, 128, 2, NSM)["kernel"] == "tcgen05"
         q, kc, vc, kl = wl.multitoken_inputs(w)
         o, lse = gb.attn_decode_multitoken(q.cuda(), kc.cuda(), vc.cuda(), kl.cuda(),
                                            num_splits=2, scale=w.scale)
