@@ -1017,15 +1017,21 @@ decode_combine_kernel(const __grid_constant__ DecodeParams p) {
     const long long row = piece / kGroups;
     const int cg = (int)(piece % kGroups);
     if (p.counted) {
-        // the block's rows [r0, r1], groups of R rows (R <= 8: the group of a row is row / R)
+        // the block's rows [r0, r1] and their counters: one per 128-row tile of a (sequence, KV
+        // head) group of R rows, counter (row / R) * ceil(R / 128) + (row % R) / 128 (for the
+        // warp-level kernel R <= 8, so simply row / R); a counter is complete once every
+        // partial of its rows has been counted in
         const long long per_row = (long long)kGroups * c;
         const long long r0 = (long long)blockIdx.x * blockDim.x / per_row;
         const long long r1 = min(rows - 1, ((long long)blockIdx.x * blockDim.x + blockDim.x - 1) / per_row);
+        const long long nrt = (p.R + 127) / 128;
         __shared__ int ok;
         if (threadIdx.x == 0) {
             ok = 1;
-            for (long long g = r0 / p.R; g <= r1 / p.R && ok; ++g) {
-                const int n = row_partials(p, (int)(g * p.R / ((long long)p.Hq * p.Tq)));
+            const long long g0 = (r0 / p.R) * nrt + (r0 % p.R) / 128;
+            const long long g1 = (r1 / p.R) * nrt + (r1 % p.R) / 128;
+            for (long long g = g0; g <= g1 && ok; ++g) {
+                const int n = row_partials(p, (int)((g / nrt) * p.R / ((long long)p.Hq * p.Tq)));
                 if (n > 1 && !counter_wait_geq(p.group_cnt + g, n, kErrWaitMerge, p.err)) ok = 0;
             }
         }

@@ -213,8 +213,9 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                     for (int i = 0; i < nrows; ++i)
                         if (GBATTN_IN_BOUNDS((row0 + i) * p.n_parts + part, (long long)p.B * p.Hq * p.Tq * p.n_parts, p.err))
                             p.ws_lse[(row0 + i) * p.n_parts + part] = -INFINITY;
-                    if (p.counted && GBATTN_IN_BOUNDS((long long)b * p.Hkv + kvh, (long long)p.B * p.Hkv, p.err))
-                        counter_add_release(p.group_cnt + (long long)b * p.Hkv + kvh, 1);
+                    const long long g = ((long long)b * p.Hkv + kvh) * p.n_rt + rt;
+                    if (p.counted && GBATTN_IN_BOUNDS(g, (long long)p.B * p.Hkv * p.n_rt, p.err))
+                        counter_add_release(p.group_cnt + g, 1);
                 }
                 __syncwarp();
                 continue;
@@ -446,7 +447,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
         }
     } else if (warp == 3) {
         // ================================ publisher =================================
-        // Counts each finished partial into its (sequence, KV head) group with a device-scope
+        // Counts each finished partial into its (sequence, KV head, 128-row tile) group with a device-scope
         // release, so that the combine, which reads the count with acquire, can merge the group
         // while the grid is still running.  The softmax warps' writes of the partial happen
         // before their arrivals here (CTA-scope mbarrier release / acquire), so the release
@@ -457,7 +458,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                 if (!mbar_wait(&pub_full[ps], (k / kPubSlots) & 1, kErrWaitConsumer, p.err)) break;
                 const int g = pub_group[ps];
                 if (g < 0) break;                    // the softmax warps are done
-                if (GBATTN_IN_BOUNDS(g, (long long)p.B * p.Hkv, p.err))
+                if (GBATTN_IN_BOUNDS(g, (long long)p.B * p.Hkv * p.n_rt, p.err))
                     counter_add_release(p.group_cnt + g, 1);
                 mbar_arrive(&pub_empty[ps]);
             }
@@ -579,7 +580,7 @@ decode_mt_kernel(const __grid_constant__ DecodeTcParams p) {
                 // counted; claimed before the meet, so no warp arrives on it earlier
                 if (p.counted && warp == kSoftmaxWarp0) {
                     if (mbar_wait(&pub_empty[k % kPubSlots], ((k / kPubSlots) & 1) ^ 1u, kErrWaitSoftmax, p.err))
-                        pub_group[k % kPubSlots] = it.b * p.Hkv + it.kvh;
+                        pub_group[k % kPubSlots] = (it.b * p.Hkv + it.kvh) * p.n_rt + it.rt;
                 }
                 mbar_arrive(merge_bar);
             }
@@ -673,7 +674,8 @@ cudaError_t launch_mt(const DecodeTcParams& p, int nsm, cudaStream_t stream) {
     cudaError_t err = cudaFuncSetAttribute(decode_mt_kernel<D>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    err = cudaMemsetAsync(p.counter, 0, (p.counted ? 1 + (size_t)p.B * p.Hkv : 1) * sizeof(int), stream);
+    err = cudaMemsetAsync(p.counter, 0, (p.counted ? 1 + (size_t)p.B * p.Hkv * p.n_rt : 1) * sizeof(int),
+                          stream);
     if (err != cudaSuccess) return err;
     decode_mt_kernel<D><<<min(p.n_items, nsm), kThreads, smem, stream>>>(p);
     return cudaGetLastError();

@@ -374,9 +374,9 @@ DecodePlan decode_plan(int B, int Hq, int Hkv, int Tq, int Lmax, int num_splits,
     // its count is complete, overlapping the split kernel's last items, instead of waiting
     // for the whole split grid (that wait and the combine after it cost about 6 us on
     // workload 4)
-    // The tcgen05 kernel counts the same way when a KV head's rows fit one 128-row tile (its
-    // items then cover a whole group), through its otherwise idle fourth warp.
-    pl.counted = pl.tc ? pl.n_rt == 1 : (!pl.fused && pl.dr.nci == 1);
+    // The tcgen05 kernel counts the same way, per (sequence, KV head, 128-row tile), through its
+    // otherwise idle fourth warp.
+    pl.counted = pl.tc || (!pl.fused && pl.dr.nci == 1);
     pl.combine_lanes = 1;
     while (pl.combine_lanes * 8 < pl.n_slots * pl.pieces) pl.combine_lanes *= 2;   // <= 256 partials: at most 32
     return pl;

@@ -138,9 +138,9 @@ struct DecodeTcParams {
     int auto_floor;       // automatic mode: split count that fills the GPU (see splits_for)
     int n_items;          // n_slots * pieces * B * Hkv * n_rt
     int* counter;         // work queue counter (zeroed before the kernel)
-    int* group_cnt;       // [B, Hkv] finished partials per (sequence, KV head), when counted
-    int counted;          // 1 (one 128-row tile per KV head): each item's partial is counted
-                          // into group_cnt, and the combine merges a group once it is complete
+    int* group_cnt;       // [B, Hkv, n_rt] finished partials per (sequence, KV head, row tile)
+    int counted;          // 1: each item's partial is counted into group_cnt, and the combine
+                          // merges a row tile's rows once their count is complete
     float scale_log2;
     int* err;
 };

@@ -84,17 +84,16 @@ def prefill_shapes(nsm: int):
 DECODE_DRAWS = 6
 DECODE_KINDS = ("single_launch", "single_launch+two_per_sm", "combine_per_group",
                 "combine_per_group+pieces", "mt:single_launch", "mt:combine",
-                "mt:tcgen05+combine_per_group", "mt:tcgen05+combine")
+                "mt:tcgen05", "mt:tcgen05+row_tiles")
 
 
 def decode_kind(Tq: int, plan: dict, nsm: int) -> str:
     """Single-token calls merge in the split kernel (single launch: one CTA per SM in one
     wave, two per SM with more items than SMs) or per group (with or without pieces);
-    multi-token calls (mt:) run the warp kernel with either merge, or the tcgen05 kernel with
-    the per-group combine (one 128-row tile per KV head) or the combine that waits for the
-    grid (more rows)."""
+    multi-token calls (mt:) run the warp kernel with either merge, or the tcgen05 kernel (its
+    partials counted per 128-row tile; one tile per KV head, or several)."""
     if plan["kernel"] == "tcgen05":
-        k = "tcgen05+" + plan["merge"]
+        k = "tcgen05" + ("+row_tiles" if plan["rows_per_kv_head"] > 128 else "")
     else:
         k = plan["merge"] + ("+pieces" if plan["pieces"] > 1 else "")
         if Tq == 1 and plan["merge"] == "single_launch" and plan["items"] > nsm:

@@ -83,11 +83,10 @@ def test_kernel_choice_by_rows_per_kv_head():
     assert dec(4, 32, 8, 3, 32768, 16)["kernel"] == "tcgen05"             # 12 rows, 2048 keys
     p = dec(1, 32, 8, 3, 8192, 0)                                         # 12 rows, 19 x 431 keys
     assert p["kernel"] == "warp" and p["splits"] == 19
-    # the tcgen05 kernel counts its partials per group when a KV head's rows fit one 128-row
-    # tile; with more rows the combine waits for the whole grid
+    # the tcgen05 kernel counts its partials per (sequence, KV head, 128-row tile)
     assert dec(1, 64, 8, 4, 4096, 0)["merge"] == "combine_per_group"     # 32 rows
     p = dec(2, 16, 2, 20, 1300, 3)                                        # 160 rows: 2 tiles
-    assert p["kernel"] == "tcgen05" and p["merge"] == "combine"
+    assert p["kernel"] == "tcgen05" and p["merge"] == "combine_per_group"
 
 
 def test_combine_lanes_cover_every_split():
@@ -178,11 +177,10 @@ def test_plan_agrees_with_workspace_size_and_invariants():
         if p["merge"] == "single_launch":
             assert p["pieces"] == 1
         if p["merge"] == "combine_per_group":
-            # the warp kernel with one row chunk per KV head, or the tcgen05 kernel with one
-            # 128-row tile per KV head
-            assert (p["kernel"] == "warp" and G * Tq <= 8) or (p["kernel"] == "tcgen05" and G * Tq <= 128)
+            # the warp kernel with one row chunk per KV head, or the tcgen05 kernel
+            assert (p["kernel"] == "warp" and G * Tq <= 8) or p["kernel"] == "tcgen05"
         if p["kernel"] == "tcgen05":
-            assert p["merge"] == ("combine_per_group" if G * Tq <= 128 else "combine")
+            assert p["merge"] == "combine_per_group"
         if p["kernel"] == "warp" and G * Tq <= 8:
             assert p["merge"] in ("single_launch", "combine_per_group")
         if p["merge"] == "single_launch":
