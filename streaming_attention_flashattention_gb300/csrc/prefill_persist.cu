@@ -165,6 +165,23 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
         mbar_init(mma_idle, 1);
         mbar_init(staged, 8);
         fence_barrier_init();
+        // the first tile's Q and first K tile go out now, under the TMEM allocation and the
+        // block barrier (this thread initialised the barriers they complete on)
+        QTile it0;
+        if (tile_of(p, 0, it0)) {
+            mbar_arrive_expect_tx(q_full, L::kTileBytes);
+            #pragma unroll
+            for (int bx = 0; bx < L::kBoxes; ++bx)
+                tma_load_3d(smem + L::kQ0 + bx * L::kBoxBytes, &p.tmap_q, bx * 64, it0.q0,
+                            it0.b * p.Hq + it0.h, q_full);
+            if (it0.n > 0) {
+                mbar_arrive_expect_tx(&k_full[0], L::kTileBytes);
+                #pragma unroll
+                for (int bx = 0; bx < L::kBoxes; ++bx)
+                    tma_load_3d(smem + L::kK0 + bx * L::kBoxBytes, &p.tmap_k, bx * 64, 0,
+                                it0.b * p.Hkv + it0.h / p.G, &k_full[0]);
+            }
+        }
     }
     if (warp == 1) tmem_alloc(tmem_slot, L::kTmemCols);
     tc_fence_before();
@@ -185,13 +202,16 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
 #endif
             QTile it;
             for (; ok && tile_of(p, k, it); ++k) {
-                // Q once the previous tile's last S product has read the buffer
-                if (k > 0 && !(ok = mbar_wait(q_empty, (k - 1) & 1, kErrWaitProducer, p.err))) break;
-                mbar_arrive_expect_tx(q_full, L::kTileBytes);
-                #pragma unroll
-                for (int bx = 0; bx < L::kBoxes; ++bx)
-                    tma_load_3d(smem + L::kQ0 + bx * L::kBoxBytes, &p.tmap_q, bx * 64, it.q0,
-                                it.b * p.Hq + it.h, q_full);
+                // Q once the previous tile's last S product has read the buffer (the first
+                // tile's Q went out before the block barrier)
+                if (k > 0) {
+                    if (!(ok = mbar_wait(q_empty, (k - 1) & 1, kErrWaitProducer, p.err))) break;
+                    mbar_arrive_expect_tx(q_full, L::kTileBytes);
+                    #pragma unroll
+                    for (int bx = 0; bx < L::kBoxes; ++bx)
+                        tma_load_3d(smem + L::kQ0 + bx * L::kBoxBytes, &p.tmap_q, bx * 64, it.q0,
+                                    it.b * p.Hq + it.h, q_full);
+                }
                 const int n0 = (it.n + 1) / 2, n1 = it.n - n0;
                 const int zkv = it.b * p.Hkv + it.h / p.G;
                 for (int j = 0; j < n0 && ok; ++j) {
@@ -199,6 +219,10 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
                         if (t == 1 && j >= n1) continue;
                         const int tile = t == 0 ? j : n0 + j;
                         const uint32_t ks = nf % KS, kph = (nf / KS) & 1;
+                        if (nf == 0) {              // went out before the block barrier
+                            ++nf;
+                            continue;
+                        }
                         if (!(ok = mbar_wait(&k_empty[ks], kph ^ 1u, kErrWaitProducer, p.err))) break;
 #ifdef GBATTN_DEBUG_CHECKS
                         if (blockIdx.x == 0 && (int)nf == g_skip_k_fill) {
