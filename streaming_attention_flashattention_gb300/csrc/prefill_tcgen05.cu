@@ -163,6 +163,9 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
         if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     const int n_kv_max = max(td[0].n_kv, td[1].n_kv);
+    // the first K/V fill (the one the producer loop below starts with) exists: it goes out
+    // before the block barrier, with Q
+    const bool early_kv = kSplit ? td[0].n_kv > 0 : n_kv_max > 0;
     // K ring slot of fill f: with KV split, slot 0 is the unused second Q buffer
     auto k_slot = [&](uint32_t f) -> uint8_t* {
         const uint32_t ks = f % KS;
@@ -187,6 +190,31 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
             mbar_init(&o_done[i], 1);
         }
         fence_barrier_init();
+        // Q and the first K and V tiles go out now, under the TMEM allocation and the block
+        // barrier (this thread initialised the barriers they complete on)
+        const int nq = kSplit ? 1 : (td[1].present ? 2 : 1);
+        mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
+        #pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (t >= nq) continue;
+            #pragma unroll
+            for (int bx = 0; bx < L::kBoxes; ++bx)
+                tma_load_3d(smem + L::kQ0 + t * L::kTileBytes + bx * L::kBoxBytes, &p.tmap_q,
+                            bx * 64, td[t].q0, b * p.Hq + td[t].h, q_full);
+        }
+        if (early_kv) {
+            const int tile0 = kSplit ? td[0].kv0 : 0;
+            mbar_arrive_expect_tx(&k_full[0], L::kTileBytes);
+            #pragma unroll
+            for (int bx = 0; bx < L::kBoxes; ++bx)
+                tma_load_3d(k_slot(0) + bx * L::kBoxBytes, &p.tmap_k, bx * 64, tile0 * kBlockN,
+                            b * p.Hkv + kvh, &k_full[0]);
+            mbar_arrive_expect_tx(&v_full[0], L::kTileBytes);
+            #pragma unroll
+            for (int bx = 0; bx < L::kBoxes; ++bx)
+                tma_load_3d(smem + L::kV0 + bx * L::kBoxBytes, &p.tmap_v, bx * 64, tile0 * kBlockN,
+                            b * p.Hkv + kvh, &v_full[0]);
+        }
     }
     if (warp == 1) tmem_alloc(tmem_slot, L::kTmemCols);
     tc_fence_before();
@@ -200,17 +228,8 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
             prefetch_tensormap(&p.tmap_q);
             prefetch_tensormap(&p.tmap_k);
             prefetch_tensormap(&p.tmap_v);
-            // one Q tile per slot (pairs), or one Q tile for both slots (KV split)
-            const int nq = kSplit ? 1 : (td[1].present ? 2 : 1);
-            mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
-            #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                if (t >= nq) continue;
-                #pragma unroll
-                for (int bx = 0; bx < L::kBoxes; ++bx)
-                    tma_load_3d(smem + L::kQ0 + t * L::kTileBytes + bx * L::kBoxBytes, &p.tmap_q,
-                                bx * 64, td[t].q0, b * p.Hq + td[t].h, q_full);
-            }
+            // (Q -- one tile per slot for pairs, one for both slots with KV split -- and the
+            // first K and V tiles went out before the block barrier)
             // K/V fills in the order the MMA issuer consumes them: one per KV step for
             // pairs (shared by both slots), slot 0 then slot 1 per step with KV split
             const int zkv = b * p.Hkv + kvh;
@@ -225,6 +244,11 @@ prefill_fwd_kernel(const __grid_constant__ PrefillParams p) {
                     if (!kSplit && t == 1) break;
                     if (kSplit && j >= td[t].n_kv) continue;
                     const int tile = kSplit ? td[t].kv0 + j : j;
+                    if (nf == 0 && early_kv) {   // fill 0 of K and V went out before the barrier
+                        ++nf;
+                        ++nfv;
+                        continue;
+                    }
                     const uint32_t ks = nf % KS, kph = (nf / KS) & 1;
                     if (!mbar_wait(&k_empty[ks], kph ^ 1u, kErrWaitProducer, p.err)) { ok = false; break; }
 #ifdef GBATTN_DEBUG_CHECKS
