@@ -144,6 +144,11 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // the first tile exists and has KV tiles: its Q and its first K (and V) tile go out before the
+    // block barrier, from the thread that initialises the barriers
+    QTile it0;
+    const bool early_q = tile_of(p, 0, it0);
+    const bool early_kv = early_q && it0.n > 0;
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
@@ -167,14 +172,13 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
         fence_barrier_init();
         // the first tile's Q and first K tile go out now, under the TMEM allocation and the
         // block barrier (this thread initialised the barriers they complete on)
-        QTile it0;
-        if (tile_of(p, 0, it0)) {
+        if (early_q) {
             mbar_arrive_expect_tx(q_full, L::kTileBytes);
             #pragma unroll
             for (int bx = 0; bx < L::kBoxes; ++bx)
                 tma_load_3d(smem + L::kQ0 + bx * L::kBoxBytes, &p.tmap_q, bx * 64, it0.q0,
                             it0.b * p.Hq + it0.h, q_full);
-            if (it0.n > 0) {
+            if (early_kv) {
                 mbar_arrive_expect_tx(&k_full[0], L::kTileBytes);
                 #pragma unroll
                 for (int bx = 0; bx < L::kBoxes; ++bx)
@@ -219,7 +223,7 @@ prefill_persist_kernel(const __grid_constant__ PrefillParams p) {
                         if (t == 1 && j >= n1) continue;
                         const int tile = t == 0 ? j : n0 + j;
                         const uint32_t ks = nf % KS, kph = (nf / KS) & 1;
-                        if (nf == 0) {              // went out before the block barrier
+                        if (nf == 0 && early_kv) {  // went out before the block barrier
                             ++nf;
                             continue;
                         }
